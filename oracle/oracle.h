@@ -1,0 +1,209 @@
+/*
+ * oracle.h -- plain, slow CPU checker for the sharded mixed-precision AdamW step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library; the product path never does.
+ * It shares no code with the CUDA library: its only shared dependency is the
+ * seeded input generator (synth.h), which holds none of the step's arithmetic.
+ *
+ * Pages cited (title, then section):
+ *   [ZF]  "Training models too big for one GPU: ZeRO & FSDP"
+ *   [SR]  "Stop Replicating What You Can Shard: ZeRO and FSDP"
+ *   [TM]  "The redundancy hiding in data parallelism" (transformer math: ZeRO)
+ *   [Z3]  "ZeRO Stage 3 Math"
+ *   [SB]  "How far does splitting the batch get you?" (interrogating
+ *         parallelism, part 2: splitting the batch)
+ *
+ * Floating point: the pages fix fp32 for the master weights, Adam moments and
+ * the gradient reduction, and bf16/fp16 for gradients and working weights, so
+ * the checker computes in those precisions, one IEEE round-to-nearest-even
+ * operation per C statement (built with -ffp-contract=off, no fast-math).
+ * Quantities the pages leave to accounting (bills, norms) are fp64.
+ *
+ * Parity status per function is listed beside each declaration; every
+ * function here is pinned by a CPU test (closed forms, printed worked
+ * examples, invariants, exhaustive comparison, brute force).
+ */
+#ifndef ZERO_ORACLE_H
+#define ZERO_ORACLE_H
+
+#include <stdint.h>
+#include "synth.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- plan ---- */
+
+typedef struct orc_segment {
+  int64_t lo, hi;      /* flat element range [lo, hi) */
+  int32_t rank;        /* owner: rank whose 1/N slice contains the range */
+  int32_t bucket;      /* bucket containing the range */
+} orc_segment;
+
+typedef struct orc_plan {
+  int64_t psi;         /* total parameters (sum of tensor sizes) */
+  int64_t pad;         /* zeros appended so that psi_pad is a multiple of n_ranks */
+  int64_t psi_pad;
+  int64_t shard;       /* psi_pad / n_ranks: elements each rank owns */
+  int64_t bucket_elems;/* bucket size in elements, 0 = one bucket */
+  int32_t n_ranks;
+  int32_t n_buckets;
+  int32_t n_segments;
+  int32_t reserved;
+  /* per-device model-state bytes, K = 12 (mixed-precision Adam) */
+  double bill_ddp, bill_z1, bill_z2, bill_z3;
+  /* ring all-reduce of 2*psi bytes of 16-bit gradients */
+  double ring_bytes_per_rank; /* 2(d-1)M/d */
+  double ring_hops;           /* 2(d-1) */
+  /* communication volume per step in elements */
+  double comm_ddp, comm_z1, comm_z2, comm_z3;
+} orc_plan;
+
+/* Flatten a tensor list, pad to a multiple of N, shard, bucket.
+ * [ZF] "FSDP: the same idea, one unit at a time" (parameters flattened and
+ * sharded); [ZF] "ZeRO stages 1, 2 and 3" (GPU i updates its 1/N slice);
+ * [SB] "How does the collective hide behind the backward pass?" (buckets).
+ * offsets: n_tensors entries or NULL. segs: capacity seg_cap or NULL.
+ * Returns 0; -1 on invalid arguments; -2 if seg_cap is too small
+ * (out->n_segments then holds the count needed). */
+int orc_plan_make(const int64_t* numels, int32_t n_tensors, int32_t n_ranks,
+                  int64_t bucket_elems, orc_plan* out, int64_t* offsets,
+                  orc_segment* segs, int32_t seg_cap);
+
+/* Model-state bytes per device for psi parameters, K = 12.
+ * [ZF] "The memory bill: 16 bytes per parameter", "ZeRO stages 1, 2 and 3";
+ * [TM] "The per-stage memory formula and a worked example";
+ * [Z3] "Stage 3: divide everything by N". out[0..3] = DDP, Z1, Z2, Z3. */
+void orc_bills(double psi, int32_t n_ranks, double out[4]);
+
+/* Bytes each rank sends in a ring all-reduce of m_bytes over d ranks:
+ * 2(d-1)M/d. [SB] "Why does the all-reduce not get more expensive with more
+ * ranks?"; [ZF] "Data parallelism and the all-reduce". */
+double orc_ring_bytes(double m_bytes, int32_t d);
+
+/* --------------------------------------------------------------- casts ---- */
+/* IEEE 754 binary16 and bfloat16 (fp32 with the mantissa cut to 7 bits),
+ * round to nearest, ties to even; overflow to infinity; subnormals kept.
+ * [ZF] "How a computer stores real numbers" (format table) and
+ * "Mixed-precision training" (the fp32 master is rounded to half). */
+uint16_t orc_f32_to_f16(float x);
+float orc_f16_to_f32(uint16_t h);
+uint16_t orc_f32_to_bf16(float x);
+float orc_bf16_to_f32(uint16_t h);
+void orc_cast_array(const float* in, uint16_t* out, int64_t n, int32_t is_bf16);
+void orc_widen_array(const uint16_t* in, float* out, int64_t n, int32_t is_bf16);
+
+/* --------------------------------------------------- step building blocks ---- */
+
+typedef struct orc_hparams {
+  double lr, beta1, beta2, eps, weight_decay;
+  double max_grad_norm;     /* <= 0: no clipping */
+  int32_t dynamic_scale;    /* 1: halve on overflow, double after growth_interval good steps */
+  int32_t growth_interval;
+} orc_hparams;
+
+typedef struct orc_scaler {
+  float scale;              /* loss scale S */
+  int32_t good_steps;       /* consecutive good steps since the last change */
+  int32_t t;                /* applied optimizer steps */
+  int32_t overflow;         /* 1 if the last step was skipped */
+  double norm_sq, norm;     /* last global gradient norm (clip configs) */
+  float clip_coef;          /* coefficient applied in the last step (1 = none) */
+  int32_t reserved;
+} orc_scaler;
+
+typedef struct orc_adam_scalars {
+  float b1, omb1, b2, omb2; /* beta1, 1-beta1, beta2, 1-beta2 rounded from fp64 */
+  float bc1, bc2;           /* 1 - beta^t rounded from fp64, beta^t by t products */
+  float lr, decay, eps;     /* decay = 1 - lr*weight_decay rounded from fp64 */
+} orc_adam_scalars;
+
+/* Sum of the N replicas' values of one element in ring order for owner i:
+ * ranks i+1, i+2, ..., N-1, 0, ..., i, fp32 accumulation.
+ * [SB] "Why does the all-reduce not get more expensive with more ranks?"
+ * (a chunk walks the ring, summed hop by hop, and is complete at rank i after
+ * d-1 hops); [SB] "What does gradient accumulation actually buy?" (fp32
+ * reduce-scatter). vals[r] is rank r's value widened to fp32. */
+float orc_ring_sum(const float* vals, int32_t n_ranks, int32_t owner);
+
+/* fp32(1 / (S * N)): divide by the loss scale ([ZF] "Mixed-precision
+ * training") and average over the N replicas ([ZF] "Data parallelism and the
+ * all-reduce"). */
+float orc_unscale_factor(float scale, int32_t n_ranks);
+
+/* Adam scalars for optimizer step t (t >= 1). [ZF] "Adam, and why it's
+ * expensive" (bias corrections 1 - beta^t). */
+orc_adam_scalars orc_adam_scalars_make(const orc_hparams* hp, int32_t t);
+
+/* One AdamW update of one element ([ZF] "Adam, and why it's expensive":
+ * moments, bias correction, eps outside the square root; decoupled weight
+ * decay as named there): m = b1*m + (1-b1)*g; v = b2*v + (1-b2)*(g*g);
+ * mh = m/bc1; vh = v/bc2; u = mh/(sqrt(vh)+eps); theta = theta*decay;
+ * theta = theta - lr*u. */
+void orc_adamw_elem(float* theta, float* m, float* v, float g, const orc_adam_scalars* a);
+
+/* Clip coefficient from the global sum of squares: c = max_norm/(sqrt(nsq)+1e-6),
+ * applied (rounded to fp32) only when c < 1. Returns 1 if it applies. */
+int32_t orc_clip_coef(double norm_sq, double max_norm, float* coef, double* norm);
+
+/* Loss-scale bookkeeping after a step ([ZF] "Mixed-precision training": pick
+ * S dynamically, skip a step on overflow). Overflow: no state change, t kept,
+ * S halved (floor 1) when dynamic, good_steps reset. Otherwise t += 1,
+ * good_steps += 1 and S doubles after growth_interval good steps when
+ * dynamic. */
+void orc_scaler_finish(orc_scaler* s, const orc_hparams* hp, int32_t overflow);
+
+/* ------------------------------------------------------ whole-step drivers ---- */
+
+/* One full step on explicit host arrays, for owners [rank_lo, rank_hi).
+ * replicas[r][j - wbase] is rank r's 16-bit gradient of flat element j;
+ * master/m/v/params/ghat are indexed by j - wbase as well.
+ * Processes flat elements [rank_lo*S, rank_hi*S) in ascending order:
+ *   reduce (ring order, fp32) -> unscale -> non-finite flag per bucket ->
+ *   if any flag: skip (nothing written, scaler updated) ->
+ *   optional clip (global L2 norm over the processed elements) ->
+ *   AdamW on the fp32 master/m/v -> cast to the 16-bit working copy.
+ * bucket_flags (n_buckets, may be NULL) are OR-ed. ghat (may be NULL)
+ * receives the unscaled, unclipped reduced gradient.
+ * Norm: squares summed in fp64 in ascending element order within fixed
+ * chunks of 2^20 elements (counted from rank_lo*S), chunk sums added in
+ * ascending order. Returns 0, or -1 on bad arguments. */
+int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t is_bf16,
+                    const uint16_t* const* replicas, int64_t wbase, float* master,
+                    float* m, float* v, uint16_t* params, float* ghat,
+                    uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc);
+
+/* Input recipe for the generator-driven driver: replica r's element j at
+ * step s is cast16(zs_grad_value(spec with loss_scale = current S, s, r, j)),
+ * except one optional injected 16-bit pattern. */
+typedef struct orc_gen {
+  zs_grad_spec spec;
+  int32_t is_bf16;
+  int32_t inject_step;      /* < 0: no injection */
+  int32_t inject_rank;
+  uint32_t inject_bits;     /* 16-bit pattern written at (inject_step, inject_rank, inject_elem) */
+  int64_t inject_elem;
+} orc_gen;
+
+/* One full step at any size without storing replicas: regenerates every
+ * replica value on the fly (n_threads workers over the fixed 2^20-element
+ * chunks, results combined in chunk order, so the output does not depend on
+ * n_threads). Applies the update only to the sampled flat elements
+ * elems[0..n_elems) (ascending, inside [rank_lo*S, rank_hi*S)), whose states
+ * master/m/v/params are given as arrays of length n_elems. Global results
+ * (flags, overflow, norm) cover all processed elements. */
+int orc_gen_step(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, const orc_gen* g,
+                 uint32_t step, int32_t n_threads, const int64_t* elems, int64_t n_elems,
+                 float* master, float* m, float* v, uint16_t* params,
+                 uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc);
+
+/* Reduced, unscaled gradient at sampled elements, regenerated (no clip). */
+int orc_gen_ghat(const orc_plan* p, const orc_gen* g, uint32_t step, float scale,
+                 const int64_t* elems, int64_t n_elems, float* ghat);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_ORACLE_H */
