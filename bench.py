@@ -1,0 +1,468 @@
+#!/usr/bin/env python3
+"""Benchmark of the per-shard ZeRO step of mixed-precision AdamW on GB300.
+
+One step = the whole hot path over one batch of synthetic gradients:
+reduce-scatter of N resident replicas in ring order with fp32 accumulation,
+unscale, non-finite vote, (clip for clip workloads), AdamW on the fp32
+master/m/v shard, cast to the 16-bit working copy, loss-scale bookkeeping.
+
+Default workload: GPT-2-small tensor list (124,439,808 parameters), N = 8
+simulated ranks, 25M-element buckets, bf16 gradients, fused single pass.
+
+Prints ONE JSON line (rank 0). `value` is Gparams/s of the whole job with
+inputs resident in HBM; `e2e` is the same metric through the C ABI with the
+replicas copied from pinned host memory and the updated parameters read
+back every step; `roofline` is the dominant kernel's algorithmic HBM bytes
+per launch over its CUDA-event duration against the measured copy
+bandwidth; `cpu_baseline` is the CPU checker timed on a bounded sample.
+
+`--impl reference` times the CPU checker (the only reference that exists
+for this path) on the host cores, same workload, metric and unit.
+Multi-GPU (torchrun): every rank runs an independent replica group on its
+own GPU (no collective on the data path), timing is max over ranks and
+`value` sums the ranks' work ("scaling": "weak").
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded AdamW step Gparams/s; achieved HBM GB/s as % of GB300 peak"
+UNIT = "Gparams/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="libzero", choices=["libzero", "reference"])
+    ap.add_argument("--workload", default="gpt2_small",
+                    choices=["tiny_flat", "gpt2_small", "flat_1p5b", "stage3_slice", "llama_2b"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def workload(name):
+    from fsdp_sharded_mixed_shard_gb300 import workloads as W
+    return {"tiny_flat": W.TINY_FLAT, "gpt2_small": W.GPT2_SMALL, "flat_1p5b": W.FLAT_1P5B,
+            "stage3_slice": W.STAGE3_SLICE, "llama_2b": W.LLAMA_2B}[name]
+
+
+def psi_step(wl):
+    """Parameters one step updates: the whole psi, or the owned slices."""
+    from fsdp_sharded_mixed_shard_gb300 import workloads as W  # noqa: F401
+    lo, hi = wl.ranks
+    if (lo, hi) == (0, wl.n_ranks):
+        return wl.psi
+    n = wl.n_ranks
+    S = (wl.psi + (-wl.psi) % n) // n
+    return min(hi * S, wl.psi) - min(lo * S, wl.psi)
+
+
+def config_of(wl, path):
+    psip = wl.psi + (-wl.psi) % wl.n_ranks
+    lo, hi = wl.ranks
+    S = psip // wl.n_ranks
+    step_gb = (2 * wl.n_ranks + (34 if path == "two_pass" else 26)) * psi_step(wl) / 1e9
+    return {"workload": wl.name, "psi": wl.psi, "psi_step": psi_step(wl),
+            "n_ranks": wl.n_ranks, "owners": [lo, hi], "shard_elems": S,
+            "bucket_elems": wl.bucket_elems, "grad_dtype": "bf16" if wl.is_bf16 else "fp16",
+            "path": path, "clip": wl.max_grad_norm,
+            "l2": "inputs larger than L2 (%.1f GB of HBM traffic per step, L2 129 MB)" % step_gb}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    p = os.path.join(ROOT, "fsdp_sharded_mixed_shard_gb300", "csrc", "zero_kernels.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel, wl_name):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (line: `traffic: kernel=<k> workload=<w>
+    bytes_per_launch=<b> source_sha=<sha>`); otherwise None."""
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    sha = kernel_source_sha()
+    pat = re.compile(r"traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=([0-9.eE+]+)"
+                     r"\s+source_sha=(\w+)")
+    for f in sorted(os.listdir(d)):
+        if not f.endswith((".md", ".txt")):
+            continue
+        for m in pat.finditer(open(os.path.join(d, f)).read()):
+            if m.group(1) == kernel and m.group(2) == wl_name and m.group(4) == sha:
+                return float(m.group(3))
+    return None
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((float(parts[2]), float(parts[3]), float(parts[4]), parts[5:10]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ libzero arm ----
+
+def run_libzero(args, rank, world, dist):
+    import torch
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    from fsdp_sharded_mixed_shard_gb300 import harness
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workload(args.workload)
+    g = harness.Group(wl, device=dev)
+    path = "two_pass" if g.two_pass else "fused"
+    g.init_state()
+    g.gen_grads(1)
+    torch.cuda.synchronize()
+    st = g.sptr
+    N = wl.n_ranks
+    lo, hi = wl.ranks
+    reps = g.rep_ptrs()
+    m, v, w = g._state_ptrs(0), g._state_ptrs(1), g._state_ptrs(2)
+    sc, fl, flat = g.scaler.data_ptr(), g.flags.data_ptr(), g.flat.data_ptr()
+    ws = g.workspace.data_ptr()
+    clip = wl.max_grad_norm > 0
+    gp = g.ghat_ptrs() if g.two_pass else None
+
+    # phases of one step (each a C-ABI call on stream st); for the fused path
+    # the update is one kernel launch per 128 segments
+    def phases():
+        if not g.two_pass:
+            return [("fused_update", lambda: Z.zero_step_update(
+                        g.plan, lo, hi, m, v, w, 2, None, reps, g.wbase, flat, g.hp, sc, fl, st)),
+                    ("finish", lambda: Z.zero_step_finish(
+                        g.plan, lo, hi, m, 2, None, g.wbase, flat, g.hp, sc, st))]
+        out = [("reduce_scatter", lambda: Z.zero_reduce_scatter(
+                    g.plan, -1, lo, hi, reps, g.wbase, gp, sc, fl, ws if clip else 0, st))]
+        if clip:
+            out.append(("grad_norm", lambda: Z.zero_grad_norm(g.plan, lo, hi, None, g.hp, sc, ws,
+                                                              st)))
+        out += [("update", lambda: Z.zero_step_update(
+                    g.plan, lo, hi, m, v, w, 1, gp, None, g.wbase, flat, g.hp, sc, fl, st)),
+                ("finish", lambda: Z.zero_step_finish(
+                    g.plan, lo, hi, m, 1, gp, g.wbase, flat, g.hp, sc, st))]
+        return out
+
+    ph = phases()
+    segs = g.info.n_segments if (lo, hi) == (0, N) else None
+    if segs is None:
+        segs = sum(1 for s in Z.zero_plan_segments(g.plan) if lo <= s[2] < hi)
+    L = -(-segs // 128)
+    launches_per_step = (2 * L + 1) if not g.two_pass else (L + (1 if clip else 0) + L + 1)
+
+    for _ in range(args.warmup):
+        for _, f in ph:
+            f()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)] for name, _ in ph}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if uuid and not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
+    t0.record(g.stream)
+    for k in range(K):
+        for name, f in ph:
+            a, b = evs[name][k]
+            a.record(g.stream)
+            f()
+            b.record(g.stream)
+    t1.record(g.stream)
+    torch.cuda.synchronize()
+    wall = time.time() - wall0
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    phase_ms = {name: statistics.mean(a.elapsed_time(b) for a, b in evs[name]) for name, _ in ph}
+
+    # max over ranks of the timed region
+    if dist:
+        tt = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / K
+    pstep = psi_step(wl)
+    value = pstep * K * world / (total_ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel
+    peak, peak_kind = peaks()
+    bytes_per_param = {"fused_update": 2 * N + 26, "reduce_scatter": 2 * N + 4,
+                       "update": 30, "grad_norm": 0, "finish": 0}
+    dom = max((n for n, _ in ph if bytes_per_param[n] > 0), key=lambda n: phase_ms[n])
+    alg_bytes = bytes_per_param[dom] * pstep
+    achieved = alg_bytes / (phase_ms[dom] / 1e3) / 1e9
+    kernel_name = {"fused_update": "step_kernel<kFused>", "reduce_scatter": "step_kernel<kReduce>",
+                   "update": "step_kernel<kUpdate>"}[dom]
+    traffic = profiled_traffic(kernel_name, wl.name)
+    step_bytes = (2 * N + (34 if g.two_pass else 26)) * pstep
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_kind": peak_kind + " (copy bandwidth, burst)",
+                "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
+                "kernel_ms": round(phase_ms[dom], 4),
+                "step_bytes_per_param": step_bytes / pstep,
+                "step_achieved_gbs": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
+                "step_frac": round(step_bytes / (ms_per_step / 1e3) / 1e9 / peak, 4),
+                "north_star_frac_2n26": round((2 * N + 26) * pstep / (ms_per_step / 1e3) / 1e9
+                                              / peak, 4)}
+
+    # end to end through the C ABI: replicas from pinned host memory, updated
+    # parameters and scaler read back every step
+    E = max(1, min(args.e2e_steps, K))
+    host_reps = torch.empty(g.replicas.shape, dtype=torch.int16, pin_memory=True)
+    host_reps.copy_(g.replicas)
+    host_params = torch.empty(g.flat.shape, dtype=torch.int16, pin_memory=True)
+    host_scaler = torch.empty(g.scaler.shape, dtype=torch.uint8, pin_memory=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    with torch.cuda.stream(g.stream):
+        e0.record(g.stream)
+        for _ in range(E):
+            g.replicas.copy_(host_reps, non_blocking=True)
+            if not g.two_pass:
+                Z.zero_step(g.plan, lo, hi, m, v, w, 2, None, reps, g.wbase, flat, g.hp, sc, fl,
+                            st)
+            else:
+                for name, f in ph:
+                    f()
+            host_params.copy_(g.flat, non_blocking=True)
+            host_scaler.copy_(g.scaler, non_blocking=True)
+        e1.record(g.stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": round(pstep * E * world / (e2e_ms / 1e3) / 1e9, 4), "unit": UNIT,
+           "steps": E, "h2d_bytes_per_step": int(g.replicas.numel() * 2),
+           "d2h_bytes_per_step": int(g.flat.numel() * 2 + g.scaler.numel())}
+    sk = g.read_scaler()
+    g.close()
+
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic: seeded counter-based generator (SplitMix64 + Irwin-Hall normal), "
+                    "same replicas every timed step",
+            "config": dict(config_of(wl, path), parallelism="%d simulated ranks per GPU x %d GPUs"
+                           % (N, world)),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * K,
+            "clocks": clk, "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
+            "wall_s_timed": round(wall, 3), "scaler_t": sk.t, "device_error": sk.error}
+    return line
+
+
+# ---------------------------------------------------------- CPU checker ----
+
+def oracle_sample(wl, n_elems):
+    """The workload's first n_elems flat elements (tensor list cut there),
+    same N, buckets, gradient format and hyperparameters."""
+    numels, left = [], n_elems
+    for x in wl.numels:
+        if left <= 0:
+            break
+        numels.append(min(x, left))
+        left -= numels[-1]
+    return wl.scaled(numels=numels, rank_lo=0, rank_hi=None, inject=None)
+
+
+def time_oracle_steps(wl_s, steps):
+    """Runs `steps` checker steps on wl_s; returns seconds of checker time
+    (input generation excluded)."""
+    import numpy as np
+    import oracle
+    from fsdp_sharded_mixed_shard_gb300 import synth
+    p, _, _ = oracle.make_plan(wl_s.numels, wl_s.n_ranks, wl_s.bucket_elems)
+    psip = p.psi_pad
+    hp = oracle.hparams(lr=wl_s.lr, beta1=wl_s.beta1, beta2=wl_s.beta2, eps=wl_s.eps,
+                        weight_decay=wl_s.weight_decay, max_grad_norm=wl_s.max_grad_norm,
+                        dynamic_scale=int(wl_s.dynamic_scale),
+                        growth_interval=wl_s.growth_interval)
+    sc = oracle.scaler(wl_s.init_scale)
+    master = synth.master_f32(psip, 0, wl_s.seed, wl_s.psi)
+    m = np.zeros(psip, np.float32)
+    v = np.zeros(psip, np.float32)
+    params = oracle.cast16(master, wl_s.is_bf16)
+    spec = synth.grad_spec(seed=wl_s.seed, sigma=wl_s.sigma, bias_sigma=wl_s.bias_sigma,
+                           loss_scale=wl_s.init_scale, outliers=wl_s.outliers, psi=wl_s.psi)
+    reps = [oracle.cast16(synth.grad_f32(psip, 0, spec, 1, r), wl_s.is_bf16)
+            for r in range(wl_s.n_ranks)]
+    flags = np.zeros(max(p.n_buckets, 1), np.uint32)
+    t = 0.0
+    for _ in range(steps):
+        a = time.perf_counter()
+        oracle.step_arrays(p, 0, wl_s.n_ranks, wl_s.is_bf16, reps, 0, master, m, v, params, hp,
+                           sc, flags)
+        t += time.perf_counter() - a
+    return t
+
+
+def calibrate_oracle(wl, seconds_total, steps):
+    probe = oracle_sample(wl, 1 << 17)
+    t = time_oracle_steps(probe, 1)
+    rate = probe.psi / max(t, 1e-6)                      # params/s
+    n = int(rate * seconds_total / max(steps, 1))
+    n = max(wl.n_ranks * 1024, min(n, 1 << 25, wl.psi))
+    return n, rate
+
+
+def cpu_baseline(wl, seconds):
+    steps = 3
+    n, _ = calibrate_oracle(wl, seconds, steps)
+    s = oracle_sample(wl, n)
+    t = time_oracle_steps(s, steps)
+    return {"value": round(s.psi * steps / t / 1e9, 6), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": "first %d flat parameters of %s (same N=%d, buckets, format and "
+                      "hyperparameters), %d steps, plain single-threaded C checker, inputs "
+                      "materialised in host memory, generation untimed" % (
+                          s.psi, wl.name, wl.n_ranks, steps),
+            "seconds": round(t, 2)}
+
+
+def run_reference(args):
+    """The CPU checker on the host cores: each of the warmup + steps steps is a
+    bounded sample of the workload, sized so the run takes about two minutes."""
+    wl = workload(args.workload)
+    total = args.steps + args.warmup
+    n, _ = calibrate_oracle(wl, 100.0, total)
+    s = oracle_sample(wl, n)
+    time_oracle_steps(s, min(args.warmup, 3))
+    t = time_oracle_steps(s, args.steps)
+    value = s.psi * args.steps / t / 1e9
+    sample = ("first %d flat parameters of %s per step (same N=%d, buckets, format and "
+              "hyperparameters), plain single-threaded C checker" % (s.psi, wl.name, wl.n_ranks))
+    path = "two_pass" if wl.max_grad_norm > 0 else "fused"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic: seeded counter-based generator", "config": config_of(wl, path),
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    line = run_libzero(args, rank, world, dist)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(workload(args.workload), args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,227 @@
+"""libzero Python binding: the per-shard ZeRO step of mixed-precision AdamW on
+one GB300.
+
+A thin ctypes layer over the C ABI in include/zero.h: every function below
+has the C function's name and only marshals arguments (device pointers are
+plain Python ints, host arrays become C arrays); all computation happens in
+the sm_103a kernels of _lib/libzero.so. Loading fails loudly when the library
+has not been built (run ``__graft_entry__.build()``); there is no fallback.
+"""
+import ctypes as C
+import os
+
+from . import _build
+
+__all__ = [
+    "ZeroError", "ZeroPlanInfo", "ZeroSegment", "ZeroHParams", "ZeroScaler",
+    "ZERO_BF16", "ZERO_FP16", "ZERO_MAX_RANKS", "ZERO_TILE_ELEMS",
+    "zero_plan_create", "zero_plan_destroy", "zero_plan_get_info", "zero_plan_tensor_offsets",
+    "zero_plan_segments", "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
+    "zero_reduce_scatter", "zero_grad_norm", "zero_step", "zero_step_update", "zero_step_finish",
+    "zero_cast_params", "zero_strerror",
+    "zero_version", "lib",
+]
+
+ZERO_BF16 = 0
+ZERO_FP16 = 1
+ZERO_MAX_RANKS = 64
+ZERO_TILE_ELEMS = 4096
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__("%s failed: %s (%d)" % (fn, zero_strerror(status), status))
+        self.status = status
+
+
+class ZeroPlanInfo(C.Structure):
+    _fields_ = [("psi", C.c_int64), ("pad", C.c_int64), ("psi_pad", C.c_int64),
+                ("shard_elems", C.c_int64), ("bucket_elems", C.c_int64), ("n_tiles", C.c_int64),
+                ("n_ranks", C.c_int32), ("n_buckets", C.c_int32), ("n_segments", C.c_int32),
+                ("n_tensors", C.c_int32), ("grad_dtype", C.c_int32), ("reserved", C.c_int32),
+                ("bill_ddp", C.c_double), ("bill_z1", C.c_double), ("bill_z2", C.c_double),
+                ("bill_z3", C.c_double), ("ring_bytes_per_rank", C.c_double),
+                ("ring_hops", C.c_double), ("comm_elems_ddp", C.c_double),
+                ("comm_elems_z1", C.c_double), ("comm_elems_z2", C.c_double),
+                ("comm_elems_z3", C.c_double), ("step_bytes_fused", C.c_double),
+                ("step_bytes_two_pass", C.c_double)]
+
+
+class ZeroSegment(C.Structure):
+    _fields_ = [("lo", C.c_int64), ("hi", C.c_int64), ("rank", C.c_int32), ("bucket", C.c_int32)]
+
+
+class ZeroHParams(C.Structure):
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("eps", C.c_double), ("weight_decay", C.c_double),
+                ("max_grad_norm", C.c_double), ("dynamic_scale", C.c_int32),
+                ("growth_interval", C.c_int32), ("init_scale", C.c_double)]
+
+
+class ZeroScaler(C.Structure):
+    _fields_ = [("scale", C.c_float), ("good_steps", C.c_int32), ("t", C.c_int32),
+                ("pending", C.c_uint32), ("overflow", C.c_uint32), ("state_index", C.c_int32),
+                ("beta1_pow", C.c_double), ("beta2_pow", C.c_double), ("norm_sq", C.c_double),
+                ("norm", C.c_double), ("clip_coef", C.c_float), ("clip_apply", C.c_int32),
+                ("norm_step", C.c_int32), ("n_skipped", C.c_int32), ("error", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
+_lib = None
+_VP = C.c_void_p
+_P = C.POINTER
+
+
+def lib():
+    """The loaded libzero.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.ZERO_LIB
+        if not os.path.exists(path):
+            raise RuntimeError("libzero.so is not built (%s); run __graft_entry__.build()" % path)
+        L = C.CDLL(path)
+        L.zero_plan_create.argtypes = [_P(C.c_int64), C.c_int32, C.c_int32, C.c_int64, C.c_int,
+                                       _P(_VP)]
+        L.zero_plan_destroy.argtypes = [_VP]
+        L.zero_plan_destroy.restype = None
+        L.zero_plan_get_info.argtypes = [_VP, _P(ZeroPlanInfo)]
+        L.zero_plan_tensor_offsets.argtypes = [_VP, _P(C.c_int64)]
+        L.zero_plan_segments.argtypes = [_VP, _P(ZeroSegment), C.c_int32]
+        L.zero_plan_bucket_range.argtypes = [_VP, C.c_int32, _P(C.c_int64), _P(C.c_int64)]
+        L.zero_workspace_bytes.argtypes = [_VP]
+        L.zero_workspace_bytes.restype = C.c_size_t
+        L.zero_scaler_init.argtypes = [_P(ZeroHParams), _P(ZeroScaler)]
+        L.zero_reduce_scatter.argtypes = [_VP, C.c_int32, C.c_int32, C.c_int32, _P(_VP),
+                                          C.c_int64, _P(_VP), _VP, _VP, _VP, _VP]
+        L.zero_grad_norm.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(ZeroHParams), _VP,
+                                     _VP, _VP]
+        L.zero_step.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _P(_VP), C.c_int32,
+                                _P(_VP), _P(_VP), C.c_int64, _VP, _P(ZeroHParams), _VP, _VP, _VP]
+        L.zero_step_update.argtypes = L.zero_step.argtypes
+        L.zero_step_finish.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), C.c_int32, _P(_VP),
+                                       C.c_int64, _VP, _P(ZeroHParams), _VP, _VP]
+        L.zero_cast_params.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _VP, C.c_int64, _VP]
+        L.zero_strerror.argtypes = [C.c_int]
+        L.zero_strerror.restype = C.c_char_p
+        L.zero_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise ZeroError(fn, rc)
+
+
+def _ptrs(seq):
+    """Python list of device addresses (int or None) -> C array of void*."""
+    if seq is None:
+        return None
+    return (_VP * len(seq))(*[None if q is None else int(q) for q in seq])
+
+
+def _vp(x):
+    return None if not x else _VP(int(x))
+
+
+# ------------------------------------------------------------------ plan ----
+
+def zero_plan_create(numels, n_ranks, bucket_elems=0, grad_dtype=ZERO_BF16):
+    arr = (C.c_int64 * max(len(numels), 1))(*[int(n) for n in numels])
+    out = _VP()
+    _check("zero_plan_create", lib().zero_plan_create(arr, len(numels), n_ranks, bucket_elems,
+                                                      grad_dtype, C.byref(out)))
+    return out
+
+
+def zero_plan_destroy(plan):
+    lib().zero_plan_destroy(plan)
+
+
+def zero_plan_get_info(plan):
+    info = ZeroPlanInfo()
+    _check("zero_plan_get_info", lib().zero_plan_get_info(plan, C.byref(info)))
+    return info
+
+
+def zero_plan_tensor_offsets(plan):
+    n = zero_plan_get_info(plan).n_tensors
+    out = (C.c_int64 * max(n, 1))()
+    _check("zero_plan_tensor_offsets", lib().zero_plan_tensor_offsets(plan, out))
+    return list(out)[:n]
+
+
+def zero_plan_segments(plan):
+    n = zero_plan_get_info(plan).n_segments
+    out = (ZeroSegment * max(n, 1))()
+    _check("zero_plan_segments", lib().zero_plan_segments(plan, out, n))
+    return [(s.lo, s.hi, s.rank, s.bucket) for s in out[:n]]
+
+
+def zero_plan_bucket_range(plan, bucket):
+    lo, hi = C.c_int64(), C.c_int64()
+    _check("zero_plan_bucket_range", lib().zero_plan_bucket_range(plan, bucket, C.byref(lo),
+                                                                  C.byref(hi)))
+    return lo.value, hi.value
+
+
+def zero_workspace_bytes(plan):
+    return int(lib().zero_workspace_bytes(plan))
+
+
+def zero_scaler_init(hp):
+    out = ZeroScaler()
+    _check("zero_scaler_init", lib().zero_scaler_init(C.byref(hp), C.byref(out)))
+    return out
+
+
+# ------------------------------------------------------------------ step ----
+
+def zero_reduce_scatter(plan, bucket, rank_lo, rank_hi, replicas, window_base, grad_shards,
+                        d_scaler, d_bucket_flags=0, d_workspace=0, stream=0):
+    _check("zero_reduce_scatter", lib().zero_reduce_scatter(
+        plan, bucket, rank_lo, rank_hi, _ptrs(replicas), window_base, _ptrs(grad_shards),
+        _vp(d_scaler), _vp(d_bucket_flags), _vp(d_workspace), _vp(stream)))
+
+
+def zero_grad_norm(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, d_workspace, stream=0):
+    _check("zero_grad_norm", lib().zero_grad_norm(
+        plan, rank_lo, rank_hi, _ptrs(grad_shards), C.byref(hp), _vp(d_scaler),
+        _vp(d_workspace), _vp(stream)))
+
+
+def zero_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
+              replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags=0, stream=0):
+    _check("zero_step", lib().zero_step(
+        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
+        _ptrs(grad_shards), _ptrs(replicas), window_base, _vp(flat_params), C.byref(hp),
+        _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
+
+
+def zero_step_update(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
+                     replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags=0,
+                     stream=0):
+    _check("zero_step_update", lib().zero_step_update(
+        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
+        _ptrs(grad_shards), _ptrs(replicas), window_base, _vp(flat_params), C.byref(hp),
+        _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
+
+
+def zero_step_finish(plan, rank_lo, rank_hi, master, n_sets, grad_shards, window_base,
+                     flat_params, hp, d_scaler, stream=0):
+    _check("zero_step_finish", lib().zero_step_finish(
+        plan, rank_lo, rank_hi, _ptrs(master), n_sets, _ptrs(grad_shards), window_base,
+        _vp(flat_params), C.byref(hp), _vp(d_scaler), _vp(stream)))
+
+
+def zero_cast_params(plan, rank_lo, rank_hi, master, flat_params, window_base, stream=0):
+    _check("zero_cast_params", lib().zero_cast_params(
+        plan, rank_lo, rank_hi, _ptrs(master), _vp(flat_params), window_base, _vp(stream)))
+
+
+def zero_strerror(status):
+    return lib().zero_strerror(status).decode()
+
+
+def zero_version():
+    return lib().zero_version()

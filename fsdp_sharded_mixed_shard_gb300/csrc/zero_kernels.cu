@@ -1,0 +1,904 @@
+/*
+ * zero_kernels.cu -- sm_103a kernels of the sharded mixed-precision AdamW step
+ * and the launch layer behind the C ABI (zero.h).
+ *
+ * Kernels
+ *   step_kernel<MODE, dtype>  one persistent, tile-scheduled kernel body with
+ *                             four modes:
+ *     kFused  reduce-scatter + unscale + non-finite vote + AdamW + cast in one
+ *             pass; reads the current optimizer set, writes the other one
+ *             (2N + 26 bytes per element);
+ *     kReduce reduce-scatter + unscale + vote, writes fp32 g and the per-tile
+ *             squared-norm partials (2N + 4 bytes per element);
+ *     kUpdate AdamW + cast from fp32 g, in place, after the overflow and clip
+ *             decisions are known (30 bytes per element);
+ *     kNorm   per-tile squared-norm partials from fp32 g (4 bytes per element);
+ *     kCast   16-bit working copy from an fp32 master set (6 bytes per element),
+ *             optionally only when the step's overflow word is set.
+ *   norm_finish_kernel        fixed-order fp64 sum of the tile partials, norm,
+ *                             clip coefficient (one CTA).
+ *   scaler_finish_kernel      loss-scale / skip / step-count bookkeeping (one
+ *                             thread).
+ *
+ * Work decomposition: the owned elements are cut into segments (one bucket of
+ * one rank) and each segment into tiles of ZERO_TILE_ELEMS elements. A
+ * persistent grid (a multiple of the SM count) walks the tiles round-robin;
+ * inside a tile each thread handles 16-byte vectors of 8 elements, so a warp
+ * reads 512 contiguous bytes of each replica per access. Segment starts that
+ * are not 8-element aligned in the replicas, or whose optimizer shard is not
+ * 4-element aligned at the same point, take a scalar path.
+ *
+ * Arithmetic: every fp32 operation of the step is an explicit round-to-
+ * nearest-even intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn) and
+ * the file is built with --fmad=false, so results are the IEEE results of the
+ * stated operation sequence; no flush-to-zero. Sum order: for owner i the
+ * replicas are added in ring order i+1, ..., N-1, 0, ..., i ("How far does
+ * splitting the batch get you?", "Why does the all-reduce not get more
+ * expensive with more ranks?": a chunk is summed hop by hop around the ring
+ * and is complete at rank i).
+ */
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "zero_internal.h"
+
+namespace zk {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTile = ZERO_TILE_ELEMS;
+constexpr int kVec = 8;                       // 16-bit elements per 16-byte vector
+constexpr int kVecPerTile = kTile / kVec;     // 512
+constexpr int kMaxSegs = 128;                 // segments per launch (kernel parameter space)
+constexpr int kChunk = 8;                     // replicas loaded together
+constexpr int kNormThreads = 1024;
+
+static_assert(kTile % (kVec * kThreads) == 0, "tile must be a whole number of vector passes");
+
+enum Mode : int { kFused = 0, kReduce = 1, kUpdate = 2, kNorm = 3, kCast = 4 };
+
+// mode flags
+constexpr int kFlagClip = 1;        // kUpdate: apply the clip coefficient from the scaler
+constexpr int kFlagIfPending = 2;   // kCast: only when the overflow word is set
+constexpr int kFlagUseScalerSet = 4;// kCast: master set = scaler->state_index
+constexpr int kFlagPartials = 8;    // kReduce: write norm partials
+
+struct Seg {
+  int64_t lo, hi;          // flat element range
+  int64_t tile_local0;     // first tile of this segment in this launch's numbering
+  int64_t tile_global0;    // first tile in the plan's numbering (norm partial index)
+  int32_t rank, bucket;
+};
+
+struct Args {
+  const uint16_t* rep[ZERO_MAX_RANKS];      // replica windows
+  float* master[2][ZERO_MAX_RANKS];
+  float* mom[2][ZERO_MAX_RANKS];
+  float* var[2][ZERO_MAX_RANKS];
+  float* ghat[ZERO_MAX_RANKS];
+  uint16_t* flat;                           // parameter window
+  zero_scaler* scaler;
+  uint32_t* flags;
+  double* partials;
+  int64_t wbase, shard, n_tiles;
+  int32_t n_ranks, n_segs, n_sets, mode_flags;
+  // step constants rounded once from the fp64 hyperparameters
+  float b1, omb1, b2, omb2, lr, decay, eps;
+  int32_t pad0;
+  double beta1, beta2;
+  Seg segs[kMaxSegs];
+};
+
+// CUDA 12.1+ accepts up to 32,764 bytes of kernel parameters on sm_70 and newer
+static_assert(sizeof(Args) <= 32000, "kernel arguments exceed the parameter space");
+
+// per-CTA step scalars that depend on device-resident state
+struct StepScalars {
+  float inv;       // fp32(1 / (S_l * N))
+  float bc1, bc2;  // fp32(1 - beta^(t+1))
+  float clip;      // clip coefficient (1 when it does not apply)
+  int src;         // optimizer set read
+  int dst;         // optimizer set written
+  int skip;        // 1: nothing to do in this launch
+};
+
+// ------------------------------------------------------------ primitives --
+
+template <bool kBf16>
+__device__ __forceinline__ float widen(uint32_t h16) {
+  if constexpr (kBf16) {
+    return __uint_as_float(h16 << 16);
+  } else {
+    __half h = __ushort_as_half(static_cast<unsigned short>(h16));
+    return __half2float(h);
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void widen8(const uint4& w, float (&x)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = widen<kBf16>(u[k] & 0xFFFFu);
+    x[2 * k + 1] = widen<kBf16>(u[k] >> 16);
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint16_t narrow(float x) {
+  if constexpr (kBf16) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  } else {
+    return __half_as_ushort(__float2half_rn(x));
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint4 narrow8(const float (&x)[8]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    u[k] = static_cast<uint32_t>(narrow<kBf16>(x[2 * k])) |
+           (static_cast<uint32_t>(narrow<kBf16>(x[2 * k + 1])) << 16);
+  return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+__device__ __forceinline__ bool nonfinite(float x) {
+  return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+__device__ __forceinline__ void load8f(const float* p, float (&x)[8]) {
+  float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+__device__ __forceinline__ void store8f(float* p, const float (&x)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(x[4], x[5], x[6], x[7]));
+}
+
+// One AdamW update ("Training models too big for one GPU: ZeRO & FSDP",
+// "Adam, and why it's expensive"; decoupled weight decay):
+//   m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2; mh = m/bc1; vh = v/bc2;
+//   theta = theta (1 - lr wd) - lr mh / (sqrt(vh) + eps)
+__device__ __forceinline__ void adamw(float& th, float& m, float& v, float g, const Args& a,
+                                      const StepScalars& s) {
+  float m_new = __fadd_rn(__fmul_rn(a.b1, m), __fmul_rn(a.omb1, g));
+  float gg = __fmul_rn(g, g);
+  float v_new = __fadd_rn(__fmul_rn(a.b2, v), __fmul_rn(a.omb2, gg));
+  float mh = __fdiv_rn(m_new, s.bc1);
+  float vh = __fdiv_rn(v_new, s.bc2);
+  float den = __fadd_rn(__fsqrt_rn(vh), a.eps);
+  float u = __fdiv_rn(mh, den);
+  th = __fsub_rn(__fmul_rn(th, a.decay), __fmul_rn(a.lr, u));
+  m = m_new;
+  v = v_new;
+}
+
+// Squared-gradient accumulation with a float-float (hi, lo) pair: the square
+// is split exactly into p + e (e = fma(g, g, -p)), p is added with an exact
+// two-sum and all error terms collect in lo. Relative accuracy ~2^-44, far
+// inside the fp64 rounding of the tile and global sums, and it needs no
+// per-element fp64 work. Magnitudes whose square is not exact in fp32 go to
+// an fp64 side sum.
+struct NormAcc {
+  float hi = 0.f, lo = 0.f;
+  double big = 0.0;
+  __device__ __forceinline__ void add(float g) {
+    float ag = fabsf(g);
+    if (ag < 0x1p60f && (ag > 0x1p-60f || ag == 0.f)) {
+      float p = __fmul_rn(g, g);
+      float e = __fmaf_rn(g, g, -p);
+      float s = __fadd_rn(hi, p);
+      float bb = __fsub_rn(s, hi);
+      float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+      hi = s;
+      lo = __fadd_rn(lo, __fadd_rn(err, e));
+    } else {
+      double d = static_cast<double>(g);
+      big = __dadd_rn(big, __dmul_rn(d, d));
+    }
+  }
+  // (hi, lo) += (h2, l2), two-sum on the high parts
+  __device__ __forceinline__ void merge(float h2, float l2) {
+    float s = __fadd_rn(hi, h2);
+    float bb = __fsub_rn(s, hi);
+    float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(h2, bb));
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, l2), err);
+  }
+};
+
+// Deterministic CTA reduction of the per-thread accumulators to one fp64
+// value (fixed shuffle tree, then warps in order). Result valid in thread 0.
+__device__ double cta_norm_total(NormAcc acc, float* sh_hi, float* sh_lo, double* sh_big) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float h2 = __shfl_down_sync(0xFFFFFFFFu, acc.hi, off);
+    float l2 = __shfl_down_sync(0xFFFFFFFFu, acc.lo, off);
+    if (lane < off) acc.merge(h2, l2);
+  }
+  const bool any_big = __syncthreads_or(acc.big != 0.0);
+  if (lane == 0) {
+    sh_hi[warp] = acc.hi;
+    sh_lo[warp] = acc.lo;
+  }
+  if (any_big) {
+    double b = acc.big;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      double b2 = __shfl_down_sync(0xFFFFFFFFu, b, off);
+      if (lane < off) b = __dadd_rn(b, b2);
+    }
+    if (lane == 0) sh_big[warp] = b;
+  }
+  __syncthreads();
+  double total = 0.0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kWarps; ++w) {
+      total = __dadd_rn(total, __dadd_rn(static_cast<double>(sh_hi[w]),
+                                         static_cast<double>(sh_lo[w])));
+      if (any_big) total = __dadd_rn(total, sh_big[w]);
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+__device__ __forceinline__ void raise_flag(const Args& a, int32_t bucket) {
+  atomicOr(&a.scaler->pending, 1u);
+  if (a.flags) atomicOr(&a.flags[bucket], 1u);
+}
+
+__device__ __forceinline__ void set_error(zero_scaler* s, int code) {
+  atomicCAS(&s->error, 0, code);
+}
+
+__device__ __forceinline__ int find_seg(const Args& a, int64_t g) {
+  int lo = 0, hi = a.n_segs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (a.segs[mid].tile_local0 <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// -------------------------------------------------------------- prologue --
+
+template <int MODE>
+__device__ void compute_step_scalars(const Args& a, StepScalars* out) {
+  zero_scaler* sc = a.scaler;
+  StepScalars s;
+  s.skip = 0;
+  s.clip = 1.0f;
+  s.inv = 1.0f;
+  s.bc1 = s.bc2 = 1.0f;
+  s.src = 0;
+  s.dst = 0;
+  if (MODE == kFused || MODE == kReduce) {
+    const double denom = __dmul_rn(static_cast<double>(sc->scale), static_cast<double>(a.n_ranks));
+    s.inv = __double2float_rn(__ddiv_rn(1.0, denom));
+  }
+  if (MODE == kFused || MODE == kUpdate) {
+    const double p1 = __dmul_rn(sc->beta1_pow, a.beta1);
+    const double p2 = __dmul_rn(sc->beta2_pow, a.beta2);
+    s.bc1 = __double2float_rn(__dsub_rn(1.0, p1));
+    s.bc2 = __double2float_rn(__dsub_rn(1.0, p2));
+    const int idx = sc->state_index;
+    if (idx < 0 || idx >= a.n_sets || (MODE == kFused && a.n_sets != 2)) {
+      set_error(sc, ZERO_DEVERR_STATE_INDEX);
+      s.skip = 1;
+    }
+    s.src = idx;
+    s.dst = MODE == kFused ? (idx ^ 1) : idx;
+  }
+  if (MODE == kUpdate) {
+    if (sc->pending) s.skip = 1;  // the step is skipped: write nothing
+    if (!s.skip && (a.mode_flags & kFlagClip)) {
+      if (sc->norm_step != sc->t + 1) {
+        set_error(sc, ZERO_DEVERR_NO_NORM);
+        s.skip = 1;
+      } else if (sc->clip_apply) {
+        s.clip = sc->clip_coef;
+      }
+    }
+  }
+  if (MODE == kCast) {
+    // without these flags the scaler is not read (it may be NULL)
+    if (a.mode_flags & kFlagIfPending) s.skip = sc->pending ? 0 : 1;
+    if (a.mode_flags & kFlagUseScalerSet) {
+      const int idx = sc->state_index;
+      if (idx < 0 || idx >= a.n_sets) {
+        set_error(sc, ZERO_DEVERR_STATE_INDEX);
+        s.skip = 1;
+      }
+      s.src = idx;
+    }
+  }
+  *out = s;
+}
+
+// ------------------------------------------------------------- the body --
+
+// Per-element work on a vector of 8 elements starting at flat index j
+// (aligned path) -- MODE-specific.
+template <int MODE, bool kBf16>
+__device__ __forceinline__ void do_vector(const Args& a, const StepScalars& s, int64_t j,
+                                          int32_t rank, int first_rep, NormAcc& nacc,
+                                          bool& bad) {
+  const int64_t w = j - a.wbase;                    // window index
+  const int64_t k = j - static_cast<int64_t>(rank) * a.shard;  // shard index
+  float g[8];
+  float th[8], m[8], v[8];
+  if constexpr (MODE == kFused || MODE == kUpdate) {
+    load8f(a.master[s.src][rank] + k, th);
+    load8f(a.mom[s.src][rank] + k, m);
+    load8f(a.var[s.src][rank] + k, v);
+  }
+  if constexpr (MODE == kFused || MODE == kReduce) {
+    const int N = a.n_ranks;
+    float acc[8];
+    for (int base = 0; base < N; base += kChunk) {
+      uint4 r[kChunk];
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const int p = base + c;
+        if (p < N) {
+          int rr = first_rep + p;
+          if (rr >= N) rr -= N;
+          r[c] = __ldcs(reinterpret_cast<const uint4*>(a.rep[rr] + w));
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const int p = base + c;
+        if (p < N) {
+          float x[8];
+          widen8<kBf16>(r[c], x);
+          if (p == 0) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = x[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      g[e] = __fmul_rn(acc[e], s.inv);
+      bad |= nonfinite(g[e]);
+    }
+  }
+  if constexpr (MODE == kUpdate || MODE == kNorm) {
+    load8f(a.ghat[rank] + k, g);
+  }
+  if constexpr (MODE == kReduce) {
+    store8f(a.ghat[rank] + k, g);
+    if (a.mode_flags & kFlagPartials) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) nacc.add(g[e]);
+    }
+  }
+  if constexpr (MODE == kNorm) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) nacc.add(g[e]);
+  }
+  if constexpr (MODE == kFused || MODE == kUpdate) {
+    if (MODE == kUpdate && s.clip != 1.0f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = __fmul_rn(g[e], s.clip);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) adamw(th[e], m[e], v[e], g[e], a, s);
+    store8f(a.master[s.dst][rank] + k, th);
+    store8f(a.mom[s.dst][rank] + k, m);
+    store8f(a.var[s.dst][rank] + k, v);
+    __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(th));
+  }
+  if constexpr (MODE == kCast) {
+    load8f(a.master[s.src][rank] + k, th);
+    __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(th));
+  }
+}
+
+// Scalar version for one element (segment heads/tails, misaligned segments).
+template <int MODE, bool kBf16>
+__device__ __forceinline__ void do_scalar(const Args& a, const StepScalars& s, int64_t j,
+                                          int32_t rank, int first_rep, NormAcc& nacc,
+                                          bool& bad) {
+  const int64_t w = j - a.wbase;
+  const int64_t k = j - static_cast<int64_t>(rank) * a.shard;
+  float g = 0.f, th = 0.f, m = 0.f, v = 0.f;
+  if constexpr (MODE == kFused || MODE == kUpdate) {
+    th = a.master[s.src][rank][k];
+    m = a.mom[s.src][rank][k];
+    v = a.var[s.src][rank][k];
+  }
+  if constexpr (MODE == kFused || MODE == kReduce) {
+    const int N = a.n_ranks;
+    float acc = 0.f;
+    for (int p = 0; p < N; ++p) {
+      int rr = first_rep + p;
+      if (rr >= N) rr -= N;
+      float x = widen<kBf16>(a.rep[rr][w]);
+      acc = p == 0 ? x : __fadd_rn(acc, x);
+    }
+    g = __fmul_rn(acc, s.inv);
+    bad |= nonfinite(g);
+  }
+  if constexpr (MODE == kUpdate || MODE == kNorm) g = a.ghat[rank][k];
+  if constexpr (MODE == kReduce) {
+    a.ghat[rank][k] = g;
+    if (a.mode_flags & kFlagPartials) nacc.add(g);
+  }
+  if constexpr (MODE == kNorm) nacc.add(g);
+  if constexpr (MODE == kFused || MODE == kUpdate) {
+    if (MODE == kUpdate && s.clip != 1.0f) g = __fmul_rn(g, s.clip);
+    adamw(th, m, v, g, a, s);
+    a.master[s.dst][rank][k] = th;
+    a.mom[s.dst][rank][k] = m;
+    a.var[s.dst][rank][k] = v;
+    a.flat[w] = narrow<kBf16>(th);
+  }
+  if constexpr (MODE == kCast) {
+    th = a.master[s.src][rank][k];
+    a.flat[w] = narrow<kBf16>(th);
+  }
+}
+
+template <int MODE, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ Args a) {
+  __shared__ StepScalars sh_s;
+  __shared__ float sh_hi[kWarps], sh_lo[kWarps];
+  __shared__ double sh_big[kWarps];
+  if (threadIdx.x == 0) compute_step_scalars<MODE>(a, &sh_s);
+  __syncthreads();
+  const StepScalars s = sh_s;
+  if (s.skip) return;
+  const int lane = threadIdx.x & 31;
+
+  for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x) {
+    const Seg& sg = a.segs[find_seg(a, g)];
+    const int64_t lo = sg.lo + (g - sg.tile_local0) * kTile;
+    const int64_t hi = min(lo + kTile, sg.hi);
+    const int32_t rank = sg.rank;
+    int first_rep = rank + 1;
+    if (first_rep >= a.n_ranks) first_rep -= a.n_ranks;
+    NormAcc nacc;
+    bool bad = false;
+
+    // vector body [va, vb): 8-element aligned in the windows and 4-element
+    // aligned in the shards; otherwise everything is scalar
+    const int64_t rank0 = static_cast<int64_t>(rank) * a.shard;
+    const bool vec_ok = (((rank0 - a.wbase) & 3) == 0);
+    int64_t va = hi, vb = hi;
+    if (vec_ok) {
+      va = lo + ((a.wbase - lo) & 7);   // first j >= lo with (j - wbase) % 8 == 0
+      if (va > hi) va = hi;
+      vb = va + ((hi - va) & ~static_cast<int64_t>(7));
+    }
+    const int nvec = static_cast<int>((vb - va) >> 3);
+    for (int q = threadIdx.x; q < nvec; q += kThreads)
+      do_vector<MODE, kBf16>(a, s, va + static_cast<int64_t>(q) * kVec, rank, first_rep, nacc,
+                             bad);
+    // scalar head [lo, va) and tail [vb, hi)
+    const int nhead = static_cast<int>(va - lo);
+    const int ntail = static_cast<int>(hi - vb);
+    for (int q = threadIdx.x; q < nhead + ntail; q += kThreads) {
+      const int64_t j = q < nhead ? lo + q : vb + (q - nhead);
+      do_scalar<MODE, kBf16>(a, s, j, rank, first_rep, nacc, bad);
+    }
+
+    if constexpr (MODE == kFused || MODE == kReduce) {
+      // non-finite vote: one atomic per warp that saw one
+      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a, sg.bucket);
+    }
+    if constexpr (MODE == kReduce || MODE == kNorm) {
+      if (MODE == kNorm || (a.mode_flags & kFlagPartials)) {
+        double total = cta_norm_total(nacc, sh_hi, sh_lo, sh_big);
+        if (threadIdx.x == 0) a.partials[sg.tile_global0 + (g - sg.tile_local0)] = total;
+      }
+    }
+  }
+}
+
+// Fixed-order fp64 sum of tile partials [t0, t1), then norm and clip
+// coefficient. One CTA of kNormThreads threads: thread k sums partials
+// t0+k, t0+k+kNormThreads, ... in order; then a fixed shared-memory tree.
+__global__ void __launch_bounds__(kNormThreads) norm_finish_kernel(
+    const double* __restrict__ partials, int64_t t0, int64_t t1, double max_norm,
+    zero_scaler* sc) {
+  __shared__ double sh[kNormThreads];
+  double sum = 0.0;
+  for (int64_t t = t0 + threadIdx.x; t < t1; t += kNormThreads) sum = __dadd_rn(sum, partials[t]);
+  sh[threadIdx.x] = sum;
+  __syncthreads();
+  for (int w = kNormThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) sh[threadIdx.x] = __dadd_rn(sh[threadIdx.x], sh[threadIdx.x + w]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double nsq = sh[0];
+    const double nrm = __dsqrt_rn(nsq);
+    const double c = __ddiv_rn(max_norm, __dadd_rn(nrm, 1e-6));
+    sc->norm_sq = nsq;
+    sc->norm = nrm;
+    sc->clip_apply = c < 1.0 ? 1 : 0;
+    sc->clip_coef = c < 1.0 ? __double2float_rn(c) : 1.0f;
+    sc->norm_step = sc->t + 1;
+  }
+}
+
+// Loss scale, skip and step-count bookkeeping at the end of a step
+// ("Training models too big for one GPU: ZeRO & FSDP", "Mixed-precision
+// training": pick the scale dynamically and skip a step on overflow).
+__global__ void scaler_finish_kernel(zero_scaler* sc, double beta1, double beta2, int dynamic,
+                                     int growth_interval, int flip_sets) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const uint32_t ov = sc->pending;
+  sc->pending = 0;
+  sc->overflow = ov ? 1u : 0u;
+  if (ov) {
+    if (dynamic) {
+      const float half = __fmul_rn(sc->scale, 0.5f);
+      sc->scale = half < 1.0f ? 1.0f : half;
+    }
+    sc->good_steps = 0;
+    sc->n_skipped += 1;
+    return;
+  }
+  sc->t += 1;
+  sc->beta1_pow = __dmul_rn(sc->beta1_pow, beta1);
+  sc->beta2_pow = __dmul_rn(sc->beta2_pow, beta2);
+  sc->good_steps += 1;
+  if (dynamic && sc->good_steps >= growth_interval) {
+    sc->scale = __fmul_rn(sc->scale, 2.0f);
+    sc->good_steps = 0;
+  }
+  if (flip_sets) sc->state_index ^= 1;
+}
+
+// ----------------------------------------------------------- launch layer --
+
+template <int MODE, bool kBf16>
+int grid_size() {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_kernel<MODE, kBf16>, kThreads,
+                                                    0) != cudaSuccess)
+    return -1;
+  return sms * std::max(per_sm, 1);
+}
+
+template <int MODE, bool kBf16>
+int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
+                cudaStream_t stream) {
+  int grid_cap = grid_size<MODE, kBf16>();
+  if (grid_cap <= 0) return ZERO_ECUDA;
+  for (int32_t s0 = seg_begin; s0 < seg_end; s0 += kMaxSegs) {
+    const int32_t s1 = std::min(seg_end, s0 + kMaxSegs);
+    int64_t tiles = 0;
+    for (int32_t s = s0; s < s1; ++s) {
+      Seg& d = a.segs[s - s0];
+      d.lo = p->segs[s].lo;
+      d.hi = p->segs[s].hi;
+      d.rank = p->segs[s].rank;
+      d.bucket = p->segs[s].bucket;
+      d.tile_local0 = tiles;
+      d.tile_global0 = p->seg_tile0[s];
+      tiles += p->seg_tiles[s];
+    }
+    a.n_segs = s1 - s0;
+    a.n_tiles = tiles;
+    if (tiles == 0) continue;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
+    step_kernel<MODE, kBf16><<<grid, kThreads, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return ZERO_ECUDA;
+  }
+  return ZERO_OK;
+}
+
+template <int MODE>
+int launch(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end, cudaStream_t st) {
+  if (p->info.grad_dtype == ZERO_BF16) return launch_mode<MODE, true>(p, a, seg_begin, seg_end, st);
+  return launch_mode<MODE, false>(p, a, seg_begin, seg_end, st);
+}
+
+void fill_constants(Args& a, const zero_hparams* hp) {
+  a.b1 = static_cast<float>(hp->beta1);
+  a.omb1 = static_cast<float>(1.0 - hp->beta1);
+  a.b2 = static_cast<float>(hp->beta2);
+  a.omb2 = static_cast<float>(1.0 - hp->beta2);
+  a.lr = static_cast<float>(hp->lr);
+  const double lr_wd = hp->lr * hp->weight_decay;
+  a.decay = static_cast<float>(1.0 - lr_wd);
+  a.eps = static_cast<float>(hp->eps);
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
+}
+
+bool ranks_ok(const zero_plan* p, int32_t lo, int32_t hi) {
+  return p && lo >= 0 && hi <= p->info.n_ranks && lo < hi;
+}
+
+int check_ptr_array(const void* const* arr, int32_t lo, int32_t hi, int32_t stride, int32_t sets) {
+  if (!arr) return ZERO_EINVAL;
+  for (int32_t s = 0; s < sets; ++s)
+    for (int32_t i = lo; i < hi; ++i) {
+      const void* q = arr[s * stride + i];
+      if (!q) return ZERO_EINVAL;
+      if (!zero_detail::aligned16(q)) return ZERO_EALIGN;
+    }
+  return ZERO_OK;
+}
+
+int set_replicas(Args& a, const zero_plan* p, const void* const* replicas) {
+  const int32_t N = p->info.n_ranks;
+  int rc = check_ptr_array(replicas, 0, N, N, 1);
+  if (rc) return rc;
+  for (int32_t r = 0; r < N; ++r) a.rep[r] = static_cast<const uint16_t*>(replicas[r]);
+  return ZERO_OK;
+}
+
+int window_ok(const zero_plan* p, int32_t rank_lo, int64_t wbase) {
+  return wbase >= 0 && wbase <= static_cast<int64_t>(rank_lo) * p->info.shard_elems;
+}
+
+Args* new_args(const zero_plan* p) {
+  Args* a = new (std::nothrow) Args;
+  if (!a) return nullptr;
+  std::memset(a, 0, sizeof(Args));
+  a->n_ranks = p->info.n_ranks;
+  a->shard = p->info.shard_elems;
+  return a;
+}
+
+int seg_range(const zero_plan* p, int32_t bucket, int32_t rank_lo, int32_t rank_hi,
+              std::vector<std::pair<int32_t, int32_t>>& runs) {
+  const int32_t s0 = p->rank_seg0[rank_lo], s1 = p->rank_seg0[rank_hi];
+  if (bucket < 0) {
+    runs.emplace_back(s0, s1);
+    return ZERO_OK;
+  }
+  // segments of one bucket inside [s0, s1) are contiguous
+  int32_t b0 = -1, b1 = -1;
+  for (int32_t s = s0; s < s1; ++s) {
+    if (p->segs[s].bucket == bucket) {
+      if (b0 < 0) b0 = s;
+      b1 = s + 1;
+    }
+  }
+  if (b0 >= 0) runs.emplace_back(b0, b1);
+  return ZERO_OK;
+}
+
+}  // namespace zk
+
+using namespace zk;
+
+extern "C" {
+
+ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t rank_lo,
+                                 int32_t rank_hi, const void* const* replicas,
+                                 int64_t window_base, float* const* grad_shards,
+                                 zero_scaler* d_scaler, uint32_t* d_bucket_flags,
+                                 void* d_workspace, void* stream) {
+  if (!ranks_ok(plan, rank_lo, rank_hi) || !d_scaler) return ZERO_EINVAL;
+  if (bucket < -1 || bucket >= plan->info.n_buckets) return ZERO_EINVAL;
+  if (!window_ok(plan, rank_lo, window_base)) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler) || !zero_detail::aligned16(d_bucket_flags) ||
+      !zero_detail::aligned16(d_workspace))
+    return ZERO_EALIGN;
+  int rc = check_ptr_array(reinterpret_cast<const void* const*>(grad_shards), rank_lo, rank_hi,
+                           0, 1);
+  if (rc) return rc;
+  Args* a = new_args(plan);
+  if (!a) return ZERO_ENOMEM;
+  rc = set_replicas(*a, plan, replicas);
+  if (!rc) {
+    for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = grad_shards[i];
+    a->wbase = window_base;
+    a->scaler = d_scaler;
+    a->flags = d_bucket_flags;
+    a->partials = static_cast<double*>(d_workspace);
+    a->mode_flags = d_workspace ? kFlagPartials : 0;
+    std::vector<std::pair<int32_t, int32_t>> runs;
+    seg_range(plan, bucket, rank_lo, rank_hi, runs);
+    for (auto& r : runs) {
+      rc = launch<kReduce>(plan, *a, r.first, r.second, static_cast<cudaStream_t>(stream));
+      if (rc) break;
+    }
+  }
+  delete a;
+  return rc;
+}
+
+ZERO_API int zero_grad_norm(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                            const float* const* grad_shards, const zero_hparams* hp,
+                            zero_scaler* d_scaler, void* d_workspace, void* stream) {
+  if (!ranks_ok(plan, rank_lo, rank_hi) || !hp || !d_scaler || !d_workspace) return ZERO_EINVAL;
+  if (!(hp->max_grad_norm > 0.0)) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler) || !zero_detail::aligned16(d_workspace))
+    return ZERO_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+  if (grad_shards) {
+    int rc = check_ptr_array(reinterpret_cast<const void* const*>(grad_shards), rank_lo, rank_hi,
+                             0, 1);
+    if (rc) return rc;
+    Args* a = new_args(plan);
+    if (!a) return ZERO_ENOMEM;
+    for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = const_cast<float*>(grad_shards[i]);
+    a->scaler = d_scaler;
+    a->partials = static_cast<double*>(d_workspace);
+    rc = launch<kNorm>(plan, *a, s0, s1, st);
+    delete a;
+    if (rc) return rc;
+  }
+  const int64_t t0 = s0 < s1 ? plan->seg_tile0[s0] : 0;
+  const int64_t t1 = s0 < s1 ? plan->seg_tile0[s1 - 1] + plan->seg_tiles[s1 - 1] : 0;
+  norm_finish_kernel<<<1, kNormThreads, 0, st>>>(static_cast<const double*>(d_workspace), t0, t1,
+                                                 hp->max_grad_norm, d_scaler);
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+namespace {
+
+// Argument checks and kernel arguments shared by the step entry points.
+int prepare_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi, float* const* master,
+                 float* const* exp_avg, float* const* exp_avg_sq, int32_t n_sets,
+                 const float* const* grad_shards, const void* const* replicas,
+                 int64_t window_base, void* flat_params, const zero_hparams* hp,
+                 zero_scaler* d_scaler, uint32_t* d_bucket_flags, bool need_moments,
+                 bool need_replicas, Args** out) {
+  *out = nullptr;
+  if (!ranks_ok(plan, rank_lo, rank_hi) || !hp || !d_scaler || !flat_params) return ZERO_EINVAL;
+  if (n_sets < 1 || n_sets > 2) return ZERO_EINVAL;
+  if (hp->growth_interval < 1) return ZERO_EINVAL;
+  if (!window_ok(plan, rank_lo, window_base)) return ZERO_EINVAL;
+  const bool fused = grad_shards == nullptr;
+  const bool clip = hp->max_grad_norm > 0.0;
+  if (fused && (clip || n_sets != 2)) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler) || !zero_detail::aligned16(d_bucket_flags) ||
+      !zero_detail::aligned16(flat_params))
+    return ZERO_EALIGN;
+  const int32_t N = plan->info.n_ranks;
+  int rc;
+  if ((rc = check_ptr_array(reinterpret_cast<const void* const*>(master), rank_lo, rank_hi, N,
+                            n_sets)))
+    return rc;
+  if (need_moments) {
+    if ((rc = check_ptr_array(reinterpret_cast<const void* const*>(exp_avg), rank_lo, rank_hi, N,
+                              n_sets)))
+      return rc;
+    if ((rc = check_ptr_array(reinterpret_cast<const void* const*>(exp_avg_sq), rank_lo,
+                              rank_hi, N, n_sets)))
+      return rc;
+    if (!fused && (rc = check_ptr_array(reinterpret_cast<const void* const*>(grad_shards),
+                                        rank_lo, rank_hi, 0, 1)))
+      return rc;
+  }
+  Args* a = new_args(plan);
+  if (!a) return ZERO_ENOMEM;
+  if (fused && need_replicas && (rc = set_replicas(*a, plan, replicas))) {
+    delete a;
+    return rc;
+  }
+  for (int32_t s = 0; s < n_sets; ++s)
+    for (int32_t i = rank_lo; i < rank_hi; ++i) {
+      a->master[s][i] = master[s * N + i];
+      if (need_moments) {
+        a->mom[s][i] = exp_avg[s * N + i];
+        a->var[s][i] = exp_avg_sq[s * N + i];
+      }
+    }
+  if (!fused && need_moments)
+    for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = const_cast<float*>(grad_shards[i]);
+  a->n_sets = n_sets;
+  a->flat = static_cast<uint16_t*>(flat_params);
+  a->wbase = window_base;
+  a->scaler = d_scaler;
+  a->flags = d_bucket_flags;
+  a->mode_flags = (!fused && clip) ? kFlagClip : 0;
+  fill_constants(*a, hp);
+  *out = a;
+  return ZERO_OK;
+}
+
+}  // namespace
+
+ZERO_API int zero_step_update(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                              float* const* master, float* const* exp_avg,
+                              float* const* exp_avg_sq, int32_t n_sets,
+                              const float* const* grad_shards, const void* const* replicas,
+                              int64_t window_base, void* flat_params, const zero_hparams* hp,
+                              zero_scaler* d_scaler, uint32_t* d_bucket_flags, void* stream) {
+  Args* a = nullptr;
+  int rc = prepare_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
+                        replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags, true,
+                        true, &a);
+  if (rc) return rc;
+  const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = grad_shards == nullptr ? launch<kFused>(plan, *a, s0, s1, st)
+                              : launch<kUpdate>(plan, *a, s0, s1, st);
+  delete a;
+  return rc;
+}
+
+ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                              float* const* master, int32_t n_sets,
+                              const float* const* grad_shards, int64_t window_base,
+                              void* flat_params, const zero_hparams* hp, zero_scaler* d_scaler,
+                              void* stream) {
+  Args* a = nullptr;
+  int rc = prepare_step(plan, rank_lo, rank_hi, master, nullptr, nullptr, n_sets, grad_shards,
+                        nullptr, window_base, flat_params, hp, d_scaler, nullptr, false, false,
+                        &a);
+  if (rc) return rc;
+  const bool fused = grad_shards == nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (fused) {
+    // skip path: re-cast the parameters from the kept master set
+    a->mode_flags = kFlagIfPending | kFlagUseScalerSet;
+    const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+    rc = launch<kCast>(plan, *a, s0, s1, st);
+  }
+  delete a;
+  if (rc) return rc;
+  scaler_finish_kernel<<<1, 32, 0, st>>>(d_scaler, hp->beta1, hp->beta2, hp->dynamic_scale,
+                                         hp->growth_interval, fused ? 1 : 0);
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+ZERO_API int zero_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                       float* const* master, float* const* exp_avg, float* const* exp_avg_sq,
+                       int32_t n_sets, const float* const* grad_shards,
+                       const void* const* replicas, int64_t window_base, void* flat_params,
+                       const zero_hparams* hp, zero_scaler* d_scaler,
+                       uint32_t* d_bucket_flags, void* stream) {
+  int rc = zero_step_update(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
+                            grad_shards, replicas, window_base, flat_params, hp, d_scaler,
+                            d_bucket_flags, stream);
+  if (rc) return rc;
+  return zero_step_finish(plan, rank_lo, rank_hi, master, n_sets, grad_shards, window_base,
+                          flat_params, hp, d_scaler, stream);
+}
+
+ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                              const float* const* master, void* flat_params,
+                              int64_t window_base, void* stream) {
+  if (!ranks_ok(plan, rank_lo, rank_hi) || !flat_params) return ZERO_EINVAL;
+  if (!window_ok(plan, rank_lo, window_base)) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(flat_params)) return ZERO_EALIGN;
+  int rc = check_ptr_array(reinterpret_cast<const void* const*>(master), rank_lo, rank_hi, 0, 1);
+  if (rc) return rc;
+  Args* a = new_args(plan);
+  if (!a) return ZERO_ENOMEM;
+  for (int32_t i = rank_lo; i < rank_hi; ++i) a->master[0][i] = const_cast<float*>(master[i]);
+  a->n_sets = 1;
+  a->flat = static_cast<uint16_t*>(flat_params);
+  a->wbase = window_base;
+  a->mode_flags = 0;
+  // kCast without kFlagIfPending/kFlagUseScalerSet never touches the scaler
+  zero_scaler* dummy = nullptr;
+  a->scaler = dummy;
+  const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+  rc = launch<kCast>(plan, *a, s0, s1, static_cast<cudaStream_t>(stream));
+  delete a;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,190 @@
+"""Device buffers and step driver for one synthetic workload (harness only).
+
+Used by the GPU tests, the smoke check and the benchmark. PyTorch provides
+device memory and streams; every step of the path runs in libzero's kernels
+through the C ABI, and the inputs come from the seeded generator kernels.
+
+Layout in HBM for a workload with N ranks processing owners [lo, hi):
+  replicas   int16 [N, row]       rank r's 16-bit gradient window
+                                  [lo*S, hi*S), rows padded to 16 bytes
+  flat       int16 [row]          16-bit working parameters (same window)
+  state      fp32 [n_sets, 3, n_own, srow]  master / exp_avg / exp_avg_sq
+                                  shard of each owned rank, rows padded to 16 B
+  ghat       fp32 [n_own, srow]   reduced gradients (two-pass path only)
+  scaler     80 bytes             zero_scaler
+  flags      uint32 [n_buckets]   per-bucket non-finite flags
+  workspace  zero_workspace_bytes (norm tile partials, clip path only)
+"""
+import ctypes as C
+
+import torch
+
+from . import (ZERO_BF16, ZERO_FP16, ZeroHParams, ZeroScaler, zero_cast_params, zero_grad_norm,
+               zero_plan_create, zero_plan_destroy, zero_plan_get_info, zero_reduce_scatter,
+               zero_scaler_init, zero_step, zero_workspace_bytes)
+from . import synth
+
+
+def _round_up(x, m):
+    return (x + m - 1) // m * m
+
+
+def hparams_of(wl):
+    return ZeroHParams(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, wl.max_grad_norm,
+                       int(wl.dynamic_scale), wl.growth_interval, wl.init_scale)
+
+
+class Group:
+    """All device state of one simulated data-parallel group on one GPU."""
+
+    def __init__(self, wl, device="cuda", two_pass=None, stream=None, alloc_replicas=True):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.two_pass = (wl.max_grad_norm > 0) if two_pass is None else two_pass
+        self.n_sets = 1 if self.two_pass else 2
+        self.is_bf16 = wl.is_bf16
+        self.plan = zero_plan_create(wl.numels, wl.n_ranks, wl.bucket_elems,
+                                     ZERO_BF16 if wl.is_bf16 else ZERO_FP16)
+        self.info = zero_plan_get_info(self.plan)
+        self.N = wl.n_ranks
+        self.S = self.info.shard_elems
+        self.lo, self.hi = wl.ranks
+        self.wbase = self.lo * self.S
+        self.wlen = (self.hi - self.lo) * self.S
+        self.row = _round_up(max(self.wlen, 1), 8)
+        self.srow = _round_up(max(self.S, 1), 4)
+        self.hp = hparams_of(wl)
+        n_own = self.hi - self.lo
+        dev = self.device
+        self.replicas = (torch.zeros((self.N, self.row), dtype=torch.int16, device=dev)
+                         if alloc_replicas else None)
+        self.flat = torch.zeros(self.row, dtype=torch.int16, device=dev)
+        self.state = torch.zeros((self.n_sets, 3, n_own, self.srow), dtype=torch.float32,
+                                 device=dev)
+        self.ghat = (torch.zeros((n_own, self.srow), dtype=torch.float32, device=dev)
+                     if self.two_pass else None)
+        self.scaler = torch.zeros(C.sizeof(ZeroScaler), dtype=torch.uint8, device=dev)
+        self.flags = torch.zeros(max(self.info.n_buckets, 1), dtype=torch.int32, device=dev)
+        ws = zero_workspace_bytes(self.plan)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+
+    def close(self):
+        if self.plan:
+            zero_plan_destroy(self.plan)
+            self.plan = None
+
+    # -------------------------------------------------------------- pointers
+    @property
+    def sptr(self):
+        return self.stream.cuda_stream
+
+    def rep_ptrs(self, replicas=None):
+        t = self.replicas if replicas is None else replicas
+        base, rb = t.data_ptr(), self.row * 2
+        return [base + r * rb for r in range(self.N)]
+
+    def _state_ptrs(self, which):
+        out = [None] * (self.n_sets * self.N)
+        for s in range(self.n_sets):
+            for i in range(self.lo, self.hi):
+                out[s * self.N + i] = self.state[s, which, i - self.lo].data_ptr()
+        return out
+
+    def ghat_ptrs(self):
+        out = [None] * self.N
+        for i in range(self.lo, self.hi):
+            out[i] = self.ghat[i - self.lo].data_ptr()
+        return out
+
+    # ----------------------------------------------------------------- init
+    def init_state(self):
+        wl = self.wl
+        with torch.cuda.stream(self.stream):
+            self.state.zero_()
+            for i in range(self.lo, self.hi):
+                synth.gpu_fill_master(self.state[0, 0, i - self.lo].data_ptr(), self.S,
+                                      i * self.S, wl.seed, wl.psi, self.sptr)
+            master0 = [None] * self.N
+            for i in range(self.lo, self.hi):
+                master0[i] = self.state[0, 0, i - self.lo].data_ptr()
+            zero_cast_params(self.plan, self.lo, self.hi, master0, self.flat.data_ptr(),
+                             self.wbase, self.sptr)
+            sc = zero_scaler_init(self.hp)
+            host = torch.frombuffer(bytearray(bytes(sc)), dtype=torch.uint8)
+            self.scaler.copy_(host)
+
+    def read_scaler(self):
+        self.stream.synchronize()
+        raw = bytes(self.scaler.cpu().numpy().tobytes())
+        return ZeroScaler.from_buffer_copy(raw)
+
+    def grad_spec(self, scale):
+        wl = self.wl
+        return synth.grad_spec(seed=wl.seed, sigma=wl.sigma, bias_sigma=wl.bias_sigma,
+                               loss_scale=scale, outliers=wl.outliers, psi=wl.psi)
+
+    def gen_grads(self, step, scale=None, replicas=None):
+        """Fill the replicas with step `step`'s gradients at the device's
+        current loss scale (read back from the scaler unless given)."""
+        if scale is None:
+            scale = self.read_scaler().scale
+        t = self.replicas if replicas is None else replicas
+        spec = self.grad_spec(scale)
+        ptrs = self.rep_ptrs(t)
+        for r in range(self.N):
+            synth.gpu_fill_grad(ptrs[r], self.wlen, self.wbase, spec, step, r, self.is_bf16,
+                                self.sptr)
+        inj = self.wl.inject
+        if inj is not None and inj[0] == step:
+            _, r, e, bits = inj
+            if self.wbase <= e < self.wbase + self.wlen:
+                with torch.cuda.stream(self.stream):
+                    t[r, e - self.wbase] = bits - 65536 if bits >= 32768 else bits
+
+    # ----------------------------------------------------------------- step
+    def step(self, per_bucket=False, replicas=None, clear_flags=True):
+        """One optimizer step through the C ABI (fused or two-pass)."""
+        st = self.sptr
+        if clear_flags:
+            with torch.cuda.stream(self.stream):
+                self.flags.zero_()
+        reps = self.rep_ptrs(replicas)
+        m, v, w = self._state_ptrs(0), self._state_ptrs(1), self._state_ptrs(2)
+        sc = self.scaler.data_ptr()
+        fl = self.flags.data_ptr()
+        if not self.two_pass:
+            zero_step(self.plan, self.lo, self.hi, m, v, w, self.n_sets, None, reps, self.wbase,
+                      self.flat.data_ptr(), self.hp, sc, fl, st)
+            return
+        clip = self.hp.max_grad_norm > 0
+        ws = self.workspace.data_ptr() if clip else 0
+        gp = self.ghat_ptrs()
+        buckets = range(self.info.n_buckets) if per_bucket else [-1]
+        for b in buckets:
+            zero_reduce_scatter(self.plan, b, self.lo, self.hi, reps, self.wbase, gp, sc, fl, ws,
+                                st)
+        if clip:
+            zero_grad_norm(self.plan, self.lo, self.hi, None, self.hp, sc, ws, st)
+        zero_step(self.plan, self.lo, self.hi, m, v, w, self.n_sets, gp, None, self.wbase,
+                  self.flat.data_ptr(), self.hp, sc, fl, st)
+
+    # ------------------------------------------------------------- readback
+    def current_state(self):
+        """(master, exp_avg, exp_avg_sq) of the owned window as fp32 CPU
+        tensors indexed by flat element - wbase."""
+        idx = self.read_scaler().state_index if self.n_sets == 2 else 0
+        st = self.state[idx, :, :, :self.S].reshape(3, -1).cpu()
+        return st[0], st[1], st[2]
+
+    def params_u16(self):
+        self.stream.synchronize()
+        return self.flat[:self.wlen].cpu().numpy().view("uint16")
+
+    def replicas_u16(self):
+        self.stream.synchronize()
+        return self.replicas[:, :self.wlen].cpu().numpy().view("uint16")
+
+    def flags_u32(self):
+        self.stream.synchronize()
+        return self.flags[:self.info.n_buckets].cpu().numpy().view("uint32")

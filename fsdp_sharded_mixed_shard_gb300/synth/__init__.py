@@ -49,6 +49,8 @@ def host():
                                           C.c_int64]
         L.zs_host_grad_at.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, P(GradSpec),
                                       C.c_uint32, C.c_uint32]
+        L.zs_host_master_at.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_uint64,
+                                        C.c_int64]
         L.zs_host_spec_size.restype = C.c_int64
         assert L.zs_host_spec_size() == C.sizeof(GradSpec)
         _host = L
@@ -102,6 +104,13 @@ def grad_f32_at(elems, spec, step, rank):
 def master_f32(n, elem0, seed, psi):
     out = np.empty(n, dtype=np.float32)
     host().zs_host_fill_master(out.ctypes.data, n, elem0, seed, psi)
+    return out
+
+
+def master_f32_at(elems, seed, psi):
+    elems = np.ascontiguousarray(elems, dtype=np.int64)
+    out = np.empty(len(elems), dtype=np.float32)
+    host().zs_host_master_at(out.ctypes.data, elems.ctypes.data, len(elems), seed, psi)
     return out
 
 

@@ -113,6 +113,43 @@ ZS_FN float zs_grad_value(const zs_grad_spec* g, uint32_t step, uint32_t rank,
   return ZS_MUL(x, g->loss_scale);
 }
 
+/* The same values with the per-(step, rank) keys and bias formed once:
+ * zs_grad_stream_value(zs_grad_stream_make(g, step, rank), e) equals
+ * zs_grad_value(g, step, rank, e) for every e. */
+typedef struct zs_grad_stream {
+  uint64_t key_grad, key_outlier;
+  float sigma, bias, loss_scale;
+  int32_t has_bias, outliers;
+  int64_t psi;
+} zs_grad_stream;
+
+ZS_FN zs_grad_stream zs_grad_stream_make(const zs_grad_spec* g, uint32_t step, uint32_t rank) {
+  zs_grad_stream s;
+  s.key_grad = zs_key(g->seed, ZS_TAG_GRAD, step, rank);
+  s.key_outlier = zs_key(g->seed, ZS_TAG_OUTLIER, step, rank);
+  s.sigma = g->sigma;
+  s.has_bias = g->bias_sigma > 0.0f;
+  s.bias = s.has_bias
+               ? ZS_MUL(zs_normal(zs_u64(zs_key(g->seed, ZS_TAG_BIAS, step, rank), 0u)),
+                        g->bias_sigma)
+               : 0.0f;
+  s.loss_scale = g->loss_scale;
+  s.outliers = g->outliers;
+  s.psi = g->psi;
+  return s;
+}
+
+ZS_FN float zs_grad_stream_value(const zs_grad_stream* s, int64_t elem) {
+  if (elem >= s->psi) return 0.0f;
+  float x = ZS_MUL(zs_normal(zs_u64(s->key_grad, (uint64_t)elem)), s->sigma);
+  if (s->has_bias) x = ZS_ADD(x, s->bias);
+  if (s->outliers) {
+    uint64_t o = zs_u64(s->key_outlier, (uint64_t)elem);
+    if ((o & 0xFFFFFu) < 1049u) x = ZS_MUL(x, 100.0f);
+  }
+  return ZS_MUL(x, s->loss_scale);
+}
+
 /* Initial fp32 master weight of flat element `elem`: U(-0.05, 0.05) from a
  * 23-bit uniform integer u: ((u + 0.5) * 2^-23) * 0.1 - 0.05 (u + 0.5 and the
  * power-of-two scaling are exact). Padding elements (elem >= psi) start at 0. */

@@ -16,10 +16,10 @@ namespace {
 
 template <bool kBf16>
 __global__ void fill_grad_kernel(uint16_t* __restrict__ dst, int64_t n, int64_t elem0,
-                                 zs_grad_spec spec, uint32_t step, uint32_t rank) {
+                                 zs_grad_stream st) {
   int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
-    float x = zs_grad_value(&spec, step, rank, elem0 + k);
+    float x = zs_grad_stream_value(&st, elem0 + k);
     if (kBf16) {
       __nv_bfloat16 h = __float2bfloat16_rn(x);
       dst[k] = *reinterpret_cast<uint16_t*>(&h);
@@ -54,10 +54,11 @@ ZS_EXPORT int zs_gpu_fill_grad(void* dst, int64_t n, int64_t elem0, const zs_gra
                      uint32_t step, uint32_t rank, int32_t is_bf16, void* stream) {
   if (n <= 0) return 0;
   cudaStream_t s = (cudaStream_t)stream;
+  zs_grad_stream st = zs_grad_stream_make(spec, step, rank);
   if (is_bf16)
-    fill_grad_kernel<true><<<grid_for(n), 256, 0, s>>>((uint16_t*)dst, n, elem0, *spec, step, rank);
+    fill_grad_kernel<true><<<grid_for(n), 256, 0, s>>>((uint16_t*)dst, n, elem0, st);
   else
-    fill_grad_kernel<false><<<grid_for(n), 256, 0, s>>>((uint16_t*)dst, n, elem0, *spec, step, rank);
+    fill_grad_kernel<false><<<grid_for(n), 256, 0, s>>>((uint16_t*)dst, n, elem0, st);
   return (int)cudaGetLastError();
 }
 

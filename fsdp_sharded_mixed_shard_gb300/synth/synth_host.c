@@ -25,10 +25,22 @@ void zs_host_fill_master(float* out, int64_t n, int64_t elem0, uint64_t seed, in
   for (int64_t k = 0; k < n; ++k) out[k] = zs_master_value(seed, psi, elem0 + k);
 }
 
+/* same values through the per-(step, rank) stream */
+void zs_host_fill_grad_stream(float* out, int64_t n, int64_t elem0, const zs_grad_spec* spec,
+                              uint32_t step, uint32_t rank) {
+  zs_grad_stream s = zs_grad_stream_make(spec, step, rank);
+  for (int64_t k = 0; k < n; ++k) out[k] = zs_grad_stream_value(&s, elem0 + k);
+}
+
 /* gradient values at arbitrary flat indices */
 void zs_host_grad_at(float* out, const int64_t* elems, int64_t n, const zs_grad_spec* spec,
                      uint32_t step, uint32_t rank) {
   for (int64_t k = 0; k < n; ++k) out[k] = zs_grad_value(spec, step, rank, elems[k]);
+}
+
+/* initial master weights at arbitrary flat indices */
+void zs_host_master_at(float* out, const int64_t* elems, int64_t n, uint64_t seed, int64_t psi) {
+  for (int64_t k = 0; k < n; ++k) out[k] = zs_master_value(seed, psi, elems[k]);
 }
 
 int64_t zs_host_spec_size(void) { return (int64_t)sizeof(zs_grad_spec); }

@@ -1,0 +1,320 @@
+/*
+ * zero.h -- C ABI of libzero: the per-shard ZeRO step of mixed-precision
+ * AdamW on one GB300 (sm_103a).
+ *
+ * What the library computes. N data-parallel ranks hold N gradient replicas
+ * of one flattened parameter vector. Rank i owns the 1/N slice
+ * [i*S, (i+1)*S) of the padded flat vector and, for every element j it owns:
+ *   1. reduce-scatter: g = (sum of the N replicas' values in ring order
+ *      i+1, i+2, ..., N-1, 0, ..., i, accumulated in fp32) * fp32(1/(S_l*N)),
+ *      S_l the loss scale; a non-finite g raises the bucket's flag and the
+ *      step's overflow word;
+ *   2. optional global-norm clip: g *= c when c = max_norm/(||g||_2 + 1e-6) < 1;
+ *   3. AdamW on the fp32 master/m/v shard (decoupled weight decay);
+ *   4. cast of the updated master to the bf16/fp16 working copy, written into
+ *      its slot of the gathered flat parameter buffer;
+ * and a step that saw any non-finite g is skipped as a whole (no state
+ * changes, t kept, dynamic loss scale halved).
+ *
+ * Sources (page title, section):
+ *   "Training models too big for one GPU: ZeRO & FSDP": "Adam, and why it's
+ *     expensive" (update equations), "Mixed-precision training" (fp32 master,
+ *     loss scaling, skip on overflow), "Data parallelism and the all-reduce"
+ *     (averaging; reduce-scatter leaves GPU i with the sum of chunk i),
+ *     "ZeRO stages 1, 2 and 3" (each GPU updates its own 1/N slice, then the
+ *     updated weights are gathered), "FSDP: the same idea, one unit at a time"
+ *     (parameters flattened and sharded), "The memory bill: 16 bytes per
+ *     parameter" (K = 12 optimizer bytes);
+ *   "How far does splitting the batch get you?": "Why does the all-reduce not
+ *     get more expensive with more ranks?" (ring reduce-scatter, 2(d-1)M/d
+ *     bytes), "How does the collective hide behind the backward pass?"
+ *     (gradient buckets), "What does gradient accumulation actually buy?"
+ *     (fp32 reduce-scatter), "What does each stage cost on the wire?";
+ *   "ZeRO Stage 3 Math": "Stage 3: divide everything by N";
+ *   "Stop Replicating What You Can Shard: ZeRO and FSDP": "The three stages
+ *     of ZeRO" (per-stage memory).
+ * The global-norm clip is not on the pages; its convention is stated at
+ * zero_grad_norm.
+ *
+ * One GPU holds all N ranks: the N replicas are N resident HBM buffers, a
+ * single launch covers every rank's slice, and the all-gather is implicit
+ * (rank i writes its slot of the one flat parameter buffer).
+ *
+ * Conventions.
+ *   - Every function returns an int status: ZERO_OK (0) or a negative
+ *     zero_status. No call aborts or throws.
+ *   - The library allocates no device memory. Device buffers (replicas,
+ *     optimizer shards, reduced-gradient shards, flat parameters, the
+ *     scaler, bucket flags, workspace) are owned by the caller.
+ *   - Device calls are asynchronous on the given cudaStream_t (passed as
+ *     void*; NULL = legacy default stream) and never synchronize the host.
+ *     Decisions (skip, clip coefficient, loss scale) stay on the device in
+ *     zero_scaler.
+ *   - Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise).
+ *   - Plans are immutable after creation; the library has no global state,
+ *     so concurrent calls on different streams and buffers are safe. Calls
+ *     that share a scaler or buffers must be ordered by the caller.
+ *   - Element indices are int64 (N * psi may exceed 2^31).
+ */
+#ifndef ZERO_H
+#define ZERO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ZERO_API __attribute__((visibility("default")))
+#else
+#define ZERO_API
+#endif
+
+/* Largest number of simulated data-parallel ranks one plan may have. */
+#define ZERO_MAX_RANKS 64
+
+/* Elements per norm tile: the squared-gradient partial sums are formed over
+ * tiles of this many elements inside each segment (see zero_grad_norm). */
+#define ZERO_TILE_ELEMS 4096
+
+typedef enum zero_status {
+  ZERO_OK = 0,
+  ZERO_EINVAL = -1,   /* invalid argument (NULL pointer, bad range, bad size) */
+  ZERO_EALIGN = -2,   /* a device pointer is not 16-byte aligned */
+  ZERO_ERANGE = -3,   /* a size exceeds a library limit (e.g. ZERO_MAX_RANKS) */
+  ZERO_ECUDA = -4,    /* a CUDA launch or runtime call failed */
+  ZERO_ENOMEM = -5,   /* host allocation failed */
+  ZERO_ESTATE = -6    /* call order violated (e.g. clip without zero_grad_norm) */
+} zero_status;
+
+typedef enum zero_dtype { ZERO_BF16 = 0, ZERO_FP16 = 1 } zero_dtype;
+
+/* ------------------------------------------------------------------ plan -- */
+
+typedef struct zero_plan zero_plan; /* opaque, host memory, immutable */
+
+/* Flat range [lo, hi) of one bucket owned by one rank. Segments are ordered
+ * by lo, i.e. bucket-major with ranks ascending. */
+typedef struct zero_segment {
+  int64_t lo, hi;
+  int32_t rank;
+  int32_t bucket;
+} zero_segment;
+
+typedef struct zero_plan_info {
+  int64_t psi;            /* parameters: sum of the tensor sizes */
+  int64_t pad;            /* zeros appended: (N - psi mod N) mod N */
+  int64_t psi_pad;        /* psi + pad, a multiple of N */
+  int64_t shard_elems;    /* S = psi_pad / N: elements each rank owns */
+  int64_t bucket_elems;   /* bucket size in elements (0 = one bucket) */
+  int64_t n_tiles;        /* norm tiles over all segments */
+  int32_t n_ranks;        /* N */
+  int32_t n_buckets;
+  int32_t n_segments;
+  int32_t n_tensors;
+  int32_t grad_dtype;     /* zero_dtype of gradients and working parameters */
+  int32_t reserved;
+  /* Per-device model-state bytes of mixed-precision Adam (K = 12), from the
+   * unpadded psi: DDP 16 psi, ZeRO-1 4 psi + 12 psi/N, ZeRO-2 2 psi + 14 psi/N,
+   * ZeRO-3 16 psi/N ("ZeRO stages 1, 2 and 3"; "ZeRO Stage 3 Math",
+   * "Stage 3: divide everything by N"). */
+  double bill_ddp, bill_z1, bill_z2, bill_z3;
+  /* Ring all-reduce of the 2 psi bytes of 16-bit gradients: bytes each rank
+   * sends, 2(N-1)M/N, and sequential hops 2(N-1) ("Why does the all-reduce
+   * not get more expensive with more ranks?"). */
+  double ring_bytes_per_rank, ring_hops;
+  /* Communication per step in elements: 2 psi (DDP, ZeRO-1, ZeRO-2) and
+   * 3 psi (ZeRO-3) ("What does each stage cost on the wire?"). */
+  double comm_elems_ddp, comm_elems_z1, comm_elems_z2, comm_elems_z3;
+  /* HBM bytes per parameter of one whole-group step on one GPU:
+   * fused (no clip) 2N + 26; two-pass (clip) 2N + 34. */
+  double step_bytes_fused, step_bytes_two_pass;
+} zero_plan_info;
+
+/* Build a plan: flatten the tensor list (tensor k starts at the sum of the
+ * previous sizes, no per-tensor alignment), pad to a multiple of n_ranks,
+ * give rank i the slice [i*S, (i+1)*S), cut the padded buffer into buckets
+ * of bucket_elems elements (0 = one bucket) and each bucket at the owners'
+ * slice boundaries into segments.
+ *   numels:       n_tensors sizes (>= 0), host memory, read only.
+ *   n_ranks:      1 .. ZERO_MAX_RANKS (ZERO_ERANGE above).
+ *   grad_dtype:   format of gradient replicas and working parameters.
+ *   out:          receives a plan owned by the caller (zero_plan_destroy).
+ * Errors: ZERO_EINVAL (NULL out, negative size or bucket, n_ranks < 1),
+ * ZERO_ERANGE, ZERO_ENOMEM. */
+ZERO_API int zero_plan_create(const int64_t* numels, int32_t n_tensors, int32_t n_ranks,
+                              int64_t bucket_elems, zero_dtype grad_dtype, zero_plan** out);
+ZERO_API void zero_plan_destroy(zero_plan* plan);
+ZERO_API int zero_plan_get_info(const zero_plan* plan, zero_plan_info* out);
+/* out[k] = flat offset of tensor k (n_tensors entries). */
+ZERO_API int zero_plan_tensor_offsets(const zero_plan* plan, int64_t* out);
+/* Copies min(cap, n_segments) segments; ZERO_ERANGE if cap < n_segments. */
+ZERO_API int zero_plan_segments(const zero_plan* plan, zero_segment* out, int32_t cap);
+/* [lo, hi) of bucket k. */
+ZERO_API int zero_plan_bucket_range(const zero_plan* plan, int32_t bucket, int64_t* lo,
+                                    int64_t* hi);
+/* Device workspace bytes zero_reduce_scatter / zero_grad_norm need for the
+ * norm partial sums (one double per tile). */
+ZERO_API size_t zero_workspace_bytes(const zero_plan* plan);
+
+/* ---------------------------------------------------- hyperparameters -- */
+
+typedef struct zero_hparams {
+  double lr, beta1, beta2, eps, weight_decay;
+  double max_grad_norm;     /* > 0: clip to this global L2 norm; <= 0: no clip */
+  int32_t dynamic_scale;    /* 1: halve the loss scale on overflow (floor 1) and
+                               double it after growth_interval good steps */
+  int32_t growth_interval;  /* >= 1 */
+  double init_scale;        /* initial loss scale (1 for bf16 without scaling) */
+} zero_hparams;
+
+/* Device-resident step state. Create it with zero_scaler_init on the host
+ * and copy it to device memory (sizeof(zero_scaler) bytes, 16-byte aligned);
+ * after that only the library's kernels write it. The host may read it back
+ * at any time after synchronizing the stream. */
+typedef struct zero_scaler {
+  float scale;          /* loss scale S_l used to unscale this step's gradients */
+  int32_t good_steps;   /* consecutive non-overflow steps since the last change */
+  int32_t t;            /* optimizer steps applied so far */
+  uint32_t pending;     /* OR of non-finite flags raised in the current step */
+  uint32_t overflow;    /* 1 if the last finished step was skipped */
+  int32_t state_index;  /* current optimizer state set (ping-pong), 0 or 1 */
+  double beta1_pow;     /* beta1^t, formed by t successive products */
+  double beta2_pow;     /* beta2^t */
+  double norm_sq;       /* global sum of squared reduced gradients (last zero_grad_norm) */
+  double norm;          /* sqrt(norm_sq) */
+  float clip_coef;      /* coefficient applied by the last clipped step (1 = none) */
+  int32_t clip_apply;   /* 1 if clip_coef < 1 applies */
+  int32_t norm_step;    /* t + 1 of the step zero_grad_norm was computed for */
+  int32_t n_skipped;    /* steps skipped so far */
+  int32_t error;        /* device error word: 0 = ok, else a ZERO_DEVERR_* code */
+  int32_t reserved;
+} zero_scaler;
+
+/* device error codes written to zero_scaler.error (first error wins) */
+#define ZERO_DEVERR_STATE_INDEX 1   /* state_index outside the given sets */
+#define ZERO_DEVERR_NO_NORM 2       /* clip requested but zero_grad_norm not run */
+
+/* Fill *out (host memory) with the initial scaler: scale = init_scale,
+ * t = 0, beta powers 1, state set 0, all flags clear. */
+ZERO_API int zero_scaler_init(const zero_hparams* hp, zero_scaler* out);
+
+/* -------------------------------------------------------------- the step -- */
+
+/* Pointer conventions shared by the calls below.
+ *   replicas:     host array of N device pointers; replicas[r] points at
+ *                 flat element `window_base` of rank r's 16-bit gradient, and
+ *                 must cover every element of the processed ranks' slices.
+ *                 Padding elements (j >= psi) must hold zeros.
+ *   window_base:  flat index that replicas[r] and flat_params point at
+ *                 (0 for full buffers; i*S when only rank i's slice is held).
+ *   flat_params:  device pointer at flat element window_base of the 16-bit
+ *                 working parameters; rank i writes its slot [i*S, (i+1)*S).
+ *   grad_shards:  host array of N device pointers; grad_shards[i][k] is the
+ *                 fp32 reduced gradient of flat element i*S + k (S floats).
+ *   master, exp_avg, exp_avg_sq: host arrays of n_sets*N device pointers;
+ *                 entry [s*N + i] is rank i's fp32 shard (S floats) of state
+ *                 set s. Entries of ranks outside [rank_lo, rank_hi) may be NULL.
+ *   rank_lo, rank_hi: the owners processed, 0 <= rank_lo < rank_hi <= N.
+ *   d_scaler:     device pointer to the zero_scaler.
+ *   d_bucket_flags: device array of n_buckets uint32 (may be NULL); each
+ *                 call ORs 1 into the flag of every bucket in which it finds
+ *                 a non-finite reduced gradient. The caller clears them.
+ */
+
+/* Reduce-scatter (two-pass path, step 1): for the owners [rank_lo, rank_hi)
+ * and bucket `bucket` (-1 = all buckets), write the unscaled, unclipped
+ * reduced gradient to grad_shards, OR non-finite flags into d_bucket_flags
+ * and d_scaler->pending, and, when d_workspace is not NULL, store the
+ * per-tile squared-norm partial sums there for zero_grad_norm.
+ * Reads 2N bytes and writes 4 bytes per element. */
+ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t rank_lo,
+                                 int32_t rank_hi, const void* const* replicas,
+                                 int64_t window_base, float* const* grad_shards,
+                                 zero_scaler* d_scaler, uint32_t* d_bucket_flags,
+                                 void* d_workspace, void* stream);
+
+/* Global gradient norm and clip coefficient (two-pass path, step 2).
+ * Convention (the pages give none): L2 norm of the unscaled, averaged
+ * gradient over the processed owners' elements; squares accumulated with at
+ * least fp64 accuracy in a fixed order (per tile, then tiles in ascending
+ * order), so the result is deterministic and independent of the grid;
+ * c = max_norm / (norm + 1e-6) in fp64, applied (rounded to fp32) by the next
+ * zero_step only if c < 1.
+ * grad_shards == NULL: use the partials zero_reduce_scatter left in
+ * d_workspace (it must have covered all segments of [rank_lo, rank_hi) in
+ * this step). Otherwise recompute the partials from grad_shards (4 bytes
+ * read per element). Writes norm_sq, norm, clip_coef, clip_apply and
+ * norm_step to d_scaler. hp->max_grad_norm must be > 0. */
+ZERO_API int zero_grad_norm(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                            const float* const* grad_shards, const zero_hparams* hp,
+                            zero_scaler* d_scaler, void* d_workspace, void* stream);
+
+/* One optimizer step for the owners [rank_lo, rank_hi); call it once per
+ * step: it ends by updating the loss scale, t and the skip bookkeeping.
+ *
+ * Fused path (grad_shards == NULL, needs n_sets == 2, no clip): one pass
+ * reads the N replicas and the current state set (d_scaler->state_index),
+ * reduces, unscales, checks, runs AdamW and writes the other state set and
+ * the 16-bit parameters (2N + 26 bytes per element). If any element was
+ * non-finite the step is skipped: the state index stays, and the parameters
+ * are re-cast from the kept master (6 more bytes per element).
+ *
+ * Two-pass path (grad_shards != NULL, after zero_reduce_scatter and, when
+ * hp->max_grad_norm > 0, zero_grad_norm): if the step's overflow word is set
+ * nothing is written; otherwise the current state set is updated in place
+ * from the reduced gradients (times the clip coefficient when it applies)
+ * and the parameters are written (30 bytes per element). n_sets is 1 or 2.
+ *
+ * Errors: ZERO_EINVAL (bad ranges or NULL pointers, fused with clip or with
+ * n_sets != 2), ZERO_EALIGN, ZERO_ECUDA. */
+ZERO_API int zero_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                       float* const* master, float* const* exp_avg, float* const* exp_avg_sq,
+                       int32_t n_sets, const float* const* grad_shards,
+                       const void* const* replicas, int64_t window_base, void* flat_params,
+                       const zero_hparams* hp, zero_scaler* d_scaler,
+                       uint32_t* d_bucket_flags, void* stream);
+
+/* zero_step in two calls, for callers that want to place their own work (or
+ * timing events) between the update and the bookkeeping. zero_step(...) is
+ * exactly zero_step_update(...) followed by zero_step_finish(...) with the
+ * same arguments.
+ * zero_step_update launches the update kernel of the chosen path (fused or
+ * two-pass) and nothing else. zero_step_finish re-casts the parameters from
+ * the kept master set if the fused step overflowed, then updates the loss
+ * scale, t, the state index and the skip count. grad_shards only selects
+ * the path (NULL = fused) in zero_step_finish; replicas may be NULL there. */
+ZERO_API int zero_step_update(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                              float* const* master, float* const* exp_avg,
+                              float* const* exp_avg_sq, int32_t n_sets,
+                              const float* const* grad_shards, const void* const* replicas,
+                              int64_t window_base, void* flat_params, const zero_hparams* hp,
+                              zero_scaler* d_scaler, uint32_t* d_bucket_flags, void* stream);
+ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                              float* const* master, int32_t n_sets,
+                              const float* const* grad_shards, int64_t window_base,
+                              void* flat_params, const zero_hparams* hp, zero_scaler* d_scaler,
+                              void* stream);
+
+/* Write the 16-bit working copy of the owners' slices from one fp32 master
+ * set (round to nearest even): master[i] is rank i's shard (N entries).
+ * Used to initialise the parameters; 6 bytes per element. */
+ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                              const float* const* master, void* flat_params,
+                              int64_t window_base, void* stream);
+
+/* Kernels launched per call, for accounting (L = ceil(segments processed /
+ * 128), empty launches skipped): fused zero_step 2L + 1 (update, overflow
+ * re-cast check, bookkeeping), two-pass zero_step L + 1, zero_reduce_scatter
+ * L, zero_grad_norm 1 (+ L when it recomputes the partials), zero_cast_params L. */
+
+ZERO_API const char* zero_strerror(int status);
+/* Library version: major * 10000 + minor * 100 + patch. */
+ZERO_API int zero_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_H */

@@ -100,62 +100,74 @@ double orc_ring_bytes(double m_bytes, int32_t d) {
 
 /* ================================================================ casts ==== */
 
-/* Round |x| (finite, fp32) to a multiple of the quantum 2^qexp, ties to even.
- * Returns the integer multiple as a double (exact: x has <= 24 significant
- * bits and the quantum is a power of two). */
-static double round_to_quantum(double a, int qexp) {
-  double n = ldexp(a, -qexp);
-  double fl = floor(n);
-  double rem = n - fl;
-  if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) == 1.0)) fl += 1.0;
-  return fl;
-}
-
-/* Generic encoder for a binary format with `ebits` exponent bits, `mbits`
- * fraction bits, bias 2^(ebits-1)-1. */
+/* Encoder for a binary format with `ebits` exponent bits, `mbits` fraction
+ * bits and bias 2^(ebits-1)-1, from the IEEE 754 definition: write the fp32
+ * input as sig * 2^q with an integer significand, pick the target exponent
+ * Et = max(floor(log2 |x|), emin), keep the multiple n of the quantum
+ * 2^(Et - mbits) nearest to |x| (ties to the even multiple), carry into the
+ * next binade when n reaches 2^(mbits+1), overflow to infinity above the
+ * largest exponent, and encode n as a subnormal (n < 2^mbits) or normal. */
 static uint16_t encode_small_float(float x, int ebits, int mbits) {
-  uint32_t xb;
-  memcpy(&xb, &x, 4);
-  uint16_t sign = (uint16_t)((xb >> 31) << (ebits + mbits));
-  uint16_t exp_all = (uint16_t)(((1u << ebits) - 1u) << mbits);
-  if (isnan(x)) return (uint16_t)(sign | exp_all | (1u << (mbits - 1))); /* quiet NaN */
-  if (isinf(x)) return (uint16_t)(sign | exp_all);
-  double a = fabs((double)x);
-  if (a == 0.0) return sign;
-  int bias = (1 << (ebits - 1)) - 1;
-  int emin = 1 - bias;                 /* exponent of the smallest normal */
-  int emax = bias;                     /* exponent of the largest finite */
-  int e;
-  frexp(a, &e);                        /* a = f * 2^e, f in [0.5, 1) */
-  int E = e - 1;                       /* floor(log2 a) */
-  if (E < emin) E = emin;              /* subnormal range: fixed quantum */
-  double n = round_to_quantum(a, E - mbits);
-  double one = ldexp(1.0, mbits);      /* the implicit leading bit */
-  if (n >= 2.0 * one) {                /* rounded up into the next binade */
-    n = n / 2.0;
-    E += 1;
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  const uint32_t sign = (u >> 31) << (ebits + mbits);
+  const uint32_t exp_all = ((1u << ebits) - 1u) << mbits;
+  const uint32_t e32 = (u >> 23) & 0xFFu;
+  const uint32_t f32 = u & 0x7FFFFFu;
+  if (e32 == 0xFFu) /* infinity, or NaN made quiet */
+    return (uint16_t)(f32 ? (sign | exp_all | (1u << (mbits - 1))) : (sign | exp_all));
+  if (e32 == 0 && f32 == 0) return (uint16_t)sign;
+  const int bias = (1 << (ebits - 1)) - 1;
+  const int emin = 1 - bias, emax = bias;
+  /* |x| = sig * 2^q */
+  uint32_t sig = e32 ? (f32 | 0x800000u) : f32;
+  int q = e32 ? (int)e32 - 127 - 23 : -126 - 23;
+  int nb = 0;
+  for (uint32_t t = sig; t; t >>= 1) ++nb; /* bit length of sig */
+  int Et = q + nb - 1;
+  if (Et < emin) Et = emin;
+  int shift = (Et - mbits) - q; /* low bits of sig below the quantum */
+  uint32_t n;
+  if (shift <= 0) {
+    n = sig << (-shift);
+  } else if (shift >= 25) {
+    n = 0; /* below half a quantum (sig < 2^24) */
+  } else {
+    n = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (n & 1u))) n += 1;
   }
-  if (E > emax) return (uint16_t)(sign | exp_all); /* overflow -> infinity */
-  if (n < one) return (uint16_t)(sign | (uint16_t)n); /* subnormal (E == emin) */
-  uint16_t efield = (uint16_t)(E + bias);
-  uint16_t frac = (uint16_t)(n - one);
-  return (uint16_t)(sign | (uint16_t)(efield << mbits) | frac);
+  if (n == (2u << mbits)) { /* rounded up into the next binade */
+    n >>= 1;
+    Et += 1;
+  }
+  if (Et > emax) return (uint16_t)(sign | exp_all);
+  if (n < (1u << mbits)) return (uint16_t)(sign | n); /* subnormal or zero */
+  return (uint16_t)(sign | ((uint32_t)(Et + bias) << mbits) | (n - (1u << mbits)));
 }
 
+/* Decoder: subnormals are frac * 2^(emin - mbits) (exact in fp32), normals
+ * get the fp32 exponent field e - bias + 127 and the fraction shifted into
+ * the top of fp32's 23 fraction bits. */
 static float decode_small_float(uint16_t h, int ebits, int mbits) {
-  int bias = (1 << (ebits - 1)) - 1;
-  uint32_t sign = (h >> (ebits + mbits)) & 1u;
-  uint32_t ef = (h >> mbits) & ((1u << ebits) - 1u);
-  uint32_t fr = h & ((1u << mbits) - 1u);
-  double v;
+  const int bias = (1 << (ebits - 1)) - 1;
+  const uint32_t sign = ((uint32_t)h >> (ebits + mbits)) & 1u;
+  const uint32_t ef = ((uint32_t)h >> mbits) & ((1u << ebits) - 1u);
+  const uint32_t fr = (uint32_t)h & ((1u << mbits) - 1u);
+  uint32_t bits;
   if (ef == (1u << ebits) - 1u) {
-    v = fr ? NAN : INFINITY;
+    bits = 0x7F800000u | (fr << (23 - mbits));
   } else if (ef == 0) {
-    v = ldexp((double)fr, 1 - bias - mbits);
+    float mag = (float)fr * ldexpf(1.0f, 1 - bias - mbits);
+    memcpy(&bits, &mag, 4);
   } else {
-    v = ldexp((double)(fr + (1u << mbits)), (int)ef - bias - mbits);
+    bits = ((ef - (uint32_t)bias + 127u) << 23) | (fr << (23 - mbits));
   }
-  return (float)(sign ? -v : v);
+  bits |= sign << 31;
+  float out;
+  memcpy(&out, &bits, 4);
+  return out;
 }
 
 uint16_t orc_f32_to_f16(float x) { return encode_small_float(x, 5, 10); }
@@ -353,23 +365,34 @@ int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t
 
 /* ---------------------------------------------- generator-driven driver ---- */
 
-static float gen_value(const orc_gen* g, float scale, uint32_t step, int32_t rank, int64_t j) {
+/* Replica value of flat element j for every rank, widened to fp32. The
+ * per-(step, rank) generator streams are formed once per call site. */
+static float gen_value(const orc_gen* g, const zs_grad_stream* st, uint32_t step, int32_t rank,
+                       int64_t j) {
   uint16_t bits;
   if (g->inject_step >= 0 && (uint32_t)g->inject_step == step && g->inject_rank == rank &&
       g->inject_elem == j) {
     bits = (uint16_t)g->inject_bits;
   } else {
-    zs_grad_spec spec = g->spec;
-    spec.loss_scale = scale;
-    bits = cast16(zs_grad_value(&spec, step, (uint32_t)rank, j), g->is_bf16);
+    bits = cast16(zs_grad_stream_value(st, j), g->is_bf16);
   }
   return widen16(bits, g->is_bf16);
 }
 
-static float gen_ghat(const orc_plan* p, const orc_gen* g, float scale, float inv,
+static zs_grad_stream* make_streams(const orc_plan* p, const orc_gen* g, float scale,
+                                    uint32_t step) {
+  zs_grad_stream* st = (zs_grad_stream*)malloc((size_t)p->n_ranks * sizeof(zs_grad_stream));
+  if (!st) return NULL;
+  zs_grad_spec spec = g->spec;
+  spec.loss_scale = scale;
+  for (int32_t r = 0; r < p->n_ranks; ++r) st[r] = zs_grad_stream_make(&spec, step, (uint32_t)r);
+  return st;
+}
+
+static float gen_ghat(const orc_plan* p, const orc_gen* g, const zs_grad_stream* st, float inv,
                       uint32_t step, int64_t j, float* vals) {
   int32_t N = p->n_ranks;
-  for (int32_t r = 0; r < N; ++r) vals[r] = gen_value(g, scale, step, r, j);
+  for (int32_t r = 0; r < N; ++r) vals[r] = gen_value(g, &st[r], step, r, j);
   float acc = orc_ring_sum(vals, N, (int32_t)(j / p->shard));
   return acc * inv;
 }
@@ -377,8 +400,9 @@ static float gen_ghat(const orc_plan* p, const orc_gen* g, float scale, float in
 typedef struct pass_job {
   const orc_plan* p;
   const orc_gen* g;
+  const zs_grad_stream* st;
   uint32_t step;
-  float scale, inv;
+  float inv;
   int64_t lo, hi, n_chunks;
   int32_t worker, n_workers;
   double* chunk_sq;         /* per chunk */
@@ -397,7 +421,7 @@ static void* pass_worker(void* arg) {
     double part = 0.0;
     int32_t bad = 0;
     for (int64_t j = a; j < b; ++j) {
-      float gj = gen_ghat(p, J->g, J->scale, J->inv, J->step, j, vals);
+      float gj = gen_ghat(p, J->g, J->st, J->inv, J->step, j, vals);
       if (!isfinite(gj)) {
         bad = 1;
         flags[bucket_of(p, j)] |= 1u;
@@ -429,15 +453,20 @@ int orc_gen_step(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, const orc_
   pass_job* jobs = (pass_job*)calloc((size_t)n_threads, sizeof(pass_job));
   pthread_t* th = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
   float* vals = (float*)malloc((size_t)p->n_ranks * sizeof(float));
+  zs_grad_stream* streams = NULL;
   int rc = 0;
   if (!chunk_sq || !chunk_bad || !wflags || !jobs || !th || !vals) {
     rc = -1;
     goto done;
   }
-  const float scale = sc->scale;
-  const float inv = orc_unscale_factor(scale, p->n_ranks);
+  const float inv = orc_unscale_factor(sc->scale, p->n_ranks);
+  streams = make_streams(p, g, sc->scale, step);
+  if (!streams) {
+    rc = -1;
+    goto done;
+  }
   for (int32_t w = 0; w < n_threads; ++w) {
-    pass_job J = {p, g, step, scale, inv, lo, hi, n_chunks, w, n_threads, chunk_sq, chunk_bad, wflags};
+    pass_job J = {p, g, streams, step, inv, lo, hi, n_chunks, w, n_threads, chunk_sq, chunk_bad, wflags};
     jobs[w] = J;
   }
   for (int32_t w = 1; w < n_threads; ++w) pthread_create(&th[w], NULL, pass_worker, &jobs[w]);
@@ -473,7 +502,7 @@ int orc_gen_step(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, const orc_
       rc = -1;
       goto done;
     }
-    float gj = gen_ghat(p, g, scale, inv, step, j, vals);
+    float gj = gen_ghat(p, g, streams, inv, step, j, vals);
     if (apply) gj = gj * coef;
     orc_adamw_elem(&master[k], &m[k], &v[k], gj, &a);
     params[k] = cast16(master[k], g->is_bf16);
@@ -486,6 +515,7 @@ done:
   free(jobs);
   free(th);
   free(vals);
+  free(streams);
   return rc;
 }
 
@@ -493,9 +523,15 @@ int orc_gen_ghat(const orc_plan* p, const orc_gen* g, uint32_t step, float scale
                  const int64_t* elems, int64_t n_elems, float* ghat) {
   if (!p || !g || !ghat) return -1;
   float* vals = (float*)malloc((size_t)p->n_ranks * sizeof(float));
-  if (!vals) return -1;
+  zs_grad_stream* st = make_streams(p, g, scale, step);
+  if (!vals || !st) {
+    free(vals);
+    free(st);
+    return -1;
+  }
   const float inv = orc_unscale_factor(scale, p->n_ranks);
-  for (int64_t k = 0; k < n_elems; ++k) ghat[k] = gen_ghat(p, g, scale, inv, step, elems[k], vals);
+  for (int64_t k = 0; k < n_elems; ++k) ghat[k] = gen_ghat(p, g, st, inv, step, elems[k], vals);
   free(vals);
+  free(st);
   return 0;
 }

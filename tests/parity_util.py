@@ -1,0 +1,208 @@
+"""Shared helpers of the GPU parity tests: run a workload through libzero and
+through the CPU checker on the same seeded inputs and compare."""
+import numpy as np
+import torch
+
+import oracle
+from fsdp_sharded_mixed_shard_gb300 import harness, synth
+
+F32 = np.float32
+
+# acceptance bars
+MASTER_REL = 1e-6        # fp32 master / exp_avg / exp_avg_sq: max relative error
+PARAM_EXACT_FRAC = 0.9999
+PARAM_MAX_ULP = 1
+
+
+def oracle_hp(wl):
+    return oracle.hparams(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                          weight_decay=wl.weight_decay, max_grad_norm=wl.max_grad_norm,
+                          dynamic_scale=int(wl.dynamic_scale),
+                          growth_interval=wl.growth_interval)
+
+
+def rel_err(got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    d = np.abs(got - want) / np.maximum(np.abs(want), np.finfo(np.float64).tiny)
+    d[same] = 0.0
+    return float(d.max()) if d.size else 0.0
+
+
+def ulp_diff16(a, b):
+    """Distance in representable 16-bit values (same-sign encodings)."""
+    a = np.asarray(a, np.int64)
+    b = np.asarray(b, np.int64)
+
+    def ordered(x):
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+
+    return np.abs(ordered(a) - ordered(b))
+
+
+def assert_params(got, want):
+    got = np.asarray(got, np.uint16)
+    want = np.asarray(want, np.uint16)
+    if got.size == 0:
+        return
+    exact = (got == want).mean()
+    assert exact >= PARAM_EXACT_FRAC, "params exact fraction %.6f" % exact
+    assert ulp_diff16(got, want).max() <= PARAM_MAX_ULP
+
+
+def assert_state(got, want, what):
+    e = rel_err(got, want)
+    assert e <= MASTER_REL, "%s max rel err %.3g" % (what, e)
+
+
+def norm_tol(n_elems):
+    # both sides sum squares in fp64 in different fixed orders: each within
+    # (n-1) u of the exact sum (u = 2^-53), the device's float-float tile
+    # sums within 2^-43
+    return (2.0 * n_elems * 2.0 ** -53 + 2.0 ** -43)
+
+
+def compare_scaler(dev, orc, n_elems, clip):
+    assert dev.t == orc.t, (dev.t, orc.t)
+    assert dev.scale == orc.scale, (dev.scale, orc.scale)
+    assert dev.overflow == orc.overflow
+    assert dev.good_steps == orc.good_steps
+    assert dev.error == 0
+    if clip and not orc.overflow:
+        assert abs(dev.norm_sq - orc.norm_sq) <= norm_tol(n_elems) * orc.norm_sq
+        if dev.clip_coef != orc.clip_coef:
+            # only a norm at an fp32 rounding boundary may move c by one ulp
+            assert abs(float(dev.clip_coef) - float(orc.clip_coef)) <= \
+                2.0 ** -23 * abs(float(orc.clip_coef))
+
+
+def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True):
+    """Full element-wise comparison over every step of `wl`. Returns the
+    per-step max relative errors for reporting."""
+    g = harness.Group(wl, two_pass=two_pass)
+    try:
+        g.init_state()
+        p, _, _ = oracle.make_plan(wl.numels, wl.n_ranks, wl.bucket_elems)
+        lo, hi = wl.ranks
+        S = p.shard
+        wbase, wlen = lo * S, (hi - lo) * S
+        bf = wl.is_bf16
+        hp = oracle_hp(wl)
+        sc = oracle.scaler(wl.init_scale)
+        master = synth.master_f32(wlen, wbase, wl.seed, wl.psi)
+        m = np.zeros(wlen, F32)
+        v = np.zeros(wlen, F32)
+        params = oracle.cast16(master, bf)
+        assert np.array_equal(g.params_u16(), params), "initial working copy"
+        stats = []
+        for step in range(1, wl.steps + 1):
+            spec = synth.grad_spec(seed=wl.seed, sigma=wl.sigma, bias_sigma=wl.bias_sigma,
+                                   loss_scale=sc.scale, outliers=wl.outliers, psi=wl.psi)
+            reps = [oracle.cast16(synth.grad_f32(wlen, wbase, spec, step, r), bf)
+                    for r in range(wl.n_ranks)]
+            if wl.inject is not None and wl.inject[0] == step:
+                _, r, e, bits = wl.inject
+                if wbase <= e < wbase + wlen:
+                    reps[r][e - wbase] = bits
+            g.gen_grads(step)
+            g.step(per_bucket=per_bucket)
+            flags = np.zeros(max(p.n_buckets, 1), np.uint32)
+            oracle.step_arrays(p, lo, hi, bf, reps, wbase, master, m, v, params, hp, sc, flags)
+            if check_replicas and wlen:
+                assert np.array_equal(g.replicas_u16(), np.stack(reps)), "generator parity"
+            dev = g.read_scaler()
+            compare_scaler(dev, sc, wlen, wl.max_grad_norm > 0)
+            assert np.array_equal(g.flags_u32(), flags[:p.n_buckets])
+            gm, gmm, gv = (t.numpy() for t in g.current_state())
+            assert_state(gm, master, "master")
+            assert_state(gmm, m, "exp_avg")
+            assert_state(gv, v, "exp_avg_sq")
+            assert_params(g.params_u16(), params)
+            stats.append((rel_err(gm, master), rel_err(gmm, m), rel_err(gv, v),
+                          float((g.params_u16() == params).mean()) if wlen else 1.0))
+        return stats, g.read_scaler(), sc
+    finally:
+        g.close()
+        del g
+        torch.cuda.empty_cache()
+
+
+def sample_elems(wl, p, n_random=2048, seed=0):
+    """Sampled flat indices inside the processed owners' slices: slice and
+    bucket edges, padding, the injected element, and random ones."""
+    lo, hi = wl.ranks
+    a, b = lo * p.shard, hi * p.shard
+    pts = set()
+    for i in range(lo, hi + 1):
+        for d in (-9, -8, -1, 0, 1, 7, 8):
+            pts.add(i * p.shard + d)
+    if p.bucket_elems:
+        for k in range(1, p.n_buckets):
+            for d in (-1, 0, 1):
+                pts.add(k * p.bucket_elems + d)
+    for d in (-2, -1, 0, 1):
+        pts.add(p.psi + d)
+    if wl.inject is not None:
+        pts.add(wl.inject[2])
+    rng = np.random.default_rng(seed)
+    if b > a:
+        pts.update(rng.integers(a, b, n_random).tolist())
+    e = np.array(sorted(x for x in pts if a <= x < b), dtype=np.int64)
+    return e
+
+
+def gather_state(g, elems):
+    idx_set = g.read_scaler().state_index if g.n_sets == 2 else 0
+    i = elems // g.S
+    k = elems - i * g.S
+    flat_idx = torch.from_numpy((i - g.lo) * g.srow + k).to(g.device)
+    out = []
+    for which in range(3):
+        t = g.state[idx_set, which].reshape(-1)
+        out.append(t.index_select(0, flat_idx).cpu().numpy())
+    w = torch.from_numpy(elems - g.wbase).to(g.device)
+    params = g.flat.index_select(0, w).cpu().numpy().view(np.uint16)
+    return out[0], out[1], out[2], params
+
+
+def run_sampled(wl, steps=None, n_random=2048, n_threads=None):
+    """Full-size run on the device; the checker regenerates every input on
+    the host, computes the global quantities (flags, overflow, norm) over all
+    elements and the updates of the sampled elements."""
+    steps = wl.steps if steps is None else steps
+    g = harness.Group(wl)
+    try:
+        g.init_state()
+        p, _, _ = oracle.make_plan(wl.numels, wl.n_ranks, wl.bucket_elems)
+        elems = sample_elems(wl, p, n_random)
+        bf = wl.is_bf16
+        hp = oracle_hp(wl)
+        sc = oracle.scaler(wl.init_scale)
+        master = synth.master_f32_at(elems, wl.seed, wl.psi)
+        m = np.zeros(len(elems), F32)
+        v = np.zeros(len(elems), F32)
+        params = oracle.cast16(master, bf)
+        spec = synth.grad_spec(seed=wl.seed, sigma=wl.sigma, bias_sigma=wl.bias_sigma,
+                               loss_scale=1.0, outliers=wl.outliers, psi=wl.psi)
+        gen = oracle.gen(spec, bf, wl.inject)
+        lo, hi = wl.ranks
+        for step in range(1, steps + 1):
+            g.gen_grads(step)
+            g.step()
+            flags = np.zeros(max(p.n_buckets, 1), np.uint32)
+            oracle.gen_step(p, lo, hi, gen, step, elems, master, m, v, params, hp, sc, flags,
+                            n_threads=n_threads)
+            dev = g.read_scaler()
+            compare_scaler(dev, sc, (hi - lo) * p.shard, wl.max_grad_norm > 0)
+            assert np.array_equal(g.flags_u32(), flags[:p.n_buckets])
+            gm, gmm, gv, gp = gather_state(g, elems)
+            assert_state(gm, master, "master")
+            assert_state(gmm, m, "exp_avg")
+            assert_state(gv, v, "exp_avg_sq")
+            assert_params(gp, params)
+        return g.read_scaler(), sc
+    finally:
+        g.close()
+        del g
+        torch.cuda.empty_cache()

@@ -1,0 +1,123 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/zero.h declares, struct layouts agree with the Python mirrors, and the
+planner matches the CPU checker's planner bit for bit."""
+import ctypes as C
+import os
+import random
+import re
+import subprocess
+
+import pytest
+
+import oracle
+import fsdp_sharded_mixed_shard_gb300 as Z
+from fsdp_sharded_mixed_shard_gb300 import _build, workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"ZERO_API\s+[\w\s\*]+?\b(zero_\w+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert {"zero_plan_create", "zero_reduce_scatter", "zero_grad_norm", "zero_step"} <= names
+    L = C.CDLL(_build.ZERO_LIB)
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.ZERO_LIB], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r" T (zero_\w+)", out))
+    assert names <= exported
+    assert exported <= names, "exported but undeclared: %s" % (exported - names)
+
+
+def test_struct_sizes():
+    assert C.sizeof(Z.ZeroScaler) == 80
+    assert C.sizeof(Z.ZeroPlanInfo) == 168
+    assert C.sizeof(Z.ZeroHParams) == 64
+    assert C.sizeof(Z.ZeroSegment) == 24
+
+
+def _compare(numels, n, bsz, dtype=Z.ZERO_BF16):
+    p = Z.zero_plan_create(numels, n, bsz, dtype)
+    try:
+        info = Z.zero_plan_get_info(p)
+        op, ooffs, osegs = oracle.make_plan(numels, n, bsz)
+        assert (info.psi, info.pad, info.psi_pad, info.shard_elems, info.n_buckets,
+                info.n_segments) == (op.psi, op.pad, op.psi_pad, op.shard, op.n_buckets,
+                                     op.n_segments)
+        assert Z.zero_plan_tensor_offsets(p) == list(ooffs)
+        assert Z.zero_plan_segments(p) == [tuple(s) for s in osegs]
+        for k in range(info.n_buckets):
+            lo, hi = Z.zero_plan_bucket_range(p, k)
+            assert lo == (k * bsz if bsz else 0)
+            assert hi == (min((k + 1) * bsz, info.psi_pad) if bsz else info.psi_pad)
+        for a, b in ((info.bill_ddp, op.bill_ddp), (info.bill_z1, op.bill_z1),
+                     (info.bill_z2, op.bill_z2), (info.bill_z3, op.bill_z3),
+                     (info.ring_bytes_per_rank, op.ring_bytes_per_rank),
+                     (info.ring_hops, op.ring_hops), (info.comm_elems_z3, op.comm_z3)):
+            assert a == pytest.approx(b, rel=1e-15, abs=0)
+        assert info.step_bytes_fused == 2 * n + 26
+        assert info.n_tiles == sum(-(-(hi - lo) // Z.ZERO_TILE_ELEMS) for lo, hi, _, _ in osegs)
+        assert Z.zero_workspace_bytes(p) >= info.n_tiles * 8
+    finally:
+        Z.zero_plan_destroy(p)
+
+
+def test_planner_matches_checker_on_workloads():
+    for wl in W.ALL:
+        _compare(wl.numels, wl.n_ranks, wl.bucket_elems)
+
+
+def test_planner_matches_checker_random():
+    rng = random.Random(7)
+    for _ in range(400):
+        n = rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 16, 63, 64])
+        numels = [rng.choice([0, 1, 2, 5, 31, 4096, 10007]) for _ in range(rng.randint(0, 7))]
+        bsz = rng.choice([0, 1, 2, 7, 64, 1000, 4096, 99991])
+        _compare(numels, n, bsz)
+
+
+def test_planner_rejects_bad_arguments():
+    for args, status in ((([10], 0, 0), -1), (([10], 65, 0), -3), (([-1], 2, 0), -1),
+                         (([10], 2, -3), -1)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_plan_create(*args)
+        assert e.value.status == status
+    with pytest.raises(Z.ZeroError):
+        Z.zero_plan_create([10], 2, 0, 7)
+
+
+def test_scaler_init_and_strerror():
+    hp = Z.ZeroHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 0.0, 1, 2000, 65536.0)
+    s = Z.zero_scaler_init(hp)
+    assert s.scale == 65536.0 and s.t == 0 and s.beta1_pow == 1.0 and s.state_index == 0
+    assert Z.zero_strerror(-2).startswith("device pointer")
+    assert Z.zero_version() >= 100
+    bad = Z.ZeroHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 0.0, 1, 0, 65536.0)
+    with pytest.raises(Z.ZeroError):
+        Z.zero_scaler_init(bad)
+
+
+def test_host_validation_without_gpu():
+    """Argument checks run before any CUDA call, so they work on a CPU host."""
+    p = Z.zero_plan_create([1000], 4, 0)
+    hp = Z.ZeroHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 0.0, 0, 2000, 1.0)
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_step(p, 0, 5, [None] * 8, [None] * 8, [None] * 8, 2, None, [None] * 4, 0, 16, hp,
+                    16)
+    assert e.value.status == -1
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_step(p, 0, 4, [16] * 8, [16] * 8, [16] * 8, 2, None, [16] * 4, 0, 24, hp, 16)
+    assert e.value.status == -2
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm(p, 0, 4, None, hp, 16, 16)
+    assert e.value.status == -1
+    Z.zero_plan_destroy(p)

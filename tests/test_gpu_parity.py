@@ -1,0 +1,174 @@
+"""GPU parity: libzero's kernels against the CPU checker, element by element,
+on the same seeded inputs (sizes the checker finishes in seconds, spanning
+many tiles and ragged tails), plus edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fsdp_sharded_mixed_shard_gb300 import harness, workloads as W
+from parity_util import run_small
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def tiny_transformer_numels(d=64, vocab=503, ctx=128, layers=3):
+    out = [vocab * d, ctx * d]
+    for _ in range(layers):
+        out += [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
+    return out + [d, d]
+
+
+def test_tiny_flat_full_size():
+    """1,000,003 parameters, 4 ranks (odd shard: scalar path for ranks 1-3),
+    fp16 gradients under a static loss scale of 1024, 3 steps, fused path."""
+    stats, dev, orc = run_small(W.TINY_FLAT)
+    assert dev.t == 3
+
+
+def test_gpt2_shaped_small_fused():
+    wl = W.GPT2_SMALL.scaled(numels=tiny_transformer_numels(), bucket_elems=50_000, steps=4)
+    run_small(wl)
+
+
+def test_gpt2_shaped_small_two_pass_per_bucket():
+    wl = W.GPT2_SMALL.scaled(numels=tiny_transformer_numels(), bucket_elems=50_000, steps=3)
+    run_small(wl, per_bucket=True, two_pass=True)
+
+
+def test_flat_fp16_dynamic_clip_inject():
+    """fp16 under a dynamic scale of 65536, clip 1.0, +inf injected at step 3
+    in rank 5: the step is skipped and the scale halves."""
+    psi = 1_000_003
+    wl = W.FLAT_1P5B.scaled(numels=[psi], inject=(3, 5, psi // 3, W.FP16_POS_INF))
+    stats, dev, orc = run_small(wl)
+    assert dev.t == 4 and dev.scale == 32768.0 and dev.n_skipped == 1
+
+
+def test_flat_fp16_inject_fused_skip_recast():
+    """Same injection on the fused path: the speculative pass writes the other
+    state set and the parameters; the skip re-casts them from the kept set."""
+    psi = 1_000_003
+    wl = W.FLAT_1P5B.scaled(numels=[psi], max_grad_norm=0.0,
+                            inject=(2, 5, psi // 3, W.FP16_POS_INF), steps=3)
+    stats, dev, orc = run_small(wl)
+    assert dev.t == 2 and dev.scale == 32768.0
+
+
+@pytest.mark.parametrize("rank", [0, 5])
+def test_stage3_slice_small(rank):
+    S = 20011  # odd: rank 5's window starts off the 16-byte grid
+    wl = W.STAGE3_SLICE.scaled(numels=[64 * S], rank_lo=rank, rank_hi=rank + 1, steps=3)
+    run_small(wl)
+
+
+def test_llama_shaped_small_outliers_clip():
+    d, f, v = 128, 512, 1000
+    numels = [v * d]
+    for _ in range(2):
+        numels += [d, d * d, d * d, d * d, d * d, d, d * f, d * f, f * d]
+    numels += [d]
+    wl = W.LLAMA_2B.scaled(numels=numels, bucket_elems=100_000, steps=3)
+    run_small(wl, per_bucket=True)
+
+
+@pytest.mark.parametrize("n,numels,bucket,bf16,two_pass", [
+    (1, [4099], 0, True, False),             # one rank: identity reduction
+    (3, [1001, 7], 0, False, True),          # non power-of-two N, two-pass, no clip
+    (3, [2], 0, True, False),                # psi < N: mostly padding
+    (4, [0, 5, 0, 3], 0, True, False),       # empty tensors in the list
+    (4, [300], 1, True, True),               # 300 one-element buckets: > 128 segments
+    (5, [12345], 7, False, False),           # odd bucket size, misaligned segments
+    (8, [8 * 4096 * 3 + 17], 0, True, False),  # several tiles per rank plus a tail
+    (16, [16 * 4096 - 3], 50_000, True, True),
+])
+def test_edge_shapes(n, numels, bucket, bf16, two_pass):
+    wl = W.Workload("edge", numels, n, bucket, bf16, 11, 1e-3,
+                    init_scale=1.0 if bf16 else 1024.0, steps=3)
+    run_small(wl, two_pass=two_pass)
+
+
+@pytest.mark.parametrize("bits", [0x7C00, 0xFC00, 0x7E00])
+@pytest.mark.parametrize("where", ["first", "last", "pad", "bucket_edge"])
+@pytest.mark.parametrize("two_pass", [False, True])
+def test_nonfinite_injection(bits, where, two_pass):
+    n, psi, bsz = 4, 40_001, 8192
+    psip = psi + (-psi) % n
+    e = {"first": 0, "last": psi - 1, "pad": psip - 1, "bucket_edge": 2 * bsz}[where]
+    wl = W.Workload("inject", [psi], n, bsz, False, 13, 1e-4, init_scale=4096.0,
+                    dynamic_scale=True, steps=3, inject=(2, 1, e, bits))
+    stats, dev, orc = run_small(wl, two_pass=two_pass)
+    assert dev.t == 2 and dev.scale == 2048.0 and dev.overflow == 0
+
+
+def test_clip_inactive_equals_no_clip():
+    wl = W.Workload("clipbig", [70_001], 4, 0, True, 21, 1e-3, max_grad_norm=1e9, steps=2)
+    stats, dev, orc = run_small(wl)
+    assert dev.clip_apply == 0
+
+
+def test_clip_active_two_pass_recomputed_norm():
+    """zero_grad_norm recomputing the partials from the reduced gradients
+    gives the same result as the partials left by zero_reduce_scatter."""
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    wl = W.Workload("clipnorm", [200_003], 4, 30_000, True, 22, 1e-2, max_grad_norm=0.5,
+                    steps=1)
+    g = harness.Group(wl)
+    g.init_state()
+    g.gen_grads(1)
+    sc, ws, st = g.scaler.data_ptr(), g.workspace.data_ptr(), g.sptr
+    Z.zero_reduce_scatter(g.plan, -1, 0, 4, g.rep_ptrs(), 0, g.ghat_ptrs(), sc, 0, ws, st)
+    Z.zero_grad_norm(g.plan, 0, 4, None, g.hp, sc, ws, st)
+    a = g.read_scaler()
+    Z.zero_grad_norm(g.plan, 0, 4, g.ghat_ptrs(), g.hp, sc, ws, st)
+    b = g.read_scaler()
+    assert a.norm_sq == b.norm_sq and a.clip_coef == b.clip_coef and a.clip_apply == 1
+    g.close()
+
+
+def test_abi_rejects_bad_arguments():
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    wl = W.Workload("bad", [1000], 4, 0, True, 1, 1e-3, steps=1)
+    g = harness.Group(wl)
+    g.init_state()
+    m, v, w = g._state_ptrs(0), g._state_ptrs(1), g._state_ptrs(2)
+    sc = g.scaler.data_ptr()
+    with pytest.raises(Z.ZeroError) as e:   # fused with clip
+        hp = harness.hparams_of(wl.scaled(max_grad_norm=1.0))
+        Z.zero_step(g.plan, 0, 4, m, v, w, 2, None, g.rep_ptrs(), 0, g.flat.data_ptr(), hp, sc)
+    assert e.value.status == -1
+    with pytest.raises(Z.ZeroError) as e:   # misaligned replica
+        reps = g.rep_ptrs()
+        reps[1] += 2
+        Z.zero_step(g.plan, 0, 4, m, v, w, 2, None, reps, 0, g.flat.data_ptr(), g.hp, sc)
+    assert e.value.status == -2
+    with pytest.raises(Z.ZeroError):        # bad rank range
+        Z.zero_step(g.plan, 2, 1, m, v, w, 2, None, g.rep_ptrs(), 0, g.flat.data_ptr(), g.hp, sc)
+    with pytest.raises(Z.ZeroError):        # clip without zero_grad_norm is caught on device
+        pass
+    g.close()
+
+
+def test_missing_norm_sets_device_error():
+    """Two-pass step with clip but no zero_grad_norm in this step: the kernel
+    writes nothing and records ZERO_DEVERR_NO_NORM."""
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    wl = W.Workload("nonorm", [5000], 2, 0, True, 1, 1e-3, max_grad_norm=1.0, steps=1)
+    g = harness.Group(wl)
+    g.init_state()
+    g.gen_grads(1)
+    before = g.state.clone()
+    sc = g.scaler.data_ptr()
+    Z.zero_reduce_scatter(g.plan, -1, 0, 2, g.rep_ptrs(), 0, g.ghat_ptrs(), sc, 0, 0, g.sptr)
+    Z.zero_step(g.plan, 0, 2, g._state_ptrs(0), g._state_ptrs(1), g._state_ptrs(2), 1,
+                g.ghat_ptrs(), None, 0, g.flat.data_ptr(), g.hp, sc, 0, g.sptr)
+    s = g.read_scaler()
+    assert s.error == 2
+    assert torch.equal(before, g.state)
+    g.close()

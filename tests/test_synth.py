@@ -68,3 +68,16 @@ def test_master_range_and_padding():
     assert y.min() > -0.05 and y.max() < 0.05 and abs(y.mean()) < 2e-4
     spec = synth.grad_spec(seed=1, psi=10)
     assert np.all(synth.grad_f32(20, 0, spec, 1, 0)[10:] == 0)
+
+
+def test_stream_form_matches_direct_form():
+    import ctypes as C
+    L = synth.host()
+    L.zs_host_fill_grad_stream.argtypes = [C.c_void_p, C.c_int64, C.c_int64,
+                                           C.POINTER(synth.GradSpec), C.c_uint32, C.c_uint32]
+    for kw in (dict(), dict(bias_sigma=1e-5), dict(outliers=True, loss_scale=65536.0)):
+        spec = synth.grad_spec(seed=3, psi=5000, **kw)
+        a = synth.grad_f32(6000, 17, spec, 2, 5)
+        b = np.empty(6000, np.float32)
+        L.zs_host_fill_grad_stream(b.ctypes.data, 6000, 17, C.byref(spec), 2, 5)
+        assert np.array_equal(a, b)
