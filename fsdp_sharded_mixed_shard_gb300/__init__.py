@@ -18,7 +18,7 @@ __all__ = [
     "zero_plan_create", "zero_plan_destroy", "zero_plan_get_info", "zero_plan_tensor_offsets",
     "zero_plan_segments", "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
     "zero_reduce_scatter", "zero_grad_norm", "zero_step", "zero_step_update", "zero_step_finish",
-    "zero_cast_params", "zero_strerror",
+    "zero_cast_params", "zero_grad_norm_noalloc", "zero_strerror",
     "zero_version", "lib",
 ]
 
@@ -101,6 +101,8 @@ def lib():
         L.zero_step_finish.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), C.c_int32, _P(_VP),
                                        C.c_int64, _VP, _P(ZeroHParams), _VP, _VP]
         L.zero_cast_params.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _VP, C.c_int64, _VP]
+        L.zero_grad_norm_noalloc.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP),
+                                             _P(ZeroHParams), _VP, _VP]
         L.zero_strerror.argtypes = [C.c_int]
         L.zero_strerror.restype = C.c_char_p
         L.zero_version.argtypes = []
@@ -217,6 +219,13 @@ def zero_step_finish(plan, rank_lo, rank_hi, master, n_sets, grad_shards, window
 def zero_cast_params(plan, rank_lo, rank_hi, master, flat_params, window_base, stream=0):
     _check("zero_cast_params", lib().zero_cast_params(
         plan, rank_lo, rank_hi, _ptrs(master), _vp(flat_params), window_base, _vp(stream)))
+
+
+def zero_grad_norm_noalloc(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, stream=0):
+    """zero_grad_norm without a workspace: for callers that cannot allocate
+    device memory (see include/zero.h)."""
+    _check("zero_grad_norm_noalloc", lib().zero_grad_norm_noalloc(
+        plan, rank_lo, rank_hi, _ptrs(grad_shards), C.byref(hp), _vp(d_scaler), _vp(stream)))
 
 
 def zero_strerror(status):

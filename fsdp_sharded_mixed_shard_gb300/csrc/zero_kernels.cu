@@ -43,6 +43,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "zero_internal.h"
@@ -902,3 +903,97 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ no-allocation norm entry --
+//
+// zero_grad_norm_noalloc: the same norm and clip coefficient as
+// zero_grad_norm, for callers that cannot hand the library a device
+// workspace. Its tile partials live in a fixed device array in this file.
+
+namespace zk {
+
+constexpr int64_t kNoallocTiles = ZERO_NOALLOC_MAX_TILES;
+
+// One fp64 partial per norm tile, 4 MiB. Every GPU that loads this library
+// holds this array until the process exits. All calls share it, and each call
+// overwrites the partials of exactly the tiles it later sums, so nothing has
+// to be cleared between calls. Calls that overlap on the GPU (different
+// streams, or different host threads without ordering) race on it.
+static __device__ __align__(256) double g_noalloc_partials[kNoallocTiles];
+
+// Device address of g_noalloc_partials per device ordinal, resolved once per
+// device with that device current. In host code the array's name only stands
+// for the symbol; it is never a device address.
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+double* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+int noalloc_scratch(double** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return ZERO_ERANGE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return ZERO_ECUDA;
+    g_noalloc_ptr[dev] = static_cast<double*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return ZERO_OK;
+}
+
+}  // namespace zk
+
+extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t rank_lo,
+                                               int32_t rank_hi, const float* const* grad_shards,
+                                               const zero_hparams* hp, zero_scaler* d_scaler,
+                                               void* stream) {
+  if (!ranks_ok(plan, rank_lo, rank_hi) || !hp || !d_scaler || !grad_shards) return ZERO_EINVAL;
+  if (!(hp->max_grad_norm > 0.0)) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler)) return ZERO_EALIGN;
+  int rc = check_ptr_array(reinterpret_cast<const void* const*>(grad_shards), rank_lo, rank_hi,
+                           0, 1);
+  if (rc) return rc;
+  const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+  const int64_t t0 = s0 < s1 ? plan->seg_tile0[s0] : 0;
+  const int64_t t1 = s0 < s1 ? plan->seg_tile0[s1 - 1] + plan->seg_tiles[s1 - 1] : 0;
+  if (t1 - t0 > kNoallocTiles) return ZERO_ERANGE;
+  double* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+
+  Args* a = new_args(plan);
+  if (!a) return ZERO_ENOMEM;
+  for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = const_cast<float*>(grad_shards[i]);
+  a->scaler = d_scaler;
+  a->partials = scratch;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int grid_cap = grid_size<kNorm, true>();
+  if (grid_cap <= 0) rc = ZERO_ECUDA;
+  // tiles are numbered from t0 so that the partials start at the array's base
+  for (int32_t b0 = s0; !rc && b0 < s1; b0 += kMaxSegs) {
+    const int32_t b1 = std::min(s1, b0 + kMaxSegs);
+    int64_t tiles = 0;
+    for (int32_t s = b0; s < b1; ++s) {
+      Seg& d = a->segs[s - b0];
+      d.lo = plan->segs[s].lo;
+      d.hi = plan->segs[s].hi;
+      d.rank = plan->segs[s].rank;
+      d.bucket = plan->segs[s].bucket;
+      d.tile_local0 = tiles;
+      d.tile_global0 = plan->seg_tile0[s] - t0;
+      tiles += plan->seg_tiles[s];
+    }
+    a->n_segs = b1 - b0;
+    a->n_tiles = tiles;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
+    // the kNorm body only reads fp32 gradients, so one instantiation serves
+    // both 16-bit formats
+    step_kernel<kNorm, true><<<grid, kThreads, 0, st>>>(*a);
+    if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
+  }
+  delete a;
+  if (rc) return rc;
+  norm_finish_kernel<<<1, kNormThreads, 0, st>>>(scratch, 0, t1 - t0, hp->max_grad_norm,
+                                                 d_scaler);
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}

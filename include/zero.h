@@ -51,9 +51,11 @@
  *     Decisions (skip, clip coefficient, loss scale) stay on the device in
  *     zero_scaler.
  *   - Every device pointer must be 16-byte aligned (ZERO_EALIGN otherwise).
- *   - Plans are immutable after creation; the library has no global state,
- *     so concurrent calls on different streams and buffers are safe. Calls
- *     that share a scaler or buffers must be ordered by the caller.
+ *   - Plans are immutable after creation and the library keeps no global
+ *     state (the one exception is the fixed device array behind
+ *     zero_grad_norm_noalloc), so concurrent calls on different streams and
+ *     buffers are safe. Calls that share a scaler or buffers must be ordered
+ *     by the caller.
  *   - Element indices are int64 (N * psi may exceed 2^31).
  */
 #ifndef ZERO_H
@@ -309,6 +311,36 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
  * 128), empty launches skipped): fused zero_step 2L + 1 (update, overflow
  * re-cast check, bookkeeping), two-pass zero_step L + 1, zero_reduce_scatter
  * L, zero_grad_norm 1 (+ L when it recomputes the partials), zero_cast_params L. */
+
+/* Maximum number of norm tiles (ZERO_TILE_ELEMS elements each, counted per
+ * segment) that one zero_grad_norm_noalloc call may cover: 2^19 tiles, about
+ * 2.1e9 elements, 4 MiB of device memory. */
+#define ZERO_NOALLOC_MAX_TILES (1 << 19)
+
+/* zero_grad_norm_noalloc -- the global norm and clip coefficient of
+ * zero_grad_norm (grad_shards form), without a caller-provided workspace.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: code running inside a host framework whose
+ * allocator owns all of the GPU's memory, plugins and embedded runtimes that
+ * are not allowed to call cudaMalloc themselves, and callers with a fixed
+ * memory budget that cannot grow by a workspace sized from the model.
+ * It allocates nothing: the per-tile partials live in one fixed device
+ * array of ZERO_NOALLOC_MAX_TILES doubles inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *   grad_shards: as for zero_grad_norm, required (not NULL).
+ *   Result: norm_sq, norm, clip_coef, clip_apply and norm_step in d_scaler,
+ *   equal to what zero_grad_norm computes from the same gradients.
+ * The first call on each device resolves the array's device address with
+ * that device current; make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents (each call
+ * rewrites every partial it reads). Calls that overlap on the GPU race on
+ * it: order them on one stream.
+ * Errors: ZERO_EINVAL (NULL arguments, bad ranks, max_grad_norm <= 0),
+ * ZERO_EALIGN, ZERO_ERANGE (the owners' slices need more than
+ * ZERO_NOALLOC_MAX_TILES tiles), ZERO_ECUDA. */
+ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                                    const float* const* grad_shards, const zero_hparams* hp,
+                                    zero_scaler* d_scaler, void* stream);
 
 ZERO_API const char* zero_strerror(int status);
 /* Library version: major * 10000 + minor * 100 + patch. */
