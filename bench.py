@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--numel-cap", type=int, default=0,
+                    help="run the workload's first N flat parameters only (small profiling case)")
     return ap.parse_args()
 
 
@@ -187,6 +189,8 @@ def run_libzero(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = workload(args.workload)
+    if args.numel_cap:
+        wl = truncated(wl, args.numel_cap)
     g = harness.Group(wl, device=dev)
     path = "two_pass" if g.two_pass else "fused"
     g.init_state()
@@ -349,7 +353,7 @@ def run_libzero(args, rank, world, dist):
 
 # ---------------------------------------------------------- CPU checker ----
 
-def oracle_sample(wl, n_elems):
+def truncated(wl, n_elems):
     """The workload's first n_elems flat elements (tensor list cut there),
     same N, buckets, gradient format and hyperparameters."""
     numels, left = [], n_elems
@@ -358,7 +362,11 @@ def oracle_sample(wl, n_elems):
             break
         numels.append(min(x, left))
         left -= numels[-1]
-    return wl.scaled(numels=numels, rank_lo=0, rank_hi=None, inject=None)
+    return wl.scaled(name="%s_first%d" % (wl.name, sum(numels)), numels=numels, rank_lo=0,
+                     rank_hi=None, inject=None)
+
+
+oracle_sample = truncated
 
 
 def time_oracle_steps(wl_s, steps):
