@@ -514,6 +514,432 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
   }
 }
 
+// -------------------------------------------------- bulk-copy pipeline --
+//
+// kFused, kReduce and kUpdate stream their inputs through shared memory.
+// One producer warp (its lane 0) walks the CTA's tiles and, per stage of
+// E = 256 * V elements, posts the byte count on the slot's "full" mbarrier
+// and issues one cp.async.bulk per input chunk (the N replica chunks in ring
+// order, then g and/or master, m, v). Eight consumer warps wait on "full",
+// compute from shared memory (thread t owns elements [t*V, t*V+V) of the
+// stage), write their results to global memory with streaming stores and
+// release the slot on its "empty" mbarrier. The number of slots S is chosen
+// so S stages fit in shared memory; S - 1 stages (~100+ KB per SM) are in
+// flight while one is computed, independent of the register budget.
+// Tile heads/tails that are not 16-byte aligned are done by the consumers
+// with plain loads (do_scalar).
+// Every mbarrier wait is bounded by kWaitLimitNs of %globaltimer; on expiry
+// the thread records ZERO_DEVERR_TIMEOUT, the CTA stops issuing, the
+// producer waits (again bounded) for the copies it issued, and all return.
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kBulkThreads = kConsumers + 32;
+constexpr int kMaxStages = 6;
+constexpr int kStageBudget = 72 * 1024;        // bytes per stage, upper bound
+constexpr int kSmemCap = 216 * 1024;            // dynamic shared memory per CTA
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+static_assert(kTile % (kConsumers * 8) == 0, "tile must hold whole stages");
+
+__host__ __device__ constexpr int bulk_bytes_per_elem(int mode, int n_ranks) {
+  return mode == kFused ? 2 * n_ranks + 12 : (mode == kReduce ? 2 * n_ranks : 16);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// true when the phase of the given parity has completed; false after the limit
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// global -> shared bulk copy completing on `bar`; addresses 16-byte aligned,
+// bytes a multiple of 16
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+struct TileGeom {
+  int64_t lo, hi, va, vb, partial;
+  int32_t rank, bucket, first_rep;
+};
+
+// Tile g of this launch: element range, owner, and the 16-byte aligned body
+// [va, vb) (empty when the owner's shard and the windows are misaligned).
+__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
+  const Seg& sg = a.segs[find_seg(a, g)];
+  TileGeom t;
+  t.lo = sg.lo + (g - sg.tile_local0) * kTile;
+  t.hi = min(t.lo + kTile, sg.hi);
+  t.rank = sg.rank;
+  t.bucket = sg.bucket;
+  t.partial = sg.tile_global0 + (g - sg.tile_local0);
+  t.first_rep = sg.rank + 1 == a.n_ranks ? 0 : sg.rank + 1;
+  const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
+  t.va = t.hi;
+  t.vb = t.hi;
+  if (((rank0 - a.wbase) & 3) == 0) {
+    t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
+    t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
+  }
+  return t;
+}
+
+// V consecutive 16-bit values from shared memory, widened
+template <bool kBf16, int V>
+__device__ __forceinline__ void lds_h(const unsigned char* p, float (&x)[V]) {
+  if constexpr (V == 8) {
+    uint4 w = *reinterpret_cast<const uint4*>(p);
+    widen8<kBf16>(w, x);
+  } else if constexpr (V == 4) {
+    uint2 w = *reinterpret_cast<const uint2*>(p);
+    x[0] = widen<kBf16>(w.x & 0xFFFFu);
+    x[1] = widen<kBf16>(w.x >> 16);
+    x[2] = widen<kBf16>(w.y & 0xFFFFu);
+    x[3] = widen<kBf16>(w.y >> 16);
+  } else {
+    uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    x[0] = widen<kBf16>(w & 0xFFFFu);
+    x[1] = widen<kBf16>(w >> 16);
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void lds_f(const unsigned char* p, float (&x)[V]) {
+  if constexpr (V == 8) {
+    float4 a = reinterpret_cast<const float4*>(p)[0];
+    float4 b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else if constexpr (V == 4) {
+    float4 a = *reinterpret_cast<const float4*>(p);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  } else {
+    float2 a = *reinterpret_cast<const float2*>(p);
+    x[0] = a.x; x[1] = a.y;
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void stg_f(float* p, const float (&x)[V]) {
+  if constexpr (V == 8) {
+    store8f(p, x);
+  } else if constexpr (V == 4) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+  } else {
+    __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
+  }
+}
+
+template <bool kBf16, int V>
+__device__ __forceinline__ void stg_h(uint16_t* p, const float (&x)[V]) {
+  uint32_t u[V / 2];
+#pragma unroll
+  for (int k = 0; k < V / 2; ++k)
+    u[k] = static_cast<uint32_t>(narrow<kBf16>(x[2 * k])) |
+           (static_cast<uint32_t>(narrow<kBf16>(x[2 * k + 1])) << 16);
+  if constexpr (V == 8) {
+    __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
+  } else if constexpr (V == 4) {
+    __stcs(reinterpret_cast<uint2*>(p), make_uint2(u[0], u[1]));
+  } else {
+    __stcs(reinterpret_cast<unsigned int*>(p), u[0]);
+  }
+}
+
+// One consumer thread's V elements of a stage held in shared memory.
+// Stage layout: kFused  [N replica chunks, 2E bytes each, ring order]
+//                       [master 4E][m 4E][v 4E]
+//               kReduce [N replica chunks]
+//               kUpdate [g 4E][master 4E][m 4E][v 4E]
+template <int MODE, bool kBf16, int V>
+__device__ __forceinline__ void do_stage(const Args& a, const StepScalars& s,
+                                         const unsigned char* buf, int64_t j, int32_t rank,
+                                         int t_off, NormAcc& nacc, bool& bad) {
+  constexpr int E = kConsumers * V;
+  const int64_t w = j - a.wbase;
+  const int64_t k = j - static_cast<int64_t>(rank) * a.shard;
+  float g[V], th[V], m[V], v[V];
+  const unsigned char* st = buf;
+  if constexpr (MODE == kFused || MODE == kReduce) {
+    const int N = a.n_ranks;
+    float acc[V];
+    lds_h<kBf16, V>(buf + t_off * 2, acc);
+#pragma unroll 4
+    for (int p = 1; p < N; ++p) {
+      float x[V];
+      lds_h<kBf16, V>(buf + static_cast<size_t>(p) * (2 * E) + t_off * 2, x);
+#pragma unroll
+      for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      g[e] = __fmul_rn(acc[e], s.inv);
+      bad |= nonfinite(g[e]);
+    }
+    st = buf + static_cast<size_t>(N) * (2 * E);
+  }
+  if constexpr (MODE == kReduce) {
+    stg_f<V>(a.ghat[rank] + k, g);
+    if (a.mode_flags & kFlagPartials) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) nacc.add(g[e]);
+    }
+  }
+  if constexpr (MODE == kUpdate) {
+    lds_f<V>(buf + t_off * 4, g);
+    st = buf + 4 * E;
+    if (s.clip != 1.0f) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) g[e] = __fmul_rn(g[e], s.clip);
+    }
+  }
+  if constexpr (MODE == kFused || MODE == kUpdate) {
+    lds_f<V>(st + t_off * 4, th);
+    lds_f<V>(st + 4 * E + t_off * 4, m);
+    lds_f<V>(st + 8 * E + t_off * 4, v);
+#pragma unroll
+    for (int e = 0; e < V; ++e) adamw(th[e], m[e], v[e], g[e], a, s);
+    stg_f<V>(a.master[s.dst][rank] + k, th);
+    stg_f<V>(a.mom[s.dst][rank] + k, m);
+    stg_f<V>(a.var[s.dst][rank] + k, v);
+    stg_h<kBf16, V>(a.flat + w, th);
+  }
+}
+
+template <int MODE, bool kBf16, int V>
+__global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
+                                                               int n_slots,
+                                                               uint32_t slot_bytes) {
+  constexpr int E = kConsumers * V;
+  __shared__ StepScalars sh_s;
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ float sh_hi[kConsumerWarps], sh_lo[kConsumerWarps];
+  __shared__ double sh_big[kConsumerWarps];
+  __shared__ int sh_abort;
+  extern __shared__ __align__(128) unsigned char stage_mem[];
+
+  if (threadIdx.x == 0) {
+    compute_step_scalars<MODE>(a, &sh_s);
+    for (int i = 0; i < n_slots; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumerWarps);
+    }
+    sh_abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const StepScalars s = sh_s;
+  if (s.skip) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.n_ranks;
+  volatile int* abort_flag = &sh_abort;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    const uint64_t pol = evict_first_policy();
+    const uint32_t bpe = bulk_bytes_per_elem(MODE, N);
+    uint32_t it = 0;
+    bool stop = false;
+    for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
+      const TileGeom t = tile_geom(a, g);
+      const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
+      for (int64_t j0 = t.va; j0 < t.vb; j0 += E, ++it) {
+        if (*abort_flag) {
+          stop = true;
+          break;
+        }
+        const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
+        const int slot = static_cast<int>(it % n_slots);
+        const uint32_t k = it / n_slots;
+        if (!mbar_wait(&empty_bar[slot], (k & 1u) ^ 1u)) {
+          set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          stop = true;
+          break;
+        }
+        unsigned char* buf = stage_mem + static_cast<size_t>(slot) * slot_bytes;
+        mbar_expect_tx(&full_bar[slot], len * bpe);
+        const int64_t w = j0 - a.wbase;
+        const int64_t kk = j0 - rank0;
+        unsigned char* dst = buf;
+        if constexpr (MODE == kFused || MODE == kReduce) {
+          int rr = t.first_rep;
+          for (int p = 0; p < N; ++p) {
+            bulk_g2s(buf + static_cast<size_t>(p) * (2 * E), a.rep[rr] + w, len * 2,
+                     &full_bar[slot], pol);
+            rr = rr + 1 == N ? 0 : rr + 1;
+          }
+          dst = buf + static_cast<size_t>(N) * (2 * E);
+        }
+        if constexpr (MODE == kUpdate) {
+          bulk_g2s(buf, a.ghat[t.rank] + kk, len * 4, &full_bar[slot], pol);
+          dst = buf + 4 * E;
+        }
+        if constexpr (MODE == kFused || MODE == kUpdate) {
+          bulk_g2s(dst, a.master[s.src][t.rank] + kk, len * 4, &full_bar[slot], pol);
+          bulk_g2s(dst + 4 * E, a.mom[s.src][t.rank] + kk, len * 4, &full_bar[slot], pol);
+          bulk_g2s(dst + 8 * E, a.var[s.src][t.rank] + kk, len * 4, &full_bar[slot], pol);
+        }
+      }
+    }
+    // make sure no copy is still landing when the CTA exits (bounded)
+    const uint32_t issued = it;
+    for (uint32_t back = 0; back < static_cast<uint32_t>(n_slots) && back < issued; ++back) {
+      const uint32_t i = issued - 1 - back;
+      if (!mbar_wait(&full_bar[i % n_slots], (i / n_slots) & 1u))
+        set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int tid = threadIdx.x;
+  uint32_t it = 0;
+  bool dead = false;
+  for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x) {
+    const TileGeom t = tile_geom(a, g);
+    NormAcc nacc;
+    bool bad = false;
+    // unaligned head [lo, va) and tail [vb, hi) with plain loads
+    const int nhead = static_cast<int>(t.va - t.lo);
+    const int ntail = static_cast<int>(t.hi - t.vb);
+    for (int q = tid; q < nhead + ntail; q += kConsumers) {
+      const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
+      do_scalar<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad);
+    }
+    for (int64_t j0 = t.va; j0 < t.vb; j0 += E, ++it) {
+      const int len = static_cast<int>(min(static_cast<int64_t>(E), t.vb - j0));
+      const int slot = static_cast<int>(it % n_slots);
+      const uint32_t k = it / n_slots;
+      // keep `dead` uniform across the warp so the warp-level syncs below
+      // always see all 32 lanes
+      if (!dead) dead = __any_sync(0xFFFFFFFFu, *abort_flag != 0);
+      if (!dead) {
+        const bool landed = mbar_wait(&full_bar[slot], k & 1u);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+          if (lane == 0) {
+            set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          dead = true;
+        }
+      }
+      if (!dead) {
+        const int t_off = tid * V;
+        if (t_off < len)
+          do_stage<MODE, kBf16, V>(a, s, stage_mem + static_cast<size_t>(slot) * slot_bytes,
+                                   j0 + t_off, t.rank, t_off, nacc, bad);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      }
+    }
+    if constexpr (MODE == kFused || MODE == kReduce) {
+      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a, t.bucket);
+    }
+    if constexpr (MODE == kReduce) {
+      if (a.mode_flags & kFlagPartials) {
+        // consumer-only version of cta_norm_total (named barrier 1)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          float h2 = __shfl_down_sync(0xFFFFFFFFu, nacc.hi, off);
+          float l2 = __shfl_down_sync(0xFFFFFFFFu, nacc.lo, off);
+          if (lane < off) nacc.merge(h2, l2);
+        }
+        const bool big_here = __any_sync(0xFFFFFFFFu, nacc.big != 0.0);
+        double b = nacc.big;
+        if (big_here) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            double b2 = __shfl_down_sync(0xFFFFFFFFu, b, off);
+            if (lane < off) b = __dadd_rn(b, b2);
+          }
+        }
+        if (lane == 0) {
+          sh_hi[warp] = nacc.hi;
+          sh_lo[warp] = nacc.lo;
+          sh_big[warp] = big_here ? b : 0.0;
+        }
+        consumer_sync();
+        if (tid == 0) {
+          double total = 0.0;
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            total = __dadd_rn(total, __dadd_rn(static_cast<double>(sh_hi[w]),
+                                               static_cast<double>(sh_lo[w])));
+            if (sh_big[w] != 0.0) total = __dadd_rn(total, sh_big[w]);
+          }
+          a.partials[t.partial] = total;
+        }
+        consumer_sync();
+      }
+    }
+  }
+}
+
 // Fixed-order fp64 sum of tile partials [t0, t1), then norm and clip
 // coefficient. One CTA of kNormThreads threads: thread k sums partials
 // t0+k, t0+k+kNormThreads, ... in order; then a fixed shared-memory tree.
@@ -583,10 +1009,64 @@ int grid_size() {
   return sms * std::max(per_sm, 1);
 }
 
+// Bulk-pipeline launch parameters for MODE at N ranks: elements per
+// consumer thread V (largest of 8, 4, 2 whose stage fits kStageBudget),
+// slot bytes and number of slots.
+struct BulkShape {
+  int V, slots;
+  uint32_t slot_bytes;
+  size_t smem;
+};
+
+inline BulkShape bulk_shape(int mode, int n_ranks) {
+  BulkShape b{0, 0, 0, 0};
+  const int bpe = bulk_bytes_per_elem(mode, n_ranks);
+  for (int V = 8; V >= 2; V /= 2) {
+    const int stage = kConsumers * V * bpe;
+    if (stage <= kStageBudget) {
+      b.V = V;
+      b.slot_bytes = static_cast<uint32_t>((stage + 127) & ~127);
+      b.slots = std::min(kMaxStages, kSmemCap / static_cast<int>(b.slot_bytes));
+      b.smem = static_cast<size_t>(b.slots) * b.slot_bytes;
+      return b;
+    }
+  }
+  return b;
+}
+
+template <int MODE, bool kBf16, int V>
+int launch_bulk_v(Args& a, const BulkShape& b, int64_t tiles, cudaStream_t stream) {
+  auto kern = bulk_kernel<MODE, kBf16, V>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(b.smem)) != cudaSuccess)
+    return ZERO_ECUDA;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ZERO_ECUDA;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBulkThreads, b.smem) !=
+      cudaSuccess)
+    return ZERO_ECUDA;
+  const int64_t cap = static_cast<int64_t>(sms) * std::max(per_sm, 1);
+  const int grid = static_cast<int>(std::min<int64_t>(tiles, cap));
+  kern<<<grid, kBulkThreads, b.smem, stream>>>(a, b.slots, b.slot_bytes);
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+template <int MODE, bool kBf16>
+int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+  const BulkShape b = bulk_shape(MODE, a.n_ranks);
+  if (b.V == 8) return launch_bulk_v<MODE, kBf16, 8>(a, b, tiles, stream);
+  if (b.V == 4) return launch_bulk_v<MODE, kBf16, 4>(a, b, tiles, stream);
+  if (b.V == 2) return launch_bulk_v<MODE, kBf16, 2>(a, b, tiles, stream);
+  return ZERO_ERANGE;
+}
+
 template <int MODE, bool kBf16>
 int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
                 cudaStream_t stream) {
-  int grid_cap = grid_size<MODE, kBf16>();
+  constexpr bool kBulk = MODE == kFused || MODE == kReduce || MODE == kUpdate;
+  int grid_cap = kBulk ? 1 : grid_size<MODE, kBf16>();
   if (grid_cap <= 0) return ZERO_ECUDA;
   for (int32_t s0 = seg_begin; s0 < seg_end; s0 += kMaxSegs) {
     const int32_t s1 = std::min(seg_end, s0 + kMaxSegs);
@@ -604,9 +1084,14 @@ int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
     a.n_segs = s1 - s0;
     a.n_tiles = tiles;
     if (tiles == 0) continue;
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
-    step_kernel<MODE, kBf16><<<grid, kThreads, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return ZERO_ECUDA;
+    if constexpr (kBulk) {
+      const int rc = launch_bulk<MODE, kBf16>(a, tiles, stream);
+      if (rc) return rc;
+    } else {
+      const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
+      step_kernel<MODE, kBf16><<<grid, kThreads, 0, stream>>>(a);
+      if (cudaGetLastError() != cudaSuccess) return ZERO_ECUDA;
+    }
   }
   return ZERO_OK;
 }

@@ -198,6 +198,7 @@ typedef struct zero_scaler {
 /* device error codes written to zero_scaler.error (first error wins) */
 #define ZERO_DEVERR_STATE_INDEX 1   /* state_index outside the given sets */
 #define ZERO_DEVERR_NO_NORM 2       /* clip requested but zero_grad_norm not run */
+#define ZERO_DEVERR_TIMEOUT 3       /* a pipeline wait expired (2 s); results invalid */
 
 /* Fill *out (host memory) with the initial scaler: scale = init_scale,
  * t = 0, beta powers 1, state set 0, all flags clear. */
