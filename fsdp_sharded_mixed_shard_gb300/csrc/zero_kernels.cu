@@ -800,59 +800,77 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // lane 0 owns the barriers; the 32 lanes issue the stage's copies in
+    // parallel (chunk c by lane c mod 32), so N + 3 copies per stage do not
+    // serialise on one thread
     const uint64_t pol = evict_first_policy();
     const uint32_t bpe = bulk_bytes_per_elem(MODE, N);
+    constexpr int kStateChunks = MODE == kFused ? 3 : (MODE == kUpdate ? 4 : 0);
+    const int n_chunks = (MODE == kUpdate ? 0 : N) + kStateChunks;
     uint32_t it = 0;
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
       const TileGeom t = tile_geom(a, g);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
       for (int64_t j0 = t.va; j0 < t.vb; j0 += E, ++it) {
-        if (*abort_flag) {
-          stop = true;
-          break;
-        }
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
         const int slot = static_cast<int>(it % n_slots);
         const uint32_t k = it / n_slots;
-        if (!mbar_wait(&empty_bar[slot], (k & 1u) ^ 1u)) {
-          set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
-          *abort_flag = 1;
+        int go = 1;
+        if (lane == 0) {
+          if (*abort_flag) {
+            go = 0;
+          } else if (!mbar_wait(&empty_bar[slot], (k & 1u) ^ 1u)) {
+            set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            go = 0;
+          } else {
+            mbar_expect_tx(&full_bar[slot], len * bpe);
+          }
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
           stop = true;
           break;
         }
         unsigned char* buf = stage_mem + static_cast<size_t>(slot) * slot_bytes;
-        mbar_expect_tx(&full_bar[slot], len * bpe);
         const int64_t w = j0 - a.wbase;
         const int64_t kk = j0 - rank0;
-        unsigned char* dst = buf;
-        if constexpr (MODE == kFused || MODE == kReduce) {
-          int rr = t.first_rep;
-          for (int p = 0; p < N; ++p) {
-            bulk_g2s(buf + static_cast<size_t>(p) * (2 * E), a.rep[rr] + w, len * 2,
+        for (int c = lane; c < n_chunks; c += 32) {
+          if (MODE != kUpdate && c < N) {
+            int rr = t.first_rep + c;
+            if (rr >= N) rr -= N;
+            bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
                      &full_bar[slot], pol);
-            rr = rr + 1 == N ? 0 : rr + 1;
+          } else {
+            // state chunks: kFused master, m, v after the replicas;
+            // kUpdate g, master, m, v
+            const int q = MODE == kUpdate ? c : c - N;
+            unsigned char* base =
+                MODE == kUpdate ? buf : buf + static_cast<size_t>(N) * (2 * E);
+            const float* src;
+            if (MODE == kUpdate) {
+              src = q == 0 ? a.ghat[t.rank]
+                           : (q == 1 ? a.master[s.src][t.rank]
+                                     : (q == 2 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]));
+            } else {
+              src = q == 0 ? a.master[s.src][t.rank]
+                           : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
+            }
+            bulk_g2s(base + static_cast<size_t>(q) * (4 * E), src + kk, len * 4,
+                     &full_bar[slot], pol);
           }
-          dst = buf + static_cast<size_t>(N) * (2 * E);
         }
-        if constexpr (MODE == kUpdate) {
-          bulk_g2s(buf, a.ghat[t.rank] + kk, len * 4, &full_bar[slot], pol);
-          dst = buf + 4 * E;
-        }
-        if constexpr (MODE == kFused || MODE == kUpdate) {
-          bulk_g2s(dst, a.master[s.src][t.rank] + kk, len * 4, &full_bar[slot], pol);
-          bulk_g2s(dst + 4 * E, a.mom[s.src][t.rank] + kk, len * 4, &full_bar[slot], pol);
-          bulk_g2s(dst + 8 * E, a.var[s.src][t.rank] + kk, len * 4, &full_bar[slot], pol);
-        }
+        __syncwarp();
       }
     }
     // make sure no copy is still landing when the CTA exits (bounded)
-    const uint32_t issued = it;
-    for (uint32_t back = 0; back < static_cast<uint32_t>(n_slots) && back < issued; ++back) {
-      const uint32_t i = issued - 1 - back;
-      if (!mbar_wait(&full_bar[i % n_slots], (i / n_slots) & 1u))
-        set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+    if (lane == 0) {
+      const uint32_t issued = it;
+      for (uint32_t back = 0; back < static_cast<uint32_t>(n_slots) && back < issued; ++back) {
+        const uint32_t i = issued - 1 - back;
+        if (!mbar_wait(&full_bar[i % n_slots], (i / n_slots) & 1u))
+          set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+      }
     }
     return;
   }
