@@ -54,7 +54,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTile = ZERO_TILE_ELEMS;
 constexpr int kVec = 8;                       // 16-bit elements per 16-byte vector
-constexpr int kVecPerTile = kTile / kVec;     // 512
 constexpr int kMaxSegs = 128;                 // segments per launch (kernel parameter space)
 constexpr int kChunk = 8;                     // replicas loaded together
 constexpr int kNormThreads = 1024;
@@ -76,6 +75,18 @@ struct Seg {
   int32_t rank, bucket;
 };
 
+// Bulk pipeline stage plan for one element range of kStageElems elements:
+// stage i carries the replica chunks of ring positions [r_lo[i], r_hi[i])
+// and, when states[i] is set, the state block (kFused: master, m, v;
+// kUpdate: g, master, m, v) after them.
+constexpr int kMaxStagePlan = 8;
+struct StagePlan {
+  int32_t n;
+  int16_t r_lo[kMaxStagePlan], r_hi[kMaxStagePlan];
+  int32_t states[kMaxStagePlan];
+  int32_t bytes_per_elem[kMaxStagePlan];
+};
+
 struct Args {
   const uint16_t* rep[ZERO_MAX_RANKS];      // replica windows
   float* master[2][ZERO_MAX_RANKS];
@@ -92,6 +103,7 @@ struct Args {
   float b1, omb1, b2, omb2, lr, decay, eps;
   int32_t pad0;
   double beta1, beta2;
+  StagePlan plan;  // bulk pipeline: stages of one element range
   Seg segs[kMaxSegs];
 };
 
@@ -185,13 +197,15 @@ __device__ __forceinline__ void adamw(float& th, float& m, float& v, float g, co
 
 // Squared-gradient accumulation with a float-float (hi, lo) pair: the square
 // is split exactly into p + e (e = fma(g, g, -p)), p is added with an exact
-// two-sum and all error terms collect in lo. Relative accuracy ~2^-44, far
-// inside the fp64 rounding of the tile and global sums, and it needs no
-// per-element fp64 work. Magnitudes whose square is not exact in fp32 go to
-// an fp64 side sum.
+// two-sum and all error terms collect in lo (relative accuracy ~2^-44 over a
+// tile). No per-element fp64 work: GB300's fp64 path is far too slow for
+// that. Magnitudes whose square would leave fp32's exact range
+// (|g| >= 2^60, or 0 < |g| <= 2^-60) go to an fp64 side sum, flagged so that
+// the common case never touches fp64.
 struct NormAcc {
   float hi = 0.f, lo = 0.f;
   double big = 0.0;
+  bool has_big = false;
   __device__ __forceinline__ void add(float g) {
     float ag = fabsf(g);
     if (ag < 0x1p60f && (ag > 0x1p-60f || ag == 0.f)) {
@@ -205,6 +219,7 @@ struct NormAcc {
     } else {
       double d = static_cast<double>(g);
       big = __dadd_rn(big, __dmul_rn(d, d));
+      has_big = true;
     }
   }
   // (hi, lo) += (h2, l2), two-sum on the high parts
@@ -217,40 +232,53 @@ struct NormAcc {
   }
 };
 
-// Deterministic CTA reduction of the per-thread accumulators to one fp64
-// value (fixed shuffle tree, then warps in order). Result valid in thread 0.
-__device__ double cta_norm_total(NormAcc acc, float* sh_hi, float* sh_lo, double* sh_big) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Per-warp tile sums published to shared memory, double-buffered by tile
+// parity so that one barrier per tile suffices.
+constexpr int kMaxWarps = 8;
+struct NormSlots {
+  float hi[2][kMaxWarps];
+  float lo[2][kMaxWarps];
+  double big[2][kMaxWarps];
+  int has_big[2][kMaxWarps];
+};
+
+// Fixed shuffle tree inside the warp, then lane 0 publishes the warp's sum.
+__device__ __forceinline__ void tile_norm_publish(NormAcc acc, NormSlots& sl, int par, int warp,
+                                                  int lane) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     float h2 = __shfl_down_sync(0xFFFFFFFFu, acc.hi, off);
     float l2 = __shfl_down_sync(0xFFFFFFFFu, acc.lo, off);
     if (lane < off) acc.merge(h2, l2);
   }
-  const bool any_big = __syncthreads_or(acc.big != 0.0);
-  if (lane == 0) {
-    sh_hi[warp] = acc.hi;
-    sh_lo[warp] = acc.lo;
-  }
-  if (any_big) {
-    double b = acc.big;
+  const bool any_big = __any_sync(0xFFFFFFFFu, acc.has_big);
+  double b = acc.big;
+  if (any_big) {  // rare: fp64 only when a lane saw an out-of-range magnitude
+    if (!acc.has_big) b = 0.0;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       double b2 = __shfl_down_sync(0xFFFFFFFFu, b, off);
       if (lane < off) b = __dadd_rn(b, b2);
     }
-    if (lane == 0) sh_big[warp] = b;
   }
-  __syncthreads();
-  double total = 0.0;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < kWarps; ++w) {
-      total = __dadd_rn(total, __dadd_rn(static_cast<double>(sh_hi[w]),
-                                         static_cast<double>(sh_lo[w])));
-      if (any_big) total = __dadd_rn(total, sh_big[w]);
-    }
+  if (lane == 0) {
+    sl.hi[par][warp] = acc.hi;
+    sl.lo[par][warp] = acc.lo;
+    sl.big[par][warp] = b;
+    sl.has_big[par][warp] = any_big ? 1 : 0;
   }
-  __syncthreads();
+}
+
+// After the barrier: warps' sums merged in warp order in float-float, then
+// one conversion to fp64 (plus the rare fp64 side sums, in warp order).
+__device__ __forceinline__ double tile_norm_total(const NormSlots& sl, int par, int n_warps) {
+  NormAcc t;
+  t.hi = sl.hi[par][0];
+  t.lo = sl.lo[par][0];
+  for (int w = 1; w < n_warps; ++w) t.merge(sl.hi[par][w], sl.lo[par][w]);
+  double total = __dadd_rn(static_cast<double>(t.hi), static_cast<double>(t.lo));
+  for (int w = 0; w < n_warps; ++w)
+    if (sl.has_big[par][w]) total = __dadd_rn(total, sl.big[par][w]);
   return total;
 }
 
@@ -461,15 +489,16 @@ __device__ __forceinline__ void do_scalar(const Args& a, const StepScalars& s, i
 template <int MODE, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ Args a) {
   __shared__ StepScalars sh_s;
-  __shared__ float sh_hi[kWarps], sh_lo[kWarps];
-  __shared__ double sh_big[kWarps];
+  __shared__ NormSlots sh_norm;
   if (threadIdx.x == 0) compute_step_scalars<MODE>(a, &sh_s);
   __syncthreads();
   const StepScalars s = sh_s;
   if (s.skip) return;
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  uint32_t tile_no = 0;  // tiles done by this CTA
 
-  for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x) {
+  for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
     const Seg& sg = a.segs[find_seg(a, g)];
     const int64_t lo = sg.lo + (g - sg.tile_local0) * kTile;
     const int64_t hi = min(lo + kTile, sg.hi);
@@ -507,8 +536,14 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
     }
     if constexpr (MODE == kReduce || MODE == kNorm) {
       if (MODE == kNorm || (a.mode_flags & kFlagPartials)) {
-        double total = cta_norm_total(nacc, sh_hi, sh_lo, sh_big);
-        if (threadIdx.x == 0) a.partials[sg.tile_global0 + (g - sg.tile_local0)] = total;
+        // publish, one barrier, and the tile's fp64 total formed by warp
+        // (tile_no mod 8) so the fp64 work rotates over the warps
+        const int par = tile_no & 1;
+        tile_norm_publish(nacc, sh_norm, par, warp, lane);
+        __syncthreads();
+        if (warp == static_cast<int>(tile_no % kWarps) && lane == 0)
+          a.partials[sg.tile_global0 + (g - sg.tile_local0)] =
+              tile_norm_total(sh_norm, par, kWarps);
       }
     }
   }
@@ -517,15 +552,20 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 // -------------------------------------------------- bulk-copy pipeline --
 //
 // kFused, kReduce and kUpdate stream their inputs through shared memory.
-// One producer warp (its lane 0) walks the CTA's tiles and, per stage of
-// E = 256 * V elements, posts the byte count on the slot's "full" mbarrier
-// and issues one cp.async.bulk per input chunk (the N replica chunks in ring
-// order, then g and/or master, m, v). Eight consumer warps wait on "full",
-// compute from shared memory (thread t owns elements [t*V, t*V+V) of the
-// stage), write their results to global memory with streaming stores and
-// release the slot on its "empty" mbarrier. The number of slots S is chosen
-// so S stages fit in shared memory; S - 1 stages (~100+ KB per SM) are in
-// flight while one is computed, independent of the register budget.
+// Work is cut into element ranges of E = 2048 elements (a 4096-element tile
+// holds two). The inputs of one range are chunks: one per replica (ring
+// order, 4 KB) and the state block (master, m, v; for kUpdate also g;
+// 8 KB each). The host packs the chunks of a range into at most 64 KB
+// stages (StagePlan): N = 8 fused is one 56 KB stage, N = 64 fused is four
+// stages of 16 replicas and one state stage. One producer warp posts each
+// stage's byte count on the slot's "full" mbarrier and its 32 lanes issue
+// the stage's cp.async.bulk copies in parallel; eight consumer warps wait on
+// "full", accumulate the replicas of the stage in registers (thread t owns
+// elements [8t, 8t+8) of the range, held across the range's stages), finish
+// the step when the state block arrives, write results to global memory
+// with streaming stores and release the slot on its "empty" mbarrier. With
+// S slots, S - 1 stages (~100-170 KB per SM) are in flight while one is
+// computed, independent of the register budget.
 // Tile heads/tails that are not 16-byte aligned are done by the consumers
 // with plain loads (do_scalar).
 // Every mbarrier wait is bounded by kWaitLimitNs of %globaltimer; on expiry
@@ -535,16 +575,14 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kBulkThreads = kConsumers + 32;
+constexpr int kStageElems = kConsumers * 8;     // 2048
 constexpr int kMaxStages = 6;
-constexpr int kStageBudget = 72 * 1024;        // bytes per stage, upper bound
+constexpr int kStageBudget = 64 * 1024;         // bytes per stage, upper bound
 constexpr int kSmemCap = 216 * 1024;            // dynamic shared memory per CTA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-static_assert(kTile % (kConsumers * 8) == 0, "tile must hold whole stages");
-
-__host__ __device__ constexpr int bulk_bytes_per_elem(int mode, int n_ranks) {
-  return mode == kFused ? 2 * n_ranks + 12 : (mode == kReduce ? 2 * n_ranks : 16);
-}
+static_assert(kTile % kStageElems == 0, "tile must hold whole ranges");
+static_assert(kConsumerWarps <= kMaxWarps, "norm slots");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -647,138 +685,22 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
   return t;
 }
 
-// V consecutive 16-bit values from shared memory, widened
-template <bool kBf16, int V>
-__device__ __forceinline__ void lds_h(const unsigned char* p, float (&x)[V]) {
-  if constexpr (V == 8) {
-    uint4 w = *reinterpret_cast<const uint4*>(p);
-    widen8<kBf16>(w, x);
-  } else if constexpr (V == 4) {
-    uint2 w = *reinterpret_cast<const uint2*>(p);
-    x[0] = widen<kBf16>(w.x & 0xFFFFu);
-    x[1] = widen<kBf16>(w.x >> 16);
-    x[2] = widen<kBf16>(w.y & 0xFFFFu);
-    x[3] = widen<kBf16>(w.y >> 16);
-  } else {
-    uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-    x[0] = widen<kBf16>(w & 0xFFFFu);
-    x[1] = widen<kBf16>(w >> 16);
-  }
+__device__ __forceinline__ void lds_f8(const unsigned char* p, float (&x)[8]) {
+  float4 a = reinterpret_cast<const float4*>(p)[0];
+  float4 b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-template <int V>
-__device__ __forceinline__ void lds_f(const unsigned char* p, float (&x)[V]) {
-  if constexpr (V == 8) {
-    float4 a = reinterpret_cast<const float4*>(p)[0];
-    float4 b = reinterpret_cast<const float4*>(p)[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  } else if constexpr (V == 4) {
-    float4 a = *reinterpret_cast<const float4*>(p);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  } else {
-    float2 a = *reinterpret_cast<const float2*>(p);
-    x[0] = a.x; x[1] = a.y;
-  }
-}
-
-template <int V>
-__device__ __forceinline__ void stg_f(float* p, const float (&x)[V]) {
-  if constexpr (V == 8) {
-    store8f(p, x);
-  } else if constexpr (V == 4) {
-    __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
-  } else {
-    __stcs(reinterpret_cast<float2*>(p), make_float2(x[0], x[1]));
-  }
-}
-
-template <bool kBf16, int V>
-__device__ __forceinline__ void stg_h(uint16_t* p, const float (&x)[V]) {
-  uint32_t u[V / 2];
-#pragma unroll
-  for (int k = 0; k < V / 2; ++k)
-    u[k] = static_cast<uint32_t>(narrow<kBf16>(x[2 * k])) |
-           (static_cast<uint32_t>(narrow<kBf16>(x[2 * k + 1])) << 16);
-  if constexpr (V == 8) {
-    __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
-  } else if constexpr (V == 4) {
-    __stcs(reinterpret_cast<uint2*>(p), make_uint2(u[0], u[1]));
-  } else {
-    __stcs(reinterpret_cast<unsigned int*>(p), u[0]);
-  }
-}
-
-// One consumer thread's V elements of a stage held in shared memory.
-// Stage layout: kFused  [N replica chunks, 2E bytes each, ring order]
-//                       [master 4E][m 4E][v 4E]
-//               kReduce [N replica chunks]
-//               kUpdate [g 4E][master 4E][m 4E][v 4E]
-template <int MODE, bool kBf16, int V>
-__device__ __forceinline__ void do_stage(const Args& a, const StepScalars& s,
-                                         const unsigned char* buf, int64_t j, int32_t rank,
-                                         int t_off, NormAcc& nacc, bool& bad) {
-  constexpr int E = kConsumers * V;
-  const int64_t w = j - a.wbase;
-  const int64_t k = j - static_cast<int64_t>(rank) * a.shard;
-  float g[V], th[V], m[V], v[V];
-  const unsigned char* st = buf;
-  if constexpr (MODE == kFused || MODE == kReduce) {
-    const int N = a.n_ranks;
-    float acc[V];
-    lds_h<kBf16, V>(buf + t_off * 2, acc);
-#pragma unroll 4
-    for (int p = 1; p < N; ++p) {
-      float x[V];
-      lds_h<kBf16, V>(buf + static_cast<size_t>(p) * (2 * E) + t_off * 2, x);
-#pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      g[e] = __fmul_rn(acc[e], s.inv);
-      bad |= nonfinite(g[e]);
-    }
-    st = buf + static_cast<size_t>(N) * (2 * E);
-  }
-  if constexpr (MODE == kReduce) {
-    stg_f<V>(a.ghat[rank] + k, g);
-    if (a.mode_flags & kFlagPartials) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) nacc.add(g[e]);
-    }
-  }
-  if constexpr (MODE == kUpdate) {
-    lds_f<V>(buf + t_off * 4, g);
-    st = buf + 4 * E;
-    if (s.clip != 1.0f) {
-#pragma unroll
-      for (int e = 0; e < V; ++e) g[e] = __fmul_rn(g[e], s.clip);
-    }
-  }
-  if constexpr (MODE == kFused || MODE == kUpdate) {
-    lds_f<V>(st + t_off * 4, th);
-    lds_f<V>(st + 4 * E + t_off * 4, m);
-    lds_f<V>(st + 8 * E + t_off * 4, v);
-#pragma unroll
-    for (int e = 0; e < V; ++e) adamw(th[e], m[e], v[e], g[e], a, s);
-    stg_f<V>(a.master[s.dst][rank] + k, th);
-    stg_f<V>(a.mom[s.dst][rank] + k, m);
-    stg_f<V>(a.var[s.dst][rank] + k, v);
-    stg_h<kBf16, V>(a.flat + w, th);
-  }
-}
-
-template <int MODE, bool kBf16, int V>
+template <int MODE, bool kBf16>
 __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
                                                                int n_slots,
                                                                uint32_t slot_bytes) {
-  constexpr int E = kConsumers * V;
+  constexpr int E = kStageElems;
   __shared__ StepScalars sh_s;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ float sh_hi[kConsumerWarps], sh_lo[kConsumerWarps];
-  __shared__ double sh_big[kConsumerWarps];
+  __shared__ NormSlots sh_norm;
   __shared__ int sh_abort;
   extern __shared__ __align__(128) unsigned char stage_mem[];
 
@@ -796,71 +718,69 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   if (s.skip) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.n_ranks;
+  const int n_plan = a.plan.n;
   volatile int* abort_flag = &sh_abort;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     // lane 0 owns the barriers; the 32 lanes issue the stage's copies in
-    // parallel (chunk c by lane c mod 32), so N + 3 copies per stage do not
-    // serialise on one thread
+    // parallel (chunk c by lane c mod 32)
     const uint64_t pol = evict_first_policy();
-    const uint32_t bpe = bulk_bytes_per_elem(MODE, N);
-    constexpr int kStateChunks = MODE == kFused ? 3 : (MODE == kUpdate ? 4 : 0);
-    const int n_chunks = (MODE == kUpdate ? 0 : N) + kStateChunks;
     uint32_t it = 0;
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
       const TileGeom t = tile_geom(a, g);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
-      for (int64_t j0 = t.va; j0 < t.vb; j0 += E, ++it) {
+      for (int64_t j0 = t.va; j0 < t.vb && !stop; j0 += E) {
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
-        const int slot = static_cast<int>(it % n_slots);
-        const uint32_t k = it / n_slots;
-        int go = 1;
-        if (lane == 0) {
-          if (*abort_flag) {
-            go = 0;
-          } else if (!mbar_wait(&empty_bar[slot], (k & 1u) ^ 1u)) {
-            set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            go = 0;
-          } else {
-            mbar_expect_tx(&full_bar[slot], len * bpe);
-          }
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
-          stop = true;
-          break;
-        }
-        unsigned char* buf = stage_mem + static_cast<size_t>(slot) * slot_bytes;
         const int64_t w = j0 - a.wbase;
         const int64_t kk = j0 - rank0;
-        for (int c = lane; c < n_chunks; c += 32) {
-          if (MODE != kUpdate && c < N) {
-            int rr = t.first_rep + c;
-            if (rr >= N) rr -= N;
-            bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
-                     &full_bar[slot], pol);
-          } else {
-            // state chunks: kFused master, m, v after the replicas;
-            // kUpdate g, master, m, v
-            const int q = MODE == kUpdate ? c : c - N;
-            unsigned char* base =
-                MODE == kUpdate ? buf : buf + static_cast<size_t>(N) * (2 * E);
-            const float* src;
-            if (MODE == kUpdate) {
-              src = q == 0 ? a.ghat[t.rank]
-                           : (q == 1 ? a.master[s.src][t.rank]
-                                     : (q == 2 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]));
+        for (int st = 0; st < n_plan; ++st, ++it) {
+          const int slot = static_cast<int>(it % n_slots);
+          const uint32_t k = it / n_slots;
+          int go = 1;
+          if (lane == 0) {
+            if (*abort_flag) {
+              go = 0;
+            } else if (!mbar_wait(&empty_bar[slot], (k & 1u) ^ 1u)) {
+              set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              go = 0;
             } else {
-              src = q == 0 ? a.master[s.src][t.rank]
-                           : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
+              mbar_expect_tx(&full_bar[slot], len * static_cast<uint32_t>(a.plan.bytes_per_elem[st]));
             }
-            bulk_g2s(base + static_cast<size_t>(q) * (4 * E), src + kk, len * 4,
-                     &full_bar[slot], pol);
           }
+          if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
+            stop = true;
+            break;
+          }
+          unsigned char* buf = stage_mem + static_cast<size_t>(slot) * slot_bytes;
+          const int r_lo = a.plan.r_lo[st], r_hi = a.plan.r_hi[st];
+          const int n_rep = r_hi - r_lo;
+          const int n_state = a.plan.states[st] ? (MODE == kUpdate ? 4 : 3) : 0;
+          for (int c = lane; c < n_rep + n_state; c += 32) {
+            if (c < n_rep) {
+              int rr = t.first_rep + r_lo + c;
+              if (rr >= N) rr -= N;
+              bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
+                       &full_bar[slot], pol);
+            } else {
+              const int q = c - n_rep;
+              const float* src;
+              if (MODE == kUpdate) {
+                src = q == 0 ? a.ghat[t.rank]
+                             : (q == 1 ? a.master[s.src][t.rank]
+                                       : (q == 2 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]));
+              } else {
+                src = q == 0 ? a.master[s.src][t.rank]
+                             : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
+              }
+              bulk_g2s(buf + static_cast<size_t>(n_rep) * (2 * E) + static_cast<size_t>(q) * (4 * E),
+                       src + kk, len * 4, &full_bar[slot], pol);
+            }
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
     // make sure no copy is still landing when the CTA exits (bounded)
@@ -877,9 +797,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 
   // -------------------------------------------------------------- consumers
   const int tid = threadIdx.x;
+  const int t_off = tid * 8;
   uint32_t it = 0;
+  uint32_t tile_no = 0;
   bool dead = false;
-  for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x) {
+  for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
     const TileGeom t = tile_geom(a, g);
     NormAcc nacc;
     bool bad = false;
@@ -890,28 +812,87 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
       const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
       do_scalar<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad);
     }
-    for (int64_t j0 = t.va; j0 < t.vb; j0 += E, ++it) {
+    const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
+    for (int64_t j0 = t.va; j0 < t.vb; j0 += E) {
       const int len = static_cast<int>(min(static_cast<int64_t>(E), t.vb - j0));
-      const int slot = static_cast<int>(it % n_slots);
-      const uint32_t k = it / n_slots;
-      // keep `dead` uniform across the warp so the warp-level syncs below
-      // always see all 32 lanes
-      if (!dead) dead = __any_sync(0xFFFFFFFFu, *abort_flag != 0);
-      if (!dead) {
-        const bool landed = mbar_wait(&full_bar[slot], k & 1u);
-        if (!__all_sync(0xFFFFFFFFu, landed)) {
-          if (lane == 0) {
-            set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
-            *abort_flag = 1;
+      const bool mine = t_off < len;
+      const int64_t j = j0 + t_off;
+      const int64_t w = j - a.wbase;
+      const int64_t k = j - rank0;
+      float acc[8], gv[8];
+      for (int st = 0; st < n_plan; ++st, ++it) {
+        const int slot = static_cast<int>(it % n_slots);
+        const uint32_t ph = it / n_slots;
+        // keep `dead` uniform across the warp so the warp-level syncs below
+        // always see all 32 lanes
+        if (!dead) dead = __any_sync(0xFFFFFFFFu, *abort_flag != 0);
+        if (!dead) {
+          const bool landed = mbar_wait(&full_bar[slot], ph & 1u);
+          if (!__all_sync(0xFFFFFFFFu, landed)) {
+            if (lane == 0) {
+              set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+            }
+            dead = true;
           }
-          dead = true;
         }
-      }
-      if (!dead) {
-        const int t_off = tid * V;
-        if (t_off < len)
-          do_stage<MODE, kBf16, V>(a, s, stage_mem + static_cast<size_t>(slot) * slot_bytes,
-                                   j0 + t_off, t.rank, t_off, nacc, bad);
+        if (dead) continue;
+        const unsigned char* buf = stage_mem + static_cast<size_t>(slot) * slot_bytes;
+        const int r_lo = a.plan.r_lo[st], r_hi = a.plan.r_hi[st];
+        if (mine) {
+          if constexpr (MODE == kFused || MODE == kReduce) {
+            for (int p = r_lo; p < r_hi; ++p) {
+              float x[8];
+              widen8<kBf16>(*reinterpret_cast<const uint4*>(buf + static_cast<size_t>(p - r_lo) *
+                                                                        (2 * E) + t_off * 2),
+                            x);
+              if (p == 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = x[e];
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+              }
+            }
+            if (r_hi == N && r_lo < r_hi) {  // this stage completed the range's sum
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                gv[e] = __fmul_rn(acc[e], s.inv);
+                bad |= nonfinite(gv[e]);
+              }
+              if constexpr (MODE == kReduce) {
+                store8f(a.ghat[t.rank] + k, gv);
+                if (a.mode_flags & kFlagPartials) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) nacc.add(gv[e]);
+                }
+              }
+            }
+          }
+          if constexpr (MODE == kFused || MODE == kUpdate) {
+            if (a.plan.states[st]) {
+              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (2 * E);
+              if constexpr (MODE == kUpdate) {
+                lds_f8(sb + t_off * 4, gv);
+                sb += 4 * E;
+                if (s.clip != 1.0f) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) gv[e] = __fmul_rn(gv[e], s.clip);
+                }
+              }
+              float th[8], m[8], v[8];
+              lds_f8(sb + t_off * 4, th);
+              lds_f8(sb + 4 * E + t_off * 4, m);
+              lds_f8(sb + 8 * E + t_off * 4, v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) adamw(th[e], m[e], v[e], gv[e], a, s);
+              store8f(a.master[s.dst][t.rank] + k, th);
+              store8f(a.mom[s.dst][t.rank] + k, m);
+              store8f(a.var[s.dst][t.rank] + k, v);
+              __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(th));
+            }
+          }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
       }
@@ -921,38 +902,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     }
     if constexpr (MODE == kReduce) {
       if (a.mode_flags & kFlagPartials) {
-        // consumer-only version of cta_norm_total (named barrier 1)
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          float h2 = __shfl_down_sync(0xFFFFFFFFu, nacc.hi, off);
-          float l2 = __shfl_down_sync(0xFFFFFFFFu, nacc.lo, off);
-          if (lane < off) nacc.merge(h2, l2);
-        }
-        const bool big_here = __any_sync(0xFFFFFFFFu, nacc.big != 0.0);
-        double b = nacc.big;
-        if (big_here) {
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            double b2 = __shfl_down_sync(0xFFFFFFFFu, b, off);
-            if (lane < off) b = __dadd_rn(b, b2);
-          }
-        }
-        if (lane == 0) {
-          sh_hi[warp] = nacc.hi;
-          sh_lo[warp] = nacc.lo;
-          sh_big[warp] = big_here ? b : 0.0;
-        }
+        const int par = tile_no & 1;
+        tile_norm_publish(nacc, sh_norm, par, warp, lane);
         consumer_sync();
-        if (tid == 0) {
-          double total = 0.0;
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            total = __dadd_rn(total, __dadd_rn(static_cast<double>(sh_hi[w]),
-                                               static_cast<double>(sh_lo[w])));
-            if (sh_big[w] != 0.0) total = __dadd_rn(total, sh_big[w]);
-          }
-          a.partials[t.partial] = total;
-        }
-        consumer_sync();
+        if (warp == static_cast<int>(tile_no % kConsumerWarps) && lane == 0)
+          a.partials[t.partial] = tile_norm_total(sh_norm, par, kConsumerWarps);
       }
     }
   }
@@ -1027,57 +981,69 @@ int grid_size() {
   return sms * std::max(per_sm, 1);
 }
 
-// Bulk-pipeline launch parameters for MODE at N ranks: elements per
-// consumer thread V (largest of 8, 4, 2 whose stage fits kStageBudget),
-// slot bytes and number of slots.
-struct BulkShape {
-  int V, slots;
-  uint32_t slot_bytes;
-  size_t smem;
-};
-
-inline BulkShape bulk_shape(int mode, int n_ranks) {
-  BulkShape b{0, 0, 0, 0};
-  const int bpe = bulk_bytes_per_elem(mode, n_ranks);
-  for (int V = 8; V >= 2; V /= 2) {
-    const int stage = kConsumers * V * bpe;
-    if (stage <= kStageBudget) {
-      b.V = V;
-      b.slot_bytes = static_cast<uint32_t>((stage + 127) & ~127);
-      b.slots = std::min(kMaxStages, kSmemCap / static_cast<int>(b.slot_bytes));
-      b.smem = static_cast<size_t>(b.slots) * b.slot_bytes;
-      return b;
-    }
+// Greedy packing of one element range's chunks into stages of at most
+// kStageBudget bytes: replica chunks (2 bytes per element each) in ring
+// order, then the indivisible state block (kFused 12, kUpdate 16 bytes per
+// element) in the last stage if it fits, else in a stage of its own.
+inline StagePlan make_stage_plan(int mode, int n_ranks, uint32_t* slot_bytes) {
+  StagePlan pl{};
+  const int budget = kStageBudget / kStageElems;  // bytes per element
+  const int n_rep = mode == kUpdate ? 0 : n_ranks;
+  const int state_bpe = mode == kFused ? 12 : (mode == kUpdate ? 16 : 0);
+  int lo = 0, cur = 0;
+  int max_bpe = 0;
+  auto close = [&](int hi, int with_states) {
+    const int bpe = 2 * (hi - lo) + (with_states ? state_bpe : 0);
+    pl.r_lo[pl.n] = static_cast<int16_t>(lo);
+    pl.r_hi[pl.n] = static_cast<int16_t>(hi);
+    pl.states[pl.n] = with_states;
+    pl.bytes_per_elem[pl.n] = bpe;
+    max_bpe = std::max(max_bpe, bpe);
+    ++pl.n;
+    lo = hi;
+    cur = 0;
+  };
+  for (int p = 0; p < n_rep; ++p) {
+    if (cur + 2 > budget) close(p, 0);
+    cur += 2;
   }
-  return b;
+  if (state_bpe > 0) {
+    if (cur > 0 && cur + state_bpe <= budget) {
+      close(n_rep, 1);
+    } else {
+      if (cur > 0) close(n_rep, 0);
+      close(n_rep, 1);
+    }
+  } else if (cur > 0) {
+    close(n_rep, 0);
+  }
+  *slot_bytes = static_cast<uint32_t>((max_bpe * kStageElems + 127) & ~127);
+  return pl;
 }
 
-template <int MODE, bool kBf16, int V>
-int launch_bulk_v(Args& a, const BulkShape& b, int64_t tiles, cudaStream_t stream) {
-  auto kern = bulk_kernel<MODE, kBf16, V>;
+template <int MODE, bool kBf16>
+int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+  uint32_t slot_bytes = 0;
+  a.plan = make_stage_plan(MODE, a.n_ranks, &slot_bytes);
+  if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
+  const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));
+  if (slots < 2) return ZERO_ERANGE;
+  const size_t smem = static_cast<size_t>(slots) * slot_bytes;
+  auto kern = bulk_kernel<MODE, kBf16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(b.smem)) != cudaSuccess)
+                           static_cast<int>(smem)) != cudaSuccess)
     return ZERO_ECUDA;
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ZERO_ECUDA;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBulkThreads, b.smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBulkThreads, smem) !=
       cudaSuccess)
     return ZERO_ECUDA;
   const int64_t cap = static_cast<int64_t>(sms) * std::max(per_sm, 1);
   const int grid = static_cast<int>(std::min<int64_t>(tiles, cap));
-  kern<<<grid, kBulkThreads, b.smem, stream>>>(a, b.slots, b.slot_bytes);
+  kern<<<grid, kBulkThreads, smem, stream>>>(a, slots, slot_bytes);
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
-}
-
-template <int MODE, bool kBf16>
-int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
-  const BulkShape b = bulk_shape(MODE, a.n_ranks);
-  if (b.V == 8) return launch_bulk_v<MODE, kBf16, 8>(a, b, tiles, stream);
-  if (b.V == 4) return launch_bulk_v<MODE, kBf16, 4>(a, b, tiles, stream);
-  if (b.V == 2) return launch_bulk_v<MODE, kBf16, 2>(a, b, tiles, stream);
-  return ZERO_ERANGE;
 }
 
 template <int MODE, bool kBf16>
