@@ -198,87 +198,85 @@ __device__ __forceinline__ void adamw(float& th, float& m, float& v, float g, co
 // Squared-gradient accumulation with a float-float (hi, lo) pair: the square
 // is split exactly into p + e (e = fma(g, g, -p)), p is added with an exact
 // two-sum and all error terms collect in lo (relative accuracy ~2^-44 over a
-// tile). No per-element fp64 work: GB300's fp64 path is far too slow for
-// that. Magnitudes whose square would leave fp32's exact range
-// (|g| >= 2^60, or 0 < |g| <= 2^-60) go to an fp64 side sum, flagged so that
-// the common case never touches fp64.
+// tile). Everything here is fp32: GB300's fp64 path is far too slow for
+// per-element work. Magnitudes |g| >= 2^60, whose squares could overflow
+// fp32 sums, are scaled by 2^-64 and summed in a second pair (bhi, blo)
+// that stands for 2^128 times its value. Squares below 2^-126 are fp32
+// subnormals (absolute error < 2^-149 each).
+__device__ __forceinline__ void ff_add_sq(float& hi, float& lo, float g) {
+  float p = __fmul_rn(g, g);
+  float e = __fmaf_rn(g, g, -p);
+  float s = __fadd_rn(hi, p);
+  float bb = __fsub_rn(s, hi);
+  float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(err, e));
+}
+
+__device__ __forceinline__ void ff_merge(float& hi, float& lo, float h2, float l2) {
+  float s = __fadd_rn(hi, h2);
+  float bb = __fsub_rn(s, hi);
+  float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(h2, bb));
+  hi = s;
+  lo = __fadd_rn(__fadd_rn(lo, l2), err);
+}
+
 struct NormAcc {
-  float hi = 0.f, lo = 0.f;
-  double big = 0.0;
-  bool has_big = false;
+  float hi = 0.f, lo = 0.f;    // sum of g^2
+  float bhi = 0.f, blo = 0.f;  // sum of (g * 2^-64)^2 for |g| >= 2^60
   __device__ __forceinline__ void add(float g) {
-    float ag = fabsf(g);
-    if (ag < 0x1p60f && (ag > 0x1p-60f || ag == 0.f)) {
-      float p = __fmul_rn(g, g);
-      float e = __fmaf_rn(g, g, -p);
-      float s = __fadd_rn(hi, p);
-      float bb = __fsub_rn(s, hi);
-      float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(p, bb));
-      hi = s;
-      lo = __fadd_rn(lo, __fadd_rn(err, e));
+    if (fabsf(g) < 0x1p60f) {
+      ff_add_sq(hi, lo, g);
     } else {
-      double d = static_cast<double>(g);
-      big = __dadd_rn(big, __dmul_rn(d, d));
-      has_big = true;
+      ff_add_sq(bhi, blo, __fmul_rn(g, 0x1p-64f));
     }
   }
-  // (hi, lo) += (h2, l2), two-sum on the high parts
-  __device__ __forceinline__ void merge(float h2, float l2) {
-    float s = __fadd_rn(hi, h2);
-    float bb = __fsub_rn(s, hi);
-    float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(h2, bb));
-    hi = s;
-    lo = __fadd_rn(__fadd_rn(lo, l2), err);
+  __device__ __forceinline__ void merge(float h2, float l2, float bh2, float bl2) {
+    ff_merge(hi, lo, h2, l2);
+    if (bh2 != 0.f || bl2 != 0.f || bhi != 0.f) ff_merge(bhi, blo, bh2, bl2);
   }
 };
 
 // Per-warp tile sums published to shared memory, double-buffered by tile
 // parity so that one barrier per tile suffices.
-constexpr int kMaxWarps = 8;
+constexpr int kMaxWarps = 16;
 struct NormSlots {
-  float hi[2][kMaxWarps];
-  float lo[2][kMaxWarps];
-  double big[2][kMaxWarps];
-  int has_big[2][kMaxWarps];
+  float hi[2][kMaxWarps], lo[2][kMaxWarps], bhi[2][kMaxWarps], blo[2][kMaxWarps];
 };
 
-// Fixed shuffle tree inside the warp, then lane 0 publishes the warp's sum.
+// Fixed shuffle tree inside the warp, then lane 0 publishes the warp's sums.
 __device__ __forceinline__ void tile_norm_publish(NormAcc acc, NormSlots& sl, int par, int warp,
                                                   int lane) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     float h2 = __shfl_down_sync(0xFFFFFFFFu, acc.hi, off);
     float l2 = __shfl_down_sync(0xFFFFFFFFu, acc.lo, off);
-    if (lane < off) acc.merge(h2, l2);
-  }
-  const bool any_big = __any_sync(0xFFFFFFFFu, acc.has_big);
-  double b = acc.big;
-  if (any_big) {  // rare: fp64 only when a lane saw an out-of-range magnitude
-    if (!acc.has_big) b = 0.0;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      double b2 = __shfl_down_sync(0xFFFFFFFFu, b, off);
-      if (lane < off) b = __dadd_rn(b, b2);
-    }
+    float bh2 = __shfl_down_sync(0xFFFFFFFFu, acc.bhi, off);
+    float bl2 = __shfl_down_sync(0xFFFFFFFFu, acc.blo, off);
+    if (lane < off) acc.merge(h2, l2, bh2, bl2);
   }
   if (lane == 0) {
     sl.hi[par][warp] = acc.hi;
     sl.lo[par][warp] = acc.lo;
-    sl.big[par][warp] = b;
-    sl.has_big[par][warp] = any_big ? 1 : 0;
+    sl.bhi[par][warp] = acc.bhi;
+    sl.blo[par][warp] = acc.blo;
   }
 }
 
-// After the barrier: warps' sums merged in warp order in float-float, then
-// one conversion to fp64 (plus the rare fp64 side sums, in warp order).
+// After the barrier: warps' sums merged in warp order in float-float, then a
+// handful of fp64 operations for the tile's total.
 __device__ __forceinline__ double tile_norm_total(const NormSlots& sl, int par, int n_warps) {
   NormAcc t;
   t.hi = sl.hi[par][0];
   t.lo = sl.lo[par][0];
-  for (int w = 1; w < n_warps; ++w) t.merge(sl.hi[par][w], sl.lo[par][w]);
+  t.bhi = sl.bhi[par][0];
+  t.blo = sl.blo[par][0];
+  for (int w = 1; w < n_warps; ++w) t.merge(sl.hi[par][w], sl.lo[par][w], sl.bhi[par][w], sl.blo[par][w]);
   double total = __dadd_rn(static_cast<double>(t.hi), static_cast<double>(t.lo));
-  for (int w = 0; w < n_warps; ++w)
-    if (sl.has_big[par][w]) total = __dadd_rn(total, sl.big[par][w]);
+  if (t.bhi != 0.f || t.blo != 0.f)
+    total = __dadd_rn(total, __dmul_rn(__dadd_rn(static_cast<double>(t.bhi),
+                                                 static_cast<double>(t.blo)),
+                                       0x1p128));
   return total;
 }
 
@@ -559,9 +557,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 // stages (StagePlan): N = 8 fused is one 56 KB stage, N = 64 fused is four
 // stages of 16 replicas and one state stage. One producer warp posts each
 // stage's byte count on the slot's "full" mbarrier and its 32 lanes issue
-// the stage's cp.async.bulk copies in parallel; eight consumer warps wait on
+// the stage's cp.async.bulk copies in parallel; sixteen consumer warps wait on
 // "full", accumulate the replicas of the stage in registers (thread t owns
-// elements [8t, 8t+8) of the range, held across the range's stages), finish
+// elements [4t, 4t+4) of the range, held across the range's stages), finish
 // the step when the state block arrives, write results to global memory
 // with streaming stores and release the slot on its "empty" mbarrier. With
 // S slots, S - 1 stages (~100-170 KB per SM) are in flight while one is
@@ -572,10 +570,11 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 // the thread records ZERO_DEVERR_TIMEOUT, the CTA stops issuing, the
 // producer waits (again bounded) for the copies it issued, and all return.
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kBulkThreads = kConsumers + 32;
-constexpr int kStageElems = kConsumers * 8;     // 2048
+constexpr int kStageElems = 2048;
+constexpr int kEPT = kStageElems / kConsumers;   // elements per consumer thread: 4
 constexpr int kMaxStages = 6;
 constexpr int kStageBudget = 64 * 1024;         // bytes per stage, upper bound
 constexpr int kSmemCap = 216 * 1024;            // dynamic shared memory per CTA
@@ -685,11 +684,31 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
   return t;
 }
 
-__device__ __forceinline__ void lds_f8(const unsigned char* p, float (&x)[8]) {
-  float4 a = reinterpret_cast<const float4*>(p)[0];
-  float4 b = reinterpret_cast<const float4*>(p)[1];
+__device__ __forceinline__ void lds_f4(const unsigned char* p, float (&x)[4]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void lds_h4(const unsigned char* p, float (&x)[4]) {
+  uint2 w = *reinterpret_cast<const uint2*>(p);
+  x[0] = widen<kBf16>(w.x & 0xFFFFu);
+  x[1] = widen<kBf16>(w.x >> 16);
+  x[2] = widen<kBf16>(w.y & 0xFFFFu);
+  x[3] = widen<kBf16>(w.y >> 16);
+}
+
+__device__ __forceinline__ void stg_f4(float* p, const float (&x)[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void stg_h4(uint16_t* p, const float (&x)[4]) {
+  const uint32_t u0 = static_cast<uint32_t>(narrow<kBf16>(x[0])) |
+                      (static_cast<uint32_t>(narrow<kBf16>(x[1])) << 16);
+  const uint32_t u1 = static_cast<uint32_t>(narrow<kBf16>(x[2])) |
+                      (static_cast<uint32_t>(narrow<kBf16>(x[3])) << 16);
+  __stcs(reinterpret_cast<uint2*>(p), make_uint2(u0, u1));
 }
 
 template <int MODE, bool kBf16>
@@ -797,7 +816,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 
   // -------------------------------------------------------------- consumers
   const int tid = threadIdx.x;
-  const int t_off = tid * 8;
+  const int t_off = tid * kEPT;
   uint32_t it = 0;
   uint32_t tile_no = 0;
   bool dead = false;
@@ -819,7 +838,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
       const int64_t j = j0 + t_off;
       const int64_t w = j - a.wbase;
       const int64_t k = j - rank0;
-      float acc[8], gv[8];
+      // ring sum in fp32, starting from -0 (x + -0 == x for every x, so this
+      // equals starting from the first replica's value)
+      float acc[kEPT], gv[kEPT];
+#pragma unroll
+      for (int e = 0; e < kEPT; ++e) acc[e] = -0.0f;
       for (int st = 0; st < n_plan; ++st, ++it) {
         const int slot = static_cast<int>(it % n_slots);
         const uint32_t ph = it / n_slots;
@@ -841,30 +864,25 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         const int r_lo = a.plan.r_lo[st], r_hi = a.plan.r_hi[st];
         if (mine) {
           if constexpr (MODE == kFused || MODE == kReduce) {
-            for (int p = r_lo; p < r_hi; ++p) {
-              float x[8];
-              widen8<kBf16>(*reinterpret_cast<const uint4*>(buf + static_cast<size_t>(p - r_lo) *
-                                                                        (2 * E) + t_off * 2),
-                            x);
-              if (p == 0) {
+            const unsigned char* rp = buf + t_off * 2;
+#pragma unroll 4
+            for (int p = r_lo; p < r_hi; ++p, rp += 2 * E) {
+              float x[kEPT];
+              lds_h4<kBf16>(rp, x);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = x[e];
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
-              }
+              for (int e = 0; e < kEPT; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
             }
             if (r_hi == N && r_lo < r_hi) {  // this stage completed the range's sum
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
+              for (int e = 0; e < kEPT; ++e) {
                 gv[e] = __fmul_rn(acc[e], s.inv);
                 bad |= nonfinite(gv[e]);
               }
               if constexpr (MODE == kReduce) {
-                store8f(a.ghat[t.rank] + k, gv);
+                stg_f4(a.ghat[t.rank] + k, gv);
                 if (a.mode_flags & kFlagPartials) {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) nacc.add(gv[e]);
+                  for (int e = 0; e < kEPT; ++e) nacc.add(gv[e]);
                 }
               }
             }
@@ -873,23 +891,23 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             if (a.plan.states[st]) {
               const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (2 * E);
               if constexpr (MODE == kUpdate) {
-                lds_f8(sb + t_off * 4, gv);
+                lds_f4(sb + t_off * 4, gv);
                 sb += 4 * E;
                 if (s.clip != 1.0f) {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) gv[e] = __fmul_rn(gv[e], s.clip);
+                  for (int e = 0; e < kEPT; ++e) gv[e] = __fmul_rn(gv[e], s.clip);
                 }
               }
-              float th[8], m[8], v[8];
-              lds_f8(sb + t_off * 4, th);
-              lds_f8(sb + 4 * E + t_off * 4, m);
-              lds_f8(sb + 8 * E + t_off * 4, v);
+              float th[kEPT], m[kEPT], v[kEPT];
+              lds_f4(sb + t_off * 4, th);
+              lds_f4(sb + 4 * E + t_off * 4, m);
+              lds_f4(sb + 8 * E + t_off * 4, v);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) adamw(th[e], m[e], v[e], gv[e], a, s);
-              store8f(a.master[s.dst][t.rank] + k, th);
-              store8f(a.mom[s.dst][t.rank] + k, m);
-              store8f(a.var[s.dst][t.rank] + k, v);
-              __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(th));
+              for (int e = 0; e < kEPT; ++e) adamw(th[e], m[e], v[e], gv[e], a, s);
+              stg_f4(a.master[s.dst][t.rank] + k, th);
+              stg_f4(a.mom[s.dst][t.rank] + k, m);
+              stg_f4(a.var[s.dst][t.rank] + k, v);
+              stg_h4<kBf16>(a.flat + w, th);
             }
           }
         }
