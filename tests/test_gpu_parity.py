@@ -115,7 +115,8 @@ def test_clip_inactive_equals_no_clip():
 
 def test_clip_active_two_pass_recomputed_norm():
     """zero_grad_norm recomputing the partials from the reduced gradients
-    gives the same result as the partials left by zero_reduce_scatter."""
+    agrees with the partials left by zero_reduce_scatter (both fixed-order,
+    with different per-thread groupings: equal within the norm tolerance)."""
     import fsdp_sharded_mixed_shard_gb300 as Z
     wl = W.Workload("clipnorm", [200_003], 4, 30_000, True, 22, 1e-2, max_grad_norm=0.5,
                     steps=1)
@@ -128,7 +129,10 @@ def test_clip_active_two_pass_recomputed_norm():
     a = g.read_scaler()
     Z.zero_grad_norm(g.plan, 0, 4, g.ghat_ptrs(), g.hp, sc, ws, st)
     b = g.read_scaler()
-    assert a.norm_sq == b.norm_sq and a.clip_coef == b.clip_coef and a.clip_apply == 1
+    from parity_util import norm_tol
+    assert abs(a.norm_sq - b.norm_sq) <= norm_tol(g.info.psi_pad) * b.norm_sq
+    assert abs(float(a.clip_coef) - float(b.clip_coef)) <= 2.0 ** -23 * float(b.clip_coef)
+    assert a.clip_apply == 1 and b.clip_apply == 1
     g.close()
 
 
