@@ -174,3 +174,30 @@ def test_missing_norm_sets_device_error():
     assert s.error == 2
     assert torch.equal(before, g.state)
     g.close()
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_widening_all_16bit_patterns(bf16):
+    """One rank, loss scale 1: the reduced gradient is the replica value
+    widened exactly, for every one of the 65536 bit patterns (NaNs compared
+    as NaN), and every non-finite pattern raises the flag."""
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    n = 65536
+    wl = W.Workload("widen", [n], 1, 4096, bf16, 1, 1e-3, steps=1, max_grad_norm=1.0)
+    g = harness.Group(wl)
+    g.init_state()
+    pats = torch.arange(n, dtype=torch.int32).to(torch.int16)
+    g.replicas[0, :n].copy_(pats.to(g.device))
+    g.flags.zero_()
+    sc = g.scaler.data_ptr()
+    Z.zero_reduce_scatter(g.plan, -1, 0, 1, g.rep_ptrs(), 0, g.ghat_ptrs(), sc,
+                          g.flags.data_ptr(), g.workspace.data_ptr(), g.sptr)
+    got = g.ghat[0, :n].cpu().numpy()
+    want = oracle.widen16(np.arange(n, dtype=np.uint16), bf16)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+    bad_bucket = ~np.isfinite(want).reshape(-1, 4096).all(axis=1)
+    assert np.array_equal(g.flags_u32() != 0, bad_bucket)
+    assert g.read_scaler().pending == 1
+    g.close()
