@@ -201,10 +201,11 @@ __device__ __forceinline__ void adamw(float& th, float& m, float& v, float g, co
 // is split exactly into p + e (e = fma(g, g, -p)), p is added with an exact
 // two-sum and all error terms collect in lo (relative accuracy ~2^-44 over a
 // tile). Everything here is fp32: GB300's fp64 path is far too slow for
-// per-element work. Magnitudes |g| >= 2^60, whose squares could overflow
-// fp32 sums, are scaled by 2^-64 and summed in a second pair (bhi, blo)
-// that stands for 2^128 times its value. Squares below 2^-126 are fp32
-// subnormals (absolute error < 2^-149 each).
+// per-element work. Magnitudes |g| >= 2^56 are scaled by 2^-96 and summed in
+// a second pair (bhi, blo) that stands for 2^192 times its value, so no
+// per-tile sum can overflow; a NaN or infinite g lands in the second pair
+// and leaves it non-finite. Squares below 2^-126 are fp32 subnormals
+// (absolute error < 2^-149 each).
 __device__ __forceinline__ void ff_add_sq(float& hi, float& lo, float g) {
   float p = __fmul_rn(g, g);
   float e = __fmaf_rn(g, g, -p);
@@ -223,15 +224,22 @@ __device__ __forceinline__ void ff_merge(float& hi, float& lo, float h2, float l
   lo = __fadd_rn(__fadd_rn(lo, l2), err);
 }
 
+constexpr float kNormMainLimit = 0x1p56f;
+constexpr float kNormBigScale = 0x1p-96f;
+
 struct NormAcc {
-  float hi = 0.f, lo = 0.f;    // sum of g^2
-  float bhi = 0.f, blo = 0.f;  // sum of (g * 2^-64)^2 for |g| >= 2^60
+  float hi = 0.f, lo = 0.f;    // sum of g^2 for |g| < 2^56
+  float bhi = 0.f, blo = 0.f;  // sum of (g * 2^-96)^2 for the rest
   __device__ __forceinline__ void add(float g) {
-    if (fabsf(g) < 0x1p60f) {
+    if (fabsf(g) < kNormMainLimit) {
       ff_add_sq(hi, lo, g);
     } else {
-      ff_add_sq(bhi, blo, __fmul_rn(g, 0x1p-64f));
+      ff_add_sq(bhi, blo, __fmul_rn(g, kNormBigScale));
     }
+  }
+  // true if any added g was NaN or infinite
+  __device__ __forceinline__ bool nonfinite_seen() const {
+    return !(fabsf(bhi) <= 3.4028234663852886e38f) || !(fabsf(blo) <= 3.4028234663852886e38f);
   }
   __device__ __forceinline__ void merge(float h2, float l2, float bh2, float bl2) {
     ff_merge(hi, lo, h2, l2);
@@ -278,7 +286,7 @@ __device__ __forceinline__ double tile_norm_total(const NormSlots& sl, int par, 
   if (t.bhi != 0.f || t.blo != 0.f)
     total = __dadd_rn(total, __dmul_rn(__dadd_rn(static_cast<double>(t.bhi),
                                                  static_cast<double>(t.blo)),
-                                       0x1p128));
+                                       0x1p192));
   return total;
 }
 
@@ -713,6 +721,52 @@ __device__ __forceinline__ void stg_h4(uint16_t* p, const float (&x)[4]) {
   __stcs(reinterpret_cast<uint2*>(p), make_uint2(u0, u1));
 }
 
+// acc[e] += replica chunks 0..R-1 of this thread's 4 elements, in order;
+// all R shared-memory loads are issued before the adds.
+template <bool kBf16, int R>
+__device__ __forceinline__ void acc_reps(const unsigned char* rp, float (&acc)[kEPT]) {
+  uint2 w[R];
+#pragma unroll
+  for (int p = 0; p < R; ++p)
+    w[p] = *reinterpret_cast<const uint2*>(rp + static_cast<size_t>(p) * (2 * kStageElems));
+#pragma unroll
+  for (int p = 0; p < R; ++p) {
+    const float x0 = widen<kBf16>(w[p].x & 0xFFFFu), x1 = widen<kBf16>(w[p].x >> 16);
+    const float x2 = widen<kBf16>(w[p].y & 0xFFFFu), x3 = widen<kBf16>(w[p].y >> 16);
+    acc[0] = __fadd_rn(acc[0], x0);
+    acc[1] = __fadd_rn(acc[1], x1);
+    acc[2] = __fadd_rn(acc[2], x2);
+    acc[3] = __fadd_rn(acc[3], x3);
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void acc_stage(const unsigned char* rp, int n, float (&acc)[kEPT]) {
+  switch (n) {
+    case 1: acc_reps<kBf16, 1>(rp, acc); break;
+    case 2: acc_reps<kBf16, 2>(rp, acc); break;
+    case 3: acc_reps<kBf16, 3>(rp, acc); break;
+    case 4: acc_reps<kBf16, 4>(rp, acc); break;
+    case 5: acc_reps<kBf16, 5>(rp, acc); break;
+    case 6: acc_reps<kBf16, 6>(rp, acc); break;
+    case 7: acc_reps<kBf16, 7>(rp, acc); break;
+    case 8: acc_reps<kBf16, 8>(rp, acc); break;
+    case 9: acc_reps<kBf16, 9>(rp, acc); break;
+    case 10: acc_reps<kBf16, 10>(rp, acc); break;
+    case 11: acc_reps<kBf16, 11>(rp, acc); break;
+    case 12: acc_reps<kBf16, 12>(rp, acc); break;
+    case 13: acc_reps<kBf16, 13>(rp, acc); break;
+    case 14: acc_reps<kBf16, 14>(rp, acc); break;
+    case 15: acc_reps<kBf16, 15>(rp, acc); break;
+    case 16: acc_reps<kBf16, 16>(rp, acc); break;
+    default:
+      for (int p = 0; p < n; p += 16) {
+        const int m = n - p < 16 ? n - p : 16;
+        acc_stage<kBf16>(rp + static_cast<size_t>(p) * (2 * kStageElems), m, acc);
+      }
+  }
+}
+
 template <int MODE, bool kBf16>
 __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
                                                                int n_slots,
@@ -748,6 +802,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     // parallel (chunk c by lane c mod 32)
     const uint64_t pol = evict_first_policy();
     uint32_t it = 0;
+    int slot = 0;
+    uint32_t phase = 0;  // == (it / n_slots) & 1
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
       const TileGeom t = tile_geom(a, g);
@@ -757,13 +813,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         const int64_t w = j0 - a.wbase;
         const int64_t kk = j0 - rank0;
         for (int st = 0; st < n_plan; ++st, ++it) {
-          const int slot = static_cast<int>(it % n_slots);
-          const uint32_t k = it / n_slots;
           int go = 1;
           if (lane == 0) {
             if (*abort_flag) {
               go = 0;
-            } else if (!mbar_wait(&empty_bar[slot], (k & 1u) ^ 1u)) {
+            } else if (!mbar_wait(&empty_bar[slot], phase ^ 1u)) {
               set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
               *abort_flag = 1;
               go = 0;
@@ -801,6 +855,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             }
           }
           __syncwarp();
+          if (++slot == n_slots) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
@@ -819,9 +877,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   // -------------------------------------------------------------- consumers
   const int tid = threadIdx.x;
   const int t_off = tid * kEPT;
-  uint32_t it = 0;
+  int slot = 0;
+  uint32_t phase = 0;
   uint32_t tile_no = 0;
   bool dead = false;
+  const bool partials = MODE == kReduce && (a.mode_flags & kFlagPartials);
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
     const TileGeom t = tile_geom(a, g);
     NormAcc nacc;
@@ -845,14 +905,18 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
       float acc[kEPT], gv[kEPT];
 #pragma unroll
       for (int e = 0; e < kEPT; ++e) acc[e] = -0.0f;
-      for (int st = 0; st < n_plan; ++st, ++it) {
-        const int slot = static_cast<int>(it % n_slots);
-        const uint32_t ph = it / n_slots;
+      for (int st = 0; st < n_plan; ++st) {
+        const int cur = slot;
+        const uint32_t ph = phase;
+        if (++slot == n_slots) {
+          slot = 0;
+          phase ^= 1u;
+        }
         // keep `dead` uniform across the warp so the warp-level syncs below
         // always see all 32 lanes
         if (!dead) dead = __any_sync(0xFFFFFFFFu, *abort_flag != 0);
         if (!dead) {
-          const bool landed = mbar_wait(&full_bar[slot], ph & 1u);
+          const bool landed = mbar_wait(&full_bar[cur], ph);
           if (!__all_sync(0xFFFFFFFFu, landed)) {
             if (lane == 0) {
               set_error(a.scaler, ZERO_DEVERR_TIMEOUT);
@@ -862,33 +926,42 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
           }
         }
         if (dead) continue;
-        const unsigned char* buf = stage_mem + static_cast<size_t>(slot) * slot_bytes;
+        const unsigned char* buf = stage_mem + static_cast<size_t>(cur) * slot_bytes;
         const int r_lo = a.plan.r_lo[st], r_hi = a.plan.r_hi[st];
-        if (mine) {
-          if constexpr (MODE == kFused || MODE == kReduce) {
-            const unsigned char* rp = buf + t_off * 2;
-#pragma unroll 4
-            for (int p = r_lo; p < r_hi; ++p, rp += 2 * E) {
-              float x[kEPT];
-              lds_h4<kBf16>(rp, x);
+        if constexpr (MODE == kFused || MODE == kReduce) {
+          const bool completes = r_hi == N && r_lo < r_hi;  // stage ends the range's sum
+          if (mine) {
+            acc_stage<kBf16>(buf + t_off * 2, r_hi - r_lo, acc);
+            if (completes) {
 #pragma unroll
-              for (int e = 0; e < kEPT; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
-            }
-            if (r_hi == N && r_lo < r_hi) {  // this stage completed the range's sum
+              for (int e = 0; e < kEPT; ++e) gv[e] = __fmul_rn(acc[e], s.inv);
+              if (!partials) {
 #pragma unroll
-              for (int e = 0; e < kEPT; ++e) {
-                gv[e] = __fmul_rn(acc[e], s.inv);
-                bad |= nonfinite(gv[e]);
+                for (int e = 0; e < kEPT; ++e) bad |= nonfinite(gv[e]);
               }
-              if constexpr (MODE == kReduce) {
-                stg_f4(a.ghat[t.rank] + k, gv);
-                if (a.mode_flags & kFlagPartials) {
-#pragma unroll
-                  for (int e = 0; e < kEPT; ++e) nacc.add(gv[e]);
-                }
-              }
+              if constexpr (MODE == kReduce) stg_f4(a.ghat[t.rank] + k, gv);
             }
           }
+          if (partials && completes) {
+            // squares of this thread's elements: one warp-wide range check,
+            // then the straight-line fp32 path (non-finite values show up in
+            // the accumulators, checked once per tile)
+            float q[kEPT];
+#pragma unroll
+            for (int e = 0; e < kEPT; ++e) q[e] = mine ? gv[e] : 0.0f;
+            bool in_range = true;
+#pragma unroll
+            for (int e = 0; e < kEPT; ++e) in_range &= fabsf(q[e]) < kNormMainLimit;
+            if (__all_sync(0xFFFFFFFFu, in_range)) {
+#pragma unroll
+              for (int e = 0; e < kEPT; ++e) ff_add_sq(nacc.hi, nacc.lo, q[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < kEPT; ++e) nacc.add(q[e]);
+            }
+          }
+        }
+        if (mine) {
           if constexpr (MODE == kFused || MODE == kUpdate) {
             if (a.plan.states[st]) {
               const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (2 * E);
@@ -914,10 +987,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+        if (lane == 0) mbar_arrive(&empty_bar[cur]);
       }
     }
     if constexpr (MODE == kFused || MODE == kReduce) {
+      if (partials) bad |= nacc.nonfinite_seen();
       if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a, t.bucket);
     }
     if constexpr (MODE == kReduce) {
