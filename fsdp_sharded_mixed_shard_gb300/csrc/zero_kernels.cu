@@ -759,11 +759,9 @@ __device__ __forceinline__ void acc_stage(const unsigned char* rp, int n, float 
     case 14: acc_reps<kBf16, 14>(rp, acc); break;
     case 15: acc_reps<kBf16, 15>(rp, acc); break;
     case 16: acc_reps<kBf16, 16>(rp, acc); break;
-    default:
-      for (int p = 0; p < n; p += 16) {
-        const int m = n - p < 16 ? n - p : 16;
-        acc_stage<kBf16>(rp + static_cast<size_t>(p) * (2 * kStageElems), m, acc);
-      }
+    default:  // the stage plan never puts more than 16 replicas in a stage
+      for (int p = 0; p < n; ++p)
+        acc_reps<kBf16, 1>(rp + static_cast<size_t>(p) * (2 * kStageElems), acc);
   }
 }
 
