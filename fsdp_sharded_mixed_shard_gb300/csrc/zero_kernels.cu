@@ -721,8 +721,27 @@ __device__ __forceinline__ void stg_h4(uint16_t* p, const float (&x)[4]) {
   __stcs(reinterpret_cast<uint2*>(p), make_uint2(u0, u1));
 }
 
-// acc[e] += replica chunks 0..R-1 of this thread's 4 elements, in order;
-// all R shared-memory loads are issued before the adds.
+// a0 += low half of w, a1 += high half of w, each 16-bit value widened
+// exactly to fp32 and the sum rounded once to nearest even: sm_100+'s
+// mixed-precision add (PTX add.rn.f32.f16 / add.rn.f32.bf16) does the
+// widening inside the add, one instruction per element and replica.
+template <bool kBf16>
+__device__ __forceinline__ void add_halves(float& a0, float& a1, uint32_t w) {
+  if constexpr (kBf16) {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+        " add.rn.f32.bf16 %0, l, %0;\n add.rn.f32.bf16 %1, h, %1;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
+  } else {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+        " add.rn.f32.f16 %0, l, %0;\n add.rn.f32.f16 %1, h, %1;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
+  }
+}
+
+// acc[e] += replica chunks 0..R-1 of this thread's 4 elements, in ring
+// order; all R shared-memory loads are issued before the adds.
 template <bool kBf16, int R>
 __device__ __forceinline__ void acc_reps(const unsigned char* rp, float (&acc)[kEPT]) {
   uint2 w[R];
@@ -731,12 +750,8 @@ __device__ __forceinline__ void acc_reps(const unsigned char* rp, float (&acc)[k
     w[p] = *reinterpret_cast<const uint2*>(rp + static_cast<size_t>(p) * (2 * kStageElems));
 #pragma unroll
   for (int p = 0; p < R; ++p) {
-    const float x0 = widen<kBf16>(w[p].x & 0xFFFFu), x1 = widen<kBf16>(w[p].x >> 16);
-    const float x2 = widen<kBf16>(w[p].y & 0xFFFFu), x3 = widen<kBf16>(w[p].y >> 16);
-    acc[0] = __fadd_rn(acc[0], x0);
-    acc[1] = __fadd_rn(acc[1], x1);
-    acc[2] = __fadd_rn(acc[2], x2);
-    acc[3] = __fadd_rn(acc[3], x3);
+    add_halves<kBf16>(acc[0], acc[1], w[p].x);
+    add_halves<kBf16>(acc[2], acc[3], w[p].y);
   }
 }
 
