@@ -227,6 +227,50 @@ __device__ __forceinline__ void ff_merge(float& hi, float& lo, float h2, float l
 constexpr float kNormMainLimit = 0x1p56f;
 constexpr float kNormBigScale = 0x1p-96f;
 
+// Packed form of ff_add_sq for two independent accumulators at once, with
+// sm_100+'s paired fp32 instructions (PTX add/sub/mul/fma .rn.f32x2: each
+// lane is the ordinary IEEE fp32 operation, so lane k computes exactly what
+// ff_add_sq computes).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t x, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_neg(uint64_t a) { return a ^ 0x8000000080000000ull; }
+
+__device__ __forceinline__ void ff2_add_sq(uint64_t& hi, uint64_t& lo, uint64_t g) {
+  const uint64_t p = f2_mul(g, g);
+  const uint64_t e = f2_fma(g, g, f2_neg(p));
+  const uint64_t s = f2_add(hi, p);
+  const uint64_t bb = f2_sub(s, hi);
+  const uint64_t err = f2_add(f2_sub(hi, f2_sub(s, bb)), f2_sub(p, bb));
+  hi = s;
+  lo = f2_add(lo, f2_add(err, e));
+}
+
 struct NormAcc {
   float hi = 0.f, lo = 0.f;    // sum of g^2 for |g| < 2^56
   float bhi = 0.f, blo = 0.f;  // sum of (g * 2^-96)^2 for the rest
@@ -898,6 +942,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
     const TileGeom t = tile_geom(a, g);
     NormAcc nacc;
+    uint64_t phi = 0, plo = 0;  // packed in-range accumulators (elements 0,2 | 1,3)
     bool bad = false;
     // unaligned head [lo, va) and tail [vb, hi) with plain loads
     const int nhead = static_cast<int>(t.va - t.lo);
@@ -946,8 +991,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
           if (mine) {
             acc_stage<kBf16>(buf + t_off * 2, r_hi - r_lo, acc);
             if (completes) {
-#pragma unroll
-              for (int e = 0; e < kEPT; ++e) gv[e] = __fmul_rn(acc[e], s.inv);
+              {
+                const uint64_t inv2 = f2_pack(s.inv, s.inv);
+                f2_unpack(f2_mul(f2_pack(acc[0], acc[1]), inv2), gv[0], gv[1]);
+                f2_unpack(f2_mul(f2_pack(acc[2], acc[3]), inv2), gv[2], gv[3]);
+              }
               if (!partials) {
 #pragma unroll
                 for (int e = 0; e < kEPT; ++e) bad |= nonfinite(gv[e]);
@@ -966,8 +1014,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 #pragma unroll
             for (int e = 0; e < kEPT; ++e) in_range &= fabsf(q[e]) < kNormMainLimit;
             if (__all_sync(0xFFFFFFFFu, in_range)) {
-#pragma unroll
-              for (int e = 0; e < kEPT; ++e) ff_add_sq(nacc.hi, nacc.lo, q[e]);
+              ff2_add_sq(phi, plo, f2_pack(q[0], q[1]));
+              ff2_add_sq(phi, plo, f2_pack(q[2], q[3]));
             } else {
 #pragma unroll
               for (int e = 0; e < kEPT; ++e) nacc.add(q[e]);
@@ -1004,7 +1052,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
       }
     }
     if constexpr (MODE == kFused || MODE == kReduce) {
-      if (partials) bad |= nacc.nonfinite_seen();
+      if (partials) {
+        float h0, h1, l0, l1;
+        f2_unpack(phi, h0, h1);
+        f2_unpack(plo, l0, l1);
+        nacc.merge(h0, l0, 0.f, 0.f);
+        nacc.merge(h1, l1, 0.f, 0.f);
+        bad |= nacc.nonfinite_seen();
+      }
       if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a, t.bucket);
     }
     if constexpr (MODE == kReduce) {
