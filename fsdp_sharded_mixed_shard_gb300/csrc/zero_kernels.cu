@@ -75,7 +75,7 @@ struct Seg {
   int32_t rank, bucket;
 };
 
-// Bulk pipeline stage plan for one element range of kStageElems elements:
+// Bulk pipeline stage plan for one element range (2048 or 4096 elements):
 // stage i carries the replica chunks of ring positions [r_lo[i], r_hi[i])
 // and, when states[i] is set, the state block (kFused: master, m, v;
 // kUpdate: g, master, m, v) after them.
@@ -604,20 +604,21 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 // -------------------------------------------------- bulk-copy pipeline --
 //
 // kFused, kReduce and kUpdate stream their inputs through shared memory.
-// Work is cut into element ranges of E = 2048 elements (a 4096-element tile
-// holds two). The inputs of one range are chunks: one per replica (ring
-// order, 4 KB) and the state block (master, m, v; for kUpdate also g;
-// 8 KB each). The host packs the chunks of a range into at most 64 KB
-// stages (StagePlan): N = 8 fused is one 56 KB stage, N = 64 fused is four
-// stages of 16 replicas and one state stage. One producer warp posts each
-// stage's byte count on the slot's "full" mbarrier and its 32 lanes issue
-// the stage's cp.async.bulk copies in parallel; sixteen consumer warps wait on
+// Work is cut into element ranges of E = 512 * EPT elements (EPT = 8, one
+// 4096-element tile, when a range's whole input fits one 64 KB stage; else
+// EPT = 4). The inputs of one range are chunks: one per replica (ring order,
+// 2E bytes) and the state block (master, m, v; for kUpdate also g; 4E bytes
+// each). The host packs the chunks of a range into at most 64 KB stages
+// (StagePlan): N = 8 fused is one 56 KB stage, N = 64 fused is four stages
+// of 16 replicas and one state stage. One producer warp posts each stage's
+// byte count on the slot's "full" mbarrier and its 32 lanes issue the
+// stage's cp.async.bulk copies in parallel; sixteen consumer warps wait on
 // "full", accumulate the replicas of the stage in registers (thread t owns
-// elements [4t, 4t+4) of the range, held across the range's stages), finish
-// the step when the state block arrives, write results to global memory
-// with streaming stores and release the slot on its "empty" mbarrier. With
-// S slots, S - 1 stages (~100-170 KB per SM) are in flight while one is
-// computed, independent of the register budget.
+// elements [EPT*t, EPT*t+EPT) of the range, held across the range's
+// stages), finish the step when the state block arrives, write results to
+// global memory with streaming stores and release the slot on its "empty"
+// mbarrier. With S slots, S - 1 stages (~100-170 KB per SM) are in flight
+// while one is computed, independent of the register budget.
 // Tile heads/tails that are not 16-byte aligned are done by the consumers
 // with plain loads (do_scalar).
 // Every mbarrier wait is bounded by kWaitLimitNs of %globaltimer; on expiry
@@ -627,14 +628,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kBulkThreads = kConsumers + 32;
-constexpr int kStageElems = 2048;
-constexpr int kEPT = kStageElems / kConsumers;   // elements per consumer thread: 4
 constexpr int kMaxStages = 6;
 constexpr int kStageBudget = 64 * 1024;         // bytes per stage, upper bound
 constexpr int kSmemCap = 216 * 1024;            // dynamic shared memory per CTA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-static_assert(kTile % kStageElems == 0, "tile must hold whole ranges");
+static_assert(kTile % (kConsumers * 8) == 0, "tile must hold whole ranges");
 static_assert(kConsumerWarps <= kMaxWarps, "norm slots");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -717,54 +716,6 @@ struct TileGeom {
   int32_t rank, bucket, first_rep;
 };
 
-// Tile g of this launch: element range, owner, and the 16-byte aligned body
-// [va, vb) (empty when the owner's shard and the windows are misaligned).
-__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
-  const Seg& sg = a.segs[find_seg(a, g)];
-  TileGeom t;
-  t.lo = sg.lo + (g - sg.tile_local0) * kTile;
-  t.hi = min(t.lo + kTile, sg.hi);
-  t.rank = sg.rank;
-  t.bucket = sg.bucket;
-  t.partial = sg.tile_global0 + (g - sg.tile_local0);
-  t.first_rep = sg.rank + 1 == a.n_ranks ? 0 : sg.rank + 1;
-  const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
-  t.va = t.hi;
-  t.vb = t.hi;
-  if (((rank0 - a.wbase) & 3) == 0) {
-    t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
-    t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
-  }
-  return t;
-}
-
-__device__ __forceinline__ void lds_f4(const unsigned char* p, float (&x)[4]) {
-  float4 a = *reinterpret_cast<const float4*>(p);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-}
-
-template <bool kBf16>
-__device__ __forceinline__ void lds_h4(const unsigned char* p, float (&x)[4]) {
-  uint2 w = *reinterpret_cast<const uint2*>(p);
-  x[0] = widen<kBf16>(w.x & 0xFFFFu);
-  x[1] = widen<kBf16>(w.x >> 16);
-  x[2] = widen<kBf16>(w.y & 0xFFFFu);
-  x[3] = widen<kBf16>(w.y >> 16);
-}
-
-__device__ __forceinline__ void stg_f4(float* p, const float (&x)[4]) {
-  __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
-}
-
-template <bool kBf16>
-__device__ __forceinline__ void stg_h4(uint16_t* p, const float (&x)[4]) {
-  const uint32_t u0 = static_cast<uint32_t>(narrow<kBf16>(x[0])) |
-                      (static_cast<uint32_t>(narrow<kBf16>(x[1])) << 16);
-  const uint32_t u1 = static_cast<uint32_t>(narrow<kBf16>(x[2])) |
-                      (static_cast<uint32_t>(narrow<kBf16>(x[3])) << 16);
-  __stcs(reinterpret_cast<uint2*>(p), make_uint2(u0, u1));
-}
-
 // a0 += low half of w, a1 += high half of w, each 16-bit value widened
 // exactly to fp32 and the sum rounded once to nearest even: sm_100+'s
 // mixed-precision add (PTX add.rn.f32.f16 / add.rn.f32.bf16) does the
@@ -784,51 +735,130 @@ __device__ __forceinline__ void add_halves(float& a0, float& a1, uint32_t w) {
   }
 }
 
-// acc[e] += replica chunks 0..R-1 of this thread's 4 elements, in ring
-// order; all R shared-memory loads are issued before the adds.
-template <bool kBf16, int R>
-__device__ __forceinline__ void acc_reps(const unsigned char* rp, float (&acc)[kEPT]) {
-  uint2 w[R];
+// EPT consecutive 16-bit values (one 8- or 16-byte shared-memory load).
+template <int EPT>
+struct HalfVec;
+template <>
+struct HalfVec<4> {
+  uint2 v;
+  __device__ __forceinline__ void load(const unsigned char* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ uint32_t word(int i) const { return i == 0 ? v.x : v.y; }
+};
+template <>
+struct HalfVec<8> {
+  uint4 v;
+  __device__ __forceinline__ void load(const unsigned char* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ uint32_t word(int i) const {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+  }
+};
+
+// acc[e] += replica chunks 0..R-1 of this thread's EPT elements, in ring
+// order; all R shared-memory loads are issued before the adds. `stride` is
+// the chunk size in bytes.
+template <bool kBf16, int R, int EPT>
+__device__ __forceinline__ void acc_reps(const unsigned char* rp, int stride, float (&acc)[EPT]) {
+  HalfVec<EPT> w[R];
 #pragma unroll
-  for (int p = 0; p < R; ++p)
-    w[p] = *reinterpret_cast<const uint2*>(rp + static_cast<size_t>(p) * (2 * kStageElems));
+  for (int p = 0; p < R; ++p) w[p].load(rp + static_cast<size_t>(p) * stride);
 #pragma unroll
   for (int p = 0; p < R; ++p) {
-    add_halves<kBf16>(acc[0], acc[1], w[p].x);
-    add_halves<kBf16>(acc[2], acc[3], w[p].y);
+#pragma unroll
+    for (int i = 0; i < EPT / 2; ++i) add_halves<kBf16>(acc[2 * i], acc[2 * i + 1], w[p].word(i));
   }
 }
 
-template <bool kBf16>
-__device__ __forceinline__ void acc_stage(const unsigned char* rp, int n, float (&acc)[kEPT]) {
+template <bool kBf16, int EPT>
+__device__ __forceinline__ void acc_stage(const unsigned char* rp, int stride, int n,
+                                          float (&acc)[EPT]) {
   switch (n) {
-    case 1: acc_reps<kBf16, 1>(rp, acc); break;
-    case 2: acc_reps<kBf16, 2>(rp, acc); break;
-    case 3: acc_reps<kBf16, 3>(rp, acc); break;
-    case 4: acc_reps<kBf16, 4>(rp, acc); break;
-    case 5: acc_reps<kBf16, 5>(rp, acc); break;
-    case 6: acc_reps<kBf16, 6>(rp, acc); break;
-    case 7: acc_reps<kBf16, 7>(rp, acc); break;
-    case 8: acc_reps<kBf16, 8>(rp, acc); break;
-    case 9: acc_reps<kBf16, 9>(rp, acc); break;
-    case 10: acc_reps<kBf16, 10>(rp, acc); break;
-    case 11: acc_reps<kBf16, 11>(rp, acc); break;
-    case 12: acc_reps<kBf16, 12>(rp, acc); break;
-    case 13: acc_reps<kBf16, 13>(rp, acc); break;
-    case 14: acc_reps<kBf16, 14>(rp, acc); break;
-    case 15: acc_reps<kBf16, 15>(rp, acc); break;
-    case 16: acc_reps<kBf16, 16>(rp, acc); break;
+    case 1: acc_reps<kBf16, 1, EPT>(rp, stride, acc); break;
+    case 2: acc_reps<kBf16, 2, EPT>(rp, stride, acc); break;
+    case 3: acc_reps<kBf16, 3, EPT>(rp, stride, acc); break;
+    case 4: acc_reps<kBf16, 4, EPT>(rp, stride, acc); break;
+    case 5: acc_reps<kBf16, 5, EPT>(rp, stride, acc); break;
+    case 6: acc_reps<kBf16, 6, EPT>(rp, stride, acc); break;
+    case 7: acc_reps<kBf16, 7, EPT>(rp, stride, acc); break;
+    case 8: acc_reps<kBf16, 8, EPT>(rp, stride, acc); break;
+    case 9: acc_reps<kBf16, 9, EPT>(rp, stride, acc); break;
+    case 10: acc_reps<kBf16, 10, EPT>(rp, stride, acc); break;
+    case 11: acc_reps<kBf16, 11, EPT>(rp, stride, acc); break;
+    case 12: acc_reps<kBf16, 12, EPT>(rp, stride, acc); break;
+    case 13: acc_reps<kBf16, 13, EPT>(rp, stride, acc); break;
+    case 14: acc_reps<kBf16, 14, EPT>(rp, stride, acc); break;
+    case 15: acc_reps<kBf16, 15, EPT>(rp, stride, acc); break;
+    case 16: acc_reps<kBf16, 16, EPT>(rp, stride, acc); break;
     default:  // the stage plan never puts more than 16 replicas in a stage
       for (int p = 0; p < n; ++p)
-        acc_reps<kBf16, 1>(rp + static_cast<size_t>(p) * (2 * kStageElems), acc);
+        acc_reps<kBf16, 1, EPT>(rp + static_cast<size_t>(p) * stride, stride, acc);
   }
 }
 
-template <int MODE, bool kBf16>
+template <int EPT>
+__device__ __forceinline__ void lds_fv(const unsigned char* p, float (&x)[EPT]) {
+#pragma unroll
+  for (int i = 0; i < EPT / 4; ++i) {
+    const float4 a = reinterpret_cast<const float4*>(p)[i];
+    x[4 * i] = a.x;
+    x[4 * i + 1] = a.y;
+    x[4 * i + 2] = a.z;
+    x[4 * i + 3] = a.w;
+  }
+}
+
+template <int EPT>
+__device__ __forceinline__ void stg_fv(float* p, const float (&x)[EPT]) {
+#pragma unroll
+  for (int i = 0; i < EPT / 4; ++i)
+    __stcs(reinterpret_cast<float4*>(p) + i,
+           make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]));
+}
+
+template <bool kBf16, int EPT>
+__device__ __forceinline__ void stg_hv(uint16_t* p, const float (&x)[EPT]) {
+  uint32_t u[EPT / 2];
+#pragma unroll
+  for (int i = 0; i < EPT / 2; ++i)
+    u[i] = static_cast<uint32_t>(narrow<kBf16>(x[2 * i])) |
+           (static_cast<uint32_t>(narrow<kBf16>(x[2 * i + 1])) << 16);
+  if constexpr (EPT == 4) {
+    __stcs(reinterpret_cast<uint2*>(p), make_uint2(u[0], u[1]));
+  } else {
+    __stcs(reinterpret_cast<uint4*>(p), make_uint4(u[0], u[1], u[2], u[3]));
+  }
+}
+
+// Segment of tile g, searched forward from the previous tile's segment (a
+// CTA's tiles increase, so the index only moves forward).
+__device__ __forceinline__ const Seg& seg_of(const Args& a, int64_t g, int& hint) {
+  while (hint + 1 < a.n_segs && a.segs[hint + 1].tile_local0 <= g) ++hint;
+  return a.segs[hint];
+}
+
+__device__ __forceinline__ TileGeom tile_geom_hint(const Args& a, int64_t g, int& hint) {
+  const Seg& sg = seg_of(a, g, hint);
+  TileGeom t;
+  t.lo = sg.lo + (g - sg.tile_local0) * kTile;
+  t.hi = min(t.lo + kTile, sg.hi);
+  t.rank = sg.rank;
+  t.bucket = sg.bucket;
+  t.partial = sg.tile_global0 + (g - sg.tile_local0);
+  t.first_rep = sg.rank + 1 == a.n_ranks ? 0 : sg.rank + 1;
+  const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
+  t.va = t.hi;
+  t.vb = t.hi;
+  if (((rank0 - a.wbase) & 3) == 0) {
+    t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
+    t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
+  }
+  return t;
+}
+
+template <int MODE, bool kBf16, int EPT>
 __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
                                                                int n_slots,
                                                                uint32_t slot_bytes) {
-  constexpr int E = kStageElems;
+  constexpr int E = kConsumers * EPT;  // elements per range
   __shared__ StepScalars sh_s;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -852,6 +882,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   const int N = a.n_ranks;
   const int n_plan = a.plan.n;
   volatile int* abort_flag = &sh_abort;
+  int hint = 0;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -863,7 +894,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     uint32_t phase = 0;  // == (it / n_slots) & 1
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
-      const TileGeom t = tile_geom(a, g);
+      const TileGeom t = tile_geom_hint(a, g, hint);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
       for (int64_t j0 = t.va; j0 < t.vb && !stop; j0 += E) {
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
@@ -879,7 +910,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
               *abort_flag = 1;
               go = 0;
             } else {
-              mbar_expect_tx(&full_bar[slot], len * static_cast<uint32_t>(a.plan.bytes_per_elem[st]));
+              mbar_expect_tx(&full_bar[slot],
+                             len * static_cast<uint32_t>(a.plan.bytes_per_elem[st]));
             }
           }
           if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
@@ -933,16 +965,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 
   // -------------------------------------------------------------- consumers
   const int tid = threadIdx.x;
-  const int t_off = tid * kEPT;
+  const int t_off = tid * EPT;
   int slot = 0;
   uint32_t phase = 0;
   uint32_t tile_no = 0;
   bool dead = false;
   const bool partials = MODE == kReduce && (a.mode_flags & kFlagPartials);
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
-    const TileGeom t = tile_geom(a, g);
+    const TileGeom t = tile_geom_hint(a, g, hint);
     NormAcc nacc;
-    uint64_t phi = 0, plo = 0;  // packed in-range accumulators (elements 0,2 | 1,3)
+    uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
     // unaligned head [lo, va) and tail [vb, hi) with plain loads
     const int nhead = static_cast<int>(t.va - t.lo);
@@ -960,9 +992,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
       const int64_t k = j - rank0;
       // ring sum in fp32, starting from -0 (x + -0 == x for every x, so this
       // equals starting from the first replica's value)
-      float acc[kEPT], gv[kEPT];
+      float acc[EPT], gv[EPT];
 #pragma unroll
-      for (int e = 0; e < kEPT; ++e) acc[e] = -0.0f;
+      for (int e = 0; e < EPT; ++e) acc[e] = -0.0f;
       for (int st = 0; st < n_plan; ++st) {
         const int cur = slot;
         const uint32_t ph = phase;
@@ -989,36 +1021,36 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if constexpr (MODE == kFused || MODE == kReduce) {
           const bool completes = r_hi == N && r_lo < r_hi;  // stage ends the range's sum
           if (mine) {
-            acc_stage<kBf16>(buf + t_off * 2, r_hi - r_lo, acc);
+            acc_stage<kBf16, EPT>(buf + t_off * 2, 2 * E, r_hi - r_lo, acc);
             if (completes) {
-              {
-                const uint64_t inv2 = f2_pack(s.inv, s.inv);
-                f2_unpack(f2_mul(f2_pack(acc[0], acc[1]), inv2), gv[0], gv[1]);
-                f2_unpack(f2_mul(f2_pack(acc[2], acc[3]), inv2), gv[2], gv[3]);
-              }
+              const uint64_t inv2 = f2_pack(s.inv, s.inv);
+#pragma unroll
+              for (int i = 0; i < EPT / 2; ++i)
+                f2_unpack(f2_mul(f2_pack(acc[2 * i], acc[2 * i + 1]), inv2), gv[2 * i],
+                          gv[2 * i + 1]);
               if (!partials) {
 #pragma unroll
-                for (int e = 0; e < kEPT; ++e) bad |= nonfinite(gv[e]);
+                for (int e = 0; e < EPT; ++e) bad |= nonfinite(gv[e]);
               }
-              if constexpr (MODE == kReduce) stg_f4(a.ghat[t.rank] + k, gv);
+              if constexpr (MODE == kReduce) stg_fv<EPT>(a.ghat[t.rank] + k, gv);
             }
           }
           if (partials && completes) {
             // squares of this thread's elements: one warp-wide range check,
-            // then the straight-line fp32 path (non-finite values show up in
-            // the accumulators, checked once per tile)
-            float q[kEPT];
+            // then the straight-line paired-fp32 path (non-finite values
+            // show up in the accumulators, checked once per tile)
+            float q[EPT];
 #pragma unroll
-            for (int e = 0; e < kEPT; ++e) q[e] = mine ? gv[e] : 0.0f;
+            for (int e = 0; e < EPT; ++e) q[e] = mine ? gv[e] : 0.0f;
             bool in_range = true;
 #pragma unroll
-            for (int e = 0; e < kEPT; ++e) in_range &= fabsf(q[e]) < kNormMainLimit;
+            for (int e = 0; e < EPT; ++e) in_range &= fabsf(q[e]) < kNormMainLimit;
             if (__all_sync(0xFFFFFFFFu, in_range)) {
-              ff2_add_sq(phi, plo, f2_pack(q[0], q[1]));
-              ff2_add_sq(phi, plo, f2_pack(q[2], q[3]));
+#pragma unroll
+              for (int i = 0; i < EPT / 2; ++i) ff2_add_sq(phi, plo, f2_pack(q[2 * i], q[2 * i + 1]));
             } else {
 #pragma unroll
-              for (int e = 0; e < kEPT; ++e) nacc.add(q[e]);
+              for (int e = 0; e < EPT; ++e) nacc.add(q[e]);
             }
           }
         }
@@ -1027,23 +1059,23 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             if (a.plan.states[st]) {
               const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (2 * E);
               if constexpr (MODE == kUpdate) {
-                lds_f4(sb + t_off * 4, gv);
+                lds_fv<EPT>(sb + t_off * 4, gv);
                 sb += 4 * E;
                 if (s.clip != 1.0f) {
 #pragma unroll
-                  for (int e = 0; e < kEPT; ++e) gv[e] = __fmul_rn(gv[e], s.clip);
+                  for (int e = 0; e < EPT; ++e) gv[e] = __fmul_rn(gv[e], s.clip);
                 }
               }
-              float th[kEPT], m[kEPT], v[kEPT];
-              lds_f4(sb + t_off * 4, th);
-              lds_f4(sb + 4 * E + t_off * 4, m);
-              lds_f4(sb + 8 * E + t_off * 4, v);
+              float th[EPT], m[EPT], v[EPT];
+              lds_fv<EPT>(sb + t_off * 4, th);
+              lds_fv<EPT>(sb + 4 * E + t_off * 4, m);
+              lds_fv<EPT>(sb + 8 * E + t_off * 4, v);
 #pragma unroll
-              for (int e = 0; e < kEPT; ++e) adamw(th[e], m[e], v[e], gv[e], a, s);
-              stg_f4(a.master[s.dst][t.rank] + k, th);
-              stg_f4(a.mom[s.dst][t.rank] + k, m);
-              stg_f4(a.var[s.dst][t.rank] + k, v);
-              stg_h4<kBf16>(a.flat + w, th);
+              for (int e = 0; e < EPT; ++e) adamw(th[e], m[e], v[e], gv[e], a, s);
+              stg_fv<EPT>(a.master[s.dst][t.rank] + k, th);
+              stg_fv<EPT>(a.mom[s.dst][t.rank] + k, m);
+              stg_fv<EPT>(a.var[s.dst][t.rank] + k, v);
+              stg_hv<kBf16, EPT>(a.flat + w, th);
             }
           }
         }
@@ -1143,13 +1175,14 @@ int grid_size() {
   return sms * std::max(per_sm, 1);
 }
 
-// Greedy packing of one element range's chunks into stages of at most
-// kStageBudget bytes: replica chunks (2 bytes per element each) in ring
-// order, then the indivisible state block (kFused 12, kUpdate 16 bytes per
-// element) in the last stage if it fits, else in a stage of its own.
-inline StagePlan make_stage_plan(int mode, int n_ranks, uint32_t* slot_bytes) {
+// Greedy packing of one element range's chunks (range of E elements) into
+// stages of at most kStageBudget bytes: replica chunks (2 bytes per element
+// each) in ring order, then the indivisible state block (kFused 12, kUpdate
+// 16 bytes per element) in the last stage if it fits, else in a stage of
+// its own.
+inline StagePlan make_stage_plan(int mode, int n_ranks, int E, uint32_t* slot_bytes) {
   StagePlan pl{};
-  const int budget = kStageBudget / kStageElems;  // bytes per element
+  const int budget = kStageBudget / E;  // bytes per element
   const int n_rep = mode == kUpdate ? 0 : n_ranks;
   const int state_bpe = mode == kFused ? 12 : (mode == kUpdate ? 16 : 0);
   int lo = 0, cur = 0;
@@ -1179,19 +1212,20 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, uint32_t* slot_bytes) {
   } else if (cur > 0) {
     close(n_rep, 0);
   }
-  *slot_bytes = static_cast<uint32_t>((max_bpe * kStageElems + 127) & ~127);
+  *slot_bytes = static_cast<uint32_t>((max_bpe * E + 127) & ~127);
   return pl;
 }
 
-template <int MODE, bool kBf16>
-int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+template <int MODE, bool kBf16, int EPT>
+int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
+  constexpr int E = kConsumers * EPT;
   uint32_t slot_bytes = 0;
-  a.plan = make_stage_plan(MODE, a.n_ranks, &slot_bytes);
+  a.plan = make_stage_plan(MODE, a.n_ranks, E, &slot_bytes);
   if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
   const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));
   if (slots < 2) return ZERO_ERANGE;
   const size_t smem = static_cast<size_t>(slots) * slot_bytes;
-  auto kern = bulk_kernel<MODE, kBf16>;
+  auto kern = bulk_kernel<MODE, kBf16, EPT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return ZERO_ECUDA;
@@ -1206,6 +1240,15 @@ int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
   const int grid = static_cast<int>(std::min<int64_t>(tiles, cap));
   kern<<<grid, kBulkThreads, smem, stream>>>(a, slots, slot_bytes);
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+// 8 elements per consumer thread (4096-element ranges, one tile) when one
+// range's whole input fits one stage; otherwise 4 (2048-element ranges).
+template <int MODE, bool kBf16>
+int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+  const int bpe = MODE == kFused ? 2 * a.n_ranks + 12 : (MODE == kReduce ? 2 * a.n_ranks : 16);
+  if (bpe * kConsumers * 8 <= kStageBudget) return launch_bulk_ept<MODE, kBf16, 8>(a, tiles, stream);
+  return launch_bulk_ept<MODE, kBf16, 4>(a, tiles, stream);
 }
 
 template <int MODE, bool kBf16>
