@@ -159,7 +159,8 @@ ZERO_API int zero_plan_bucket_range(const zero_plan* plan, int32_t bucket, int64
 
 ZERO_API size_t zero_workspace_bytes(const zero_plan* plan) {
   if (!plan) return 0;
-  size_t b = static_cast<size_t>(plan->info.n_tiles) * sizeof(double);
+  // one 16-byte norm record per tile, then 256 records for the finish kernels
+  size_t b = (static_cast<size_t>(plan->info.n_tiles) + 256) * 16;
   return (b + 255) & ~static_cast<size_t>(255);
 }
 

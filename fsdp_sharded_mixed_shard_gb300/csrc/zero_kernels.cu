@@ -15,8 +15,8 @@
  *     kNorm   per-tile squared-norm partials from fp32 g (4 bytes per element);
  *     kCast   16-bit working copy from an fp32 master set (6 bytes per element),
  *             optionally only when the step's overflow word is set.
- *   norm_finish_kernel        fixed-order fp64 sum of the tile partials, norm,
- *                             clip coefficient (one CTA).
+ *   norm_blocks_kernel,       fixed-partition float-float merge of the tile
+ *   norm_final_kernel         records; fp64 norm and clip coefficient.
  *   scaler_finish_kernel      loss-scale / skip / step-count bookkeeping (one
  *                             thread).
  *
@@ -56,7 +56,6 @@ constexpr int kTile = ZERO_TILE_ELEMS;
 constexpr int kVec = 8;                       // 16-bit elements per 16-byte vector
 constexpr int kMaxSegs = 128;                 // segments per launch (kernel parameter space)
 constexpr int kChunk = 8;                     // replicas loaded together
-constexpr int kNormThreads = 1024;
 
 static_assert(kTile % (kVec * kThreads) == 0, "tile must be a whole number of vector passes");
 
@@ -96,7 +95,7 @@ struct Args {
   uint16_t* flat;                           // parameter window
   zero_scaler* scaler;
   uint32_t* flags;
-  double* partials;
+  float4* partials;  // norm records: one (hi, lo, bhi, blo) per tile
   int64_t wbase, shard, n_tiles;
   int32_t n_ranks, n_segs, n_sets, mode_flags;
   // step constants rounded once from the fp64 hyperparameters
@@ -317,21 +316,27 @@ __device__ __forceinline__ void tile_norm_publish(NormAcc acc, NormSlots& sl, in
   }
 }
 
-// After the barrier: warps' sums merged in warp order in float-float, then a
-// handful of fp64 operations for the tile's total.
-__device__ __forceinline__ double tile_norm_total(const NormSlots& sl, int par, int n_warps) {
+// After the barrier, run by all 32 lanes of one warp: lane l < n_warps
+// takes warp l's sums, a fixed shuffle tree merges them (float-float, no
+// fp64), lane 0 returns the tile's record (hi, lo, bhi, blo).
+__device__ __forceinline__ float4 tile_norm_record(const NormSlots& sl, int par, int n_warps,
+                                                   int lane) {
   NormAcc t;
-  t.hi = sl.hi[par][0];
-  t.lo = sl.lo[par][0];
-  t.bhi = sl.bhi[par][0];
-  t.blo = sl.blo[par][0];
-  for (int w = 1; w < n_warps; ++w) t.merge(sl.hi[par][w], sl.lo[par][w], sl.bhi[par][w], sl.blo[par][w]);
-  double total = __dadd_rn(static_cast<double>(t.hi), static_cast<double>(t.lo));
-  if (t.bhi != 0.f || t.blo != 0.f)
-    total = __dadd_rn(total, __dmul_rn(__dadd_rn(static_cast<double>(t.bhi),
-                                                 static_cast<double>(t.blo)),
-                                       0x1p192));
-  return total;
+  if (lane < n_warps) {
+    t.hi = sl.hi[par][lane];
+    t.lo = sl.lo[par][lane];
+    t.bhi = sl.bhi[par][lane];
+    t.blo = sl.blo[par][lane];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float h2 = __shfl_down_sync(0xFFFFFFFFu, t.hi, off);
+    float l2 = __shfl_down_sync(0xFFFFFFFFu, t.lo, off);
+    float bh2 = __shfl_down_sync(0xFFFFFFFFu, t.bhi, off);
+    float bl2 = __shfl_down_sync(0xFFFFFFFFu, t.blo, off);
+    if (lane < off) t.merge(h2, l2, bh2, bl2);
+  }
+  return make_float4(t.hi, t.lo, t.bhi, t.blo);
 }
 
 __device__ __forceinline__ void raise_flag(const Args& a, int32_t bucket) {
@@ -593,9 +598,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
         const int par = tile_no & 1;
         tile_norm_publish(nacc, sh_norm, par, warp, lane);
         __syncthreads();
-        if (warp == static_cast<int>(tile_no % kWarps) && lane == 0)
-          a.partials[sg.tile_global0 + (g - sg.tile_local0)] =
-              tile_norm_total(sh_norm, par, kWarps);
+        if (warp == static_cast<int>(tile_no % kWarps)) {
+          const float4 rec = tile_norm_record(sh_norm, par, kWarps, lane);
+          if (lane == 0) a.partials[sg.tile_global0 + (g - sg.tile_local0)] = rec;
+        }
       }
     }
   }
@@ -1099,30 +1105,94 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         const int par = tile_no & 1;
         tile_norm_publish(nacc, sh_norm, par, warp, lane);
         consumer_sync();
-        if (warp == static_cast<int>(tile_no % kConsumerWarps) && lane == 0)
-          a.partials[t.partial] = tile_norm_total(sh_norm, par, kConsumerWarps);
+        if (warp == static_cast<int>(tile_no % kConsumerWarps)) {
+          const float4 rec = tile_norm_record(sh_norm, par, kConsumerWarps, lane);
+          if (lane == 0) a.partials[t.partial] = rec;
+        }
       }
     }
   }
 }
 
-// Fixed-order fp64 sum of tile partials [t0, t1), then norm and clip
-// coefficient. One CTA of kNormThreads threads: thread k sums partials
-// t0+k, t0+k+kNormThreads, ... in order; then a fixed shared-memory tree.
-__global__ void __launch_bounds__(kNormThreads) norm_finish_kernel(
-    const double* __restrict__ partials, int64_t t0, int64_t t1, double max_norm,
-    zero_scaler* sc) {
-  __shared__ double sh[kNormThreads];
-  double sum = 0.0;
-  for (int64_t t = t0 + threadIdx.x; t < t1; t += kNormThreads) sum = __dadd_rn(sum, partials[t]);
-  sh[threadIdx.x] = sum;
-  __syncthreads();
-  for (int w = kNormThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) sh[threadIdx.x] = __dadd_rn(sh[threadIdx.x], sh[threadIdx.x + w]);
-    __syncthreads();
+// Norm finish, two small kernels with a fixed partition (independent of the
+// GPU), so the result is deterministic:
+//   norm_blocks_kernel: kFinishBlocks CTAs; CTA b merges the tile records of
+//     its contiguous share of [t0, t1) (thread k takes every
+//     kFinishThreads-th record, then fixed shuffle and shared-memory trees)
+//     into one record, in fp32 float-float;
+//   norm_final_kernel: one CTA merges the kFinishBlocks records the same way,
+//     forms norm^2 = hi + lo + 2^192 (bhi + blo) in fp64, the norm and the
+//     clip coefficient c = max_norm / (norm + 1e-6) (fp64; applied, rounded
+//     to fp32, only when c < 1).
+constexpr int kFinishBlocks = 256;
+constexpr int kFinishThreads = 256;
+
+// Merge the kFinishThreads per-thread accumulators of a CTA; result in
+// thread 0.
+__device__ NormAcc cta_merge(NormAcc t, float4* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float h2 = __shfl_down_sync(0xFFFFFFFFu, t.hi, off);
+    float l2 = __shfl_down_sync(0xFFFFFFFFu, t.lo, off);
+    float bh2 = __shfl_down_sync(0xFFFFFFFFu, t.bhi, off);
+    float bl2 = __shfl_down_sync(0xFFFFFFFFu, t.blo, off);
+    if (lane < off) t.merge(h2, l2, bh2, bl2);
   }
+  if (lane == 0) sh[warp] = make_float4(t.hi, t.lo, t.bhi, t.blo);
+  __syncthreads();
+  NormAcc r;
+  if (warp == 0) {
+    if (lane < kFinishThreads / 32) {
+      const float4 q = sh[lane];
+      r.hi = q.x;
+      r.lo = q.y;
+      r.bhi = q.z;
+      r.blo = q.w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float h2 = __shfl_down_sync(0xFFFFFFFFu, r.hi, off);
+      float l2 = __shfl_down_sync(0xFFFFFFFFu, r.lo, off);
+      float bh2 = __shfl_down_sync(0xFFFFFFFFu, r.bhi, off);
+      float bl2 = __shfl_down_sync(0xFFFFFFFFu, r.blo, off);
+      if (lane < off) r.merge(h2, l2, bh2, bl2);
+    }
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kFinishThreads) norm_blocks_kernel(
+    const float4* __restrict__ records, int64_t t0, int64_t t1, float4* __restrict__ out) {
+  __shared__ float4 sh[kFinishThreads / 32];
+  const int64_t n = t1 - t0;
+  const int64_t chunk = (n + kFinishBlocks - 1) / kFinishBlocks;
+  const int64_t b0 = t0 + blockIdx.x * chunk;
+  const int64_t b1 = min(b0 + chunk, t1);
+  NormAcc t;
+  for (int64_t i = b0 + threadIdx.x; i < b1; i += kFinishThreads) {
+    const float4 q = records[i];
+    t.merge(q.x, q.y, q.z, q.w);
+  }
+  const NormAcc r = cta_merge(t, sh);
+  if (threadIdx.x == 0) out[blockIdx.x] = make_float4(r.hi, r.lo, r.bhi, r.blo);
+}
+
+__global__ void __launch_bounds__(kFinishThreads) norm_final_kernel(
+    const float4* __restrict__ blocks, double max_norm, zero_scaler* sc) {
+  __shared__ float4 sh[kFinishThreads / 32];
+  NormAcc t;
+  for (int i = threadIdx.x; i < kFinishBlocks; i += kFinishThreads) {
+    const float4 q = blocks[i];
+    t.merge(q.x, q.y, q.z, q.w);
+  }
+  const NormAcc r = cta_merge(t, sh);
   if (threadIdx.x == 0) {
-    const double nsq = sh[0];
+    double nsq = __dadd_rn(static_cast<double>(r.hi), static_cast<double>(r.lo));
+    if (r.bhi != 0.f || r.blo != 0.f)
+      nsq = __dadd_rn(nsq, __dmul_rn(__dadd_rn(static_cast<double>(r.bhi),
+                                               static_cast<double>(r.blo)),
+                                     0x1p192));
     const double nrm = __dsqrt_rn(nsq);
     const double c = __ddiv_rn(max_norm, __dadd_rn(nrm, 1e-6));
     sc->norm_sq = nsq;
@@ -1131,6 +1201,13 @@ __global__ void __launch_bounds__(kNormThreads) norm_finish_kernel(
     sc->clip_coef = c < 1.0 ? __double2float_rn(c) : 1.0f;
     sc->norm_step = sc->t + 1;
   }
+}
+
+int launch_norm_finish(const float4* records, int64_t t0, int64_t t1, float4* blocks,
+                       double max_norm, zero_scaler* sc, cudaStream_t st) {
+  norm_blocks_kernel<<<kFinishBlocks, kFinishThreads, 0, st>>>(records, t0, t1, blocks);
+  norm_final_kernel<<<1, kFinishThreads, 0, st>>>(blocks, max_norm, sc);
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
 // Loss scale, skip and step-count bookkeeping at the end of a step
@@ -1242,12 +1319,15 @@ int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
-// 8 elements per consumer thread (4096-element ranges, one tile) when one
-// range's whole input fits one stage; otherwise 4 (2048-element ranges).
+// The reduce pass moves few bytes per element at small N, so its fixed
+// per-range costs are amortised over 4096-element ranges (8 elements per
+// consumer thread, one tile) whenever a range's replicas fit one stage
+// (N <= 8); the update and fused passes measured faster with 2048-element
+// ranges and more, smaller slots.
 template <int MODE, bool kBf16>
 int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
-  const int bpe = MODE == kFused ? 2 * a.n_ranks + 12 : (MODE == kReduce ? 2 * a.n_ranks : 16);
-  if (bpe * kConsumers * 8 <= kStageBudget) return launch_bulk_ept<MODE, kBf16, 8>(a, tiles, stream);
+  if (MODE == kReduce && 2 * a.n_ranks * kConsumers * 8 <= kStageBudget)
+    return launch_bulk_ept<MODE, kBf16, 8>(a, tiles, stream);
   return launch_bulk_ept<MODE, kBf16, 4>(a, tiles, stream);
 }
 
@@ -1255,7 +1335,8 @@ template <int MODE, bool kBf16>
 int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
                 cudaStream_t stream) {
   constexpr bool kBulk = MODE == kFused || MODE == kReduce || MODE == kUpdate;
-  int grid_cap = kBulk ? 1 : grid_size<MODE, kBf16>();
+  int grid_cap = 1;
+  if constexpr (!kBulk) grid_cap = grid_size<MODE, kBf16>();
   if (grid_cap <= 0) return ZERO_ECUDA;
   for (int32_t s0 = seg_begin; s0 < seg_end; s0 += kMaxSegs) {
     const int32_t s1 = std::min(seg_end, s0 + kMaxSegs);
@@ -1387,7 +1468,7 @@ ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t 
     a->wbase = window_base;
     a->scaler = d_scaler;
     a->flags = d_bucket_flags;
-    a->partials = static_cast<double*>(d_workspace);
+    a->partials = static_cast<float4*>(d_workspace);
     a->mode_flags = d_workspace ? kFlagPartials : 0;
     std::vector<std::pair<int32_t, int32_t>> runs;
     seg_range(plan, bucket, rank_lo, rank_hi, runs);
@@ -1417,16 +1498,16 @@ ZERO_API int zero_grad_norm(const zero_plan* plan, int32_t rank_lo, int32_t rank
     if (!a) return ZERO_ENOMEM;
     for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = const_cast<float*>(grad_shards[i]);
     a->scaler = d_scaler;
-    a->partials = static_cast<double*>(d_workspace);
+    a->partials = static_cast<float4*>(d_workspace);
     rc = launch<kNorm>(plan, *a, s0, s1, st);
     delete a;
     if (rc) return rc;
   }
   const int64_t t0 = s0 < s1 ? plan->seg_tile0[s0] : 0;
   const int64_t t1 = s0 < s1 ? plan->seg_tile0[s1 - 1] + plan->seg_tiles[s1 - 1] : 0;
-  norm_finish_kernel<<<1, kNormThreads, 0, st>>>(static_cast<const double*>(d_workspace), t0, t1,
-                                                 hp->max_grad_norm, d_scaler);
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  float4* records = static_cast<float4*>(d_workspace);
+  return launch_norm_finish(records, t0, t1, records + plan->info.n_tiles, hp->max_grad_norm,
+                            d_scaler, st);
 }
 
 namespace {
@@ -1588,21 +1669,22 @@ namespace zk {
 
 constexpr int64_t kNoallocTiles = ZERO_NOALLOC_MAX_TILES;
 
-// One fp64 partial per norm tile, 4 MiB. Every GPU that loads this library
-// holds this array until the process exits. All calls share it, and each call
-// overwrites the partials of exactly the tiles it later sums, so nothing has
-// to be cleared between calls. Calls that overlap on the GPU (different
-// streams, or different host threads without ordering) race on it.
-static __device__ __align__(256) double g_noalloc_partials[kNoallocTiles];
+// One 16-byte norm record per tile plus the finish kernels' per-block
+// records, 8 MiB + 4 KiB. Every GPU that loads this library holds this array
+// until the process exits. All calls share it, and each call overwrites the
+// records of exactly the tiles and blocks it later reads, so nothing has to
+// be cleared between calls. Calls that overlap on the GPU (different streams,
+// or different host threads without ordering) race on it.
+static __device__ __align__(256) float4 g_noalloc_partials[kNoallocTiles + kFinishBlocks];
 
 // Device address of g_noalloc_partials per device ordinal, resolved once per
 // device with that device current. In host code the array's name only stands
 // for the symbol; it is never a device address.
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-double* g_noalloc_ptr[kNoallocMaxDevices] = {};
+float4* g_noalloc_ptr[kNoallocMaxDevices] = {};
 
-int noalloc_scratch(double** out) {
+int noalloc_scratch(float4** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
   if (dev < 0 || dev >= kNoallocMaxDevices) return ZERO_ERANGE;
@@ -1610,7 +1692,7 @@ int noalloc_scratch(double** out) {
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return ZERO_ECUDA;
-    g_noalloc_ptr[dev] = static_cast<double*>(p);
+    g_noalloc_ptr[dev] = static_cast<float4*>(p);
   }
   *out = g_noalloc_ptr[dev];
   return ZERO_OK;
@@ -1632,7 +1714,7 @@ extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t ra
   const int64_t t0 = s0 < s1 ? plan->seg_tile0[s0] : 0;
   const int64_t t1 = s0 < s1 ? plan->seg_tile0[s1 - 1] + plan->seg_tiles[s1 - 1] : 0;
   if (t1 - t0 > kNoallocTiles) return ZERO_ERANGE;
-  double* scratch = nullptr;
+  float4* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch))) return rc;
 
   Args* a = new_args(plan);
@@ -1667,7 +1749,6 @@ extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t ra
   }
   delete a;
   if (rc) return rc;
-  norm_finish_kernel<<<1, kNormThreads, 0, st>>>(scratch, 0, t1 - t0, hp->max_grad_norm,
-                                                 d_scaler);
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  return launch_norm_finish(scratch, 0, t1 - t0, scratch + kNoallocTiles, hp->max_grad_norm,
+                            d_scaler, st);
 }

@@ -158,7 +158,7 @@ ZERO_API int zero_plan_segments(const zero_plan* plan, zero_segment* out, int32_
 ZERO_API int zero_plan_bucket_range(const zero_plan* plan, int32_t bucket, int64_t* lo,
                                     int64_t* hi);
 /* Device workspace bytes zero_reduce_scatter / zero_grad_norm need for the
- * norm partial sums (one double per tile). */
+ * norm partial sums: one 16-byte record per tile plus 256 records. */
 ZERO_API size_t zero_workspace_bytes(const zero_plan* plan);
 
 /* ---------------------------------------------------- hyperparameters -- */
@@ -241,9 +241,10 @@ ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t 
 
 /* Global gradient norm and clip coefficient (two-pass path, step 2).
  * Convention (the pages give none): L2 norm of the unscaled, averaged
- * gradient over the processed owners' elements; squares accumulated with at
- * least fp64 accuracy in a fixed order (per tile, then tiles in ascending
- * order), so the result is deterministic and independent of the grid;
+ * gradient over the processed owners' elements; squares accumulated in fp32
+ * float-float pairs (exact products, two-sum additions; relative error well
+ * below 2^-30) in a fixed order (per tile, then a fixed partition of the
+ * tiles), so the result is deterministic and independent of the grid;
  * c = max_norm / (norm + 1e-6) in fp64, applied (rounded to fp32) by the next
  * zero_step only if c < 1.
  * grad_shards == NULL: use the partials zero_reduce_scatter left in
@@ -315,7 +316,7 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
 
 /* Maximum number of norm tiles (ZERO_TILE_ELEMS elements each, counted per
  * segment) that one zero_grad_norm_noalloc call may cover: 2^19 tiles, about
- * 2.1e9 elements, 4 MiB of device memory. */
+ * 2.1e9 elements, 8 MiB of device memory. */
 #define ZERO_NOALLOC_MAX_TILES (1 << 19)
 
 /* zero_grad_norm_noalloc -- the global norm and clip coefficient of
@@ -326,8 +327,8 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
  * are not allowed to call cudaMalloc themselves, and callers with a fixed
  * memory budget that cannot grow by a workspace sized from the model.
  * It allocates nothing: the per-tile partials live in one fixed device
- * array of ZERO_NOALLOC_MAX_TILES doubles inside the library, which every GPU
- * that loads the library holds until the process exits.
+ * array of ZERO_NOALLOC_MAX_TILES 16-byte records (8 MiB) inside the library,
+ * which every GPU that loads the library holds until the process exits.
  *   grad_shards: as for zero_grad_norm, required (not NULL).
  *   Result: norm_sq, norm, clip_coef, clip_apply and norm_step in d_scaler,
  *   equal to what zero_grad_norm computes from the same gradients.

@@ -57,10 +57,12 @@ def assert_state(got, want, what):
 
 
 def norm_tol(n_elems):
-    # both sides sum squares in fp64 in different fixed orders: each within
-    # (n-1) u of the exact sum (u = 2^-53), the device's float-float tile
-    # sums within 2^-43
-    return (2.0 * n_elems * 2.0 ** -53 + 2.0 ** -43)
+    # relative tolerance on norm^2: the checker's fp64 sum is within
+    # (n-1) * 2^-53 of the exact sum; the device accumulates exact fp32
+    # products in float-float pairs along summation paths of a few thousand
+    # additions (within 2^-30 of the exact sum, worst case); plus the fp32
+    # subnormal floor handled by the caller's absolute term
+    return 2.0 * n_elems * 2.0 ** -53 + 2.0 ** -30
 
 
 def compare_scaler(dev, orc, n_elems, clip):
