@@ -834,15 +834,12 @@ __device__ __forceinline__ void stg_hv(uint16_t* p, const float (&x)[EPT]) {
   }
 }
 
-// Segment of tile g, searched forward from the previous tile's segment (a
-// CTA's tiles increase, so the index only moves forward).
-__device__ __forceinline__ const Seg& seg_of(const Args& a, int64_t g, int& hint) {
-  while (hint + 1 < a.n_segs && a.segs[hint + 1].tile_local0 <= g) ++hint;
-  return a.segs[hint];
-}
-
-__device__ __forceinline__ TileGeom tile_geom_hint(const Args& a, int64_t g, int& hint) {
-  const Seg& sg = seg_of(a, g, hint);
+// Tile g of this launch: element range, owner, and the 16-byte aligned body
+// [va, vb) (empty when the owner's shard and the windows are misaligned).
+// (A forward scan from the previous tile's segment measured slower than this
+// binary search.)
+__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
+  const Seg& sg = a.segs[find_seg(a, g)];
   TileGeom t;
   t.lo = sg.lo + (g - sg.tile_local0) * kTile;
   t.hi = min(t.lo + kTile, sg.hi);
@@ -888,7 +885,6 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   const int N = a.n_ranks;
   const int n_plan = a.plan.n;
   volatile int* abort_flag = &sh_abort;
-  int hint = 0;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -900,7 +896,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     uint32_t phase = 0;  // == (it / n_slots) & 1
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
-      const TileGeom t = tile_geom_hint(a, g, hint);
+      const TileGeom t = tile_geom(a, g);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
       for (int64_t j0 = t.va; j0 < t.vb && !stop; j0 += E) {
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
@@ -978,7 +974,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   bool dead = false;
   const bool partials = MODE == kReduce && (a.mode_flags & kFlagPartials);
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
-    const TileGeom t = tile_geom_hint(a, g, hint);
+    const TileGeom t = tile_geom(a, g);
     NormAcc nacc;
     uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
