@@ -230,7 +230,9 @@ def run_libzero(args, rank, world, dist):
     if segs is None:
         segs = sum(1 for s in Z.zero_plan_segments(g.plan) if lo <= s[2] < hi)
     L = -(-segs // 128)
-    launches_per_step = (2 * L + 1) if not g.two_pass else (L + (1 if clip else 0) + L + 1)
+    # fused: update + (re-cast check merged with bookkeeping); two-pass:
+    # reduce + norm finish (2) + update + bookkeeping
+    launches_per_step = (2 * L) if not g.two_pass else (L + (2 if clip else 0) + L + 1)
 
     for _ in range(args.warmup):
         for _, f in ph:
@@ -287,8 +289,8 @@ def run_libzero(args, rank, world, dist):
     dom = max((n for n, _ in ph if bytes_per_param[n] > 0), key=lambda n: phase_ms[n])
     alg_bytes = bytes_per_param[dom] * pstep
     achieved = alg_bytes / (phase_ms[dom] / 1e3) / 1e9
-    kernel_name = {"fused_update": "step_kernel<kFused>", "reduce_scatter": "step_kernel<kReduce>",
-                   "update": "step_kernel<kUpdate>"}[dom]
+    kernel_name = {"fused_update": "bulk_kernel<kFused>", "reduce_scatter": "bulk_kernel<kReduce>",
+                   "update": "bulk_kernel<kUpdate>"}[dom]
     traffic = profiled_traffic(kernel_name, wl.name)
     step_bytes = (2 * N + (34 if g.two_pass else 26)) * pstep
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),

@@ -18,7 +18,7 @@ __all__ = [
     "zero_plan_create", "zero_plan_destroy", "zero_plan_get_info", "zero_plan_tensor_offsets",
     "zero_plan_segments", "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
     "zero_reduce_scatter", "zero_grad_norm", "zero_step", "zero_step_update", "zero_step_finish",
-    "zero_cast_params", "zero_grad_norm_noalloc", "zero_strerror",
+    "zero_cast_params", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
     "zero_version", "lib",
 ]
 
@@ -64,7 +64,7 @@ class ZeroScaler(C.Structure):
                 ("beta1_pow", C.c_double), ("beta2_pow", C.c_double), ("norm_sq", C.c_double),
                 ("norm", C.c_double), ("clip_coef", C.c_float), ("clip_apply", C.c_int32),
                 ("norm_step", C.c_int32), ("n_skipped", C.c_int32), ("error", C.c_int32),
-                ("reserved", C.c_int32)]
+                ("finish_count", C.c_uint32)]
 
 
 _lib = None
@@ -103,6 +103,7 @@ def lib():
         L.zero_cast_params.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _VP, C.c_int64, _VP]
         L.zero_grad_norm_noalloc.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP),
                                              _P(ZeroHParams), _VP, _VP]
+        L.zero_selftest_wait_timeout.argtypes = [_VP, C.c_int64, _VP]
         L.zero_strerror.argtypes = [C.c_int]
         L.zero_strerror.restype = C.c_char_p
         L.zero_version.argtypes = []
@@ -226,6 +227,11 @@ def zero_grad_norm_noalloc(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, st
     device memory (see include/zero.h)."""
     _check("zero_grad_norm_noalloc", lib().zero_grad_norm_noalloc(
         plan, rank_lo, rank_hi, _ptrs(grad_shards), C.byref(hp), _vp(d_scaler), _vp(stream)))
+
+
+def zero_selftest_wait_timeout(d_scaler, limit_ns, stream=0):
+    _check("zero_selftest_wait_timeout", lib().zero_selftest_wait_timeout(
+        _vp(d_scaler), int(limit_ns), _vp(stream)))
 
 
 def zero_strerror(status):

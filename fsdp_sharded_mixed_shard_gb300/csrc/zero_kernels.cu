@@ -66,6 +66,7 @@ constexpr int kFlagClip = 1;        // kUpdate: apply the clip coefficient from 
 constexpr int kFlagIfPending = 2;   // kCast: only when the overflow word is set
 constexpr int kFlagUseScalerSet = 4;// kCast: master set = scaler->state_index
 constexpr int kFlagPartials = 8;    // kReduce: write norm partials
+constexpr int kFlagFinish = 16;     // kCast: also do the step's bookkeeping (once, last CTA)
 
 struct Seg {
   int64_t lo, hi;          // flat element range
@@ -100,7 +101,7 @@ struct Args {
   int32_t n_ranks, n_segs, n_sets, mode_flags;
   // step constants rounded once from the fp64 hyperparameters
   float b1, omb1, b2, omb2, lr, decay, eps;
-  int32_t pad0;
+  int32_t bk_dynamic, bk_growth, bk_flip;  // bookkeeping (kFlagFinish)
   double beta1, beta2;
   StagePlan plan;  // bulk pipeline: stages of one element range
   Seg segs[kMaxSegs];
@@ -358,6 +359,34 @@ __device__ __forceinline__ int find_seg(const Args& a, int64_t g) {
   return lo;
 }
 
+// Loss scale, skip and step-count bookkeeping at the end of a step
+// ("Training models too big for one GPU: ZeRO & FSDP", "Mixed-precision
+// training": pick the scale dynamically and skip a step on overflow).
+__device__ void step_bookkeeping(zero_scaler* sc, double beta1, double beta2, int dynamic,
+                                 int growth_interval, int flip_sets) {
+  const uint32_t ov = sc->pending;
+  sc->pending = 0;
+  sc->overflow = ov ? 1u : 0u;
+  if (ov) {
+    if (dynamic) {
+      const float half = __fmul_rn(sc->scale, 0.5f);
+      sc->scale = half < 1.0f ? 1.0f : half;
+    }
+    sc->good_steps = 0;
+    sc->n_skipped += 1;
+    return;
+  }
+  sc->t += 1;
+  sc->beta1_pow = __dmul_rn(sc->beta1_pow, beta1);
+  sc->beta2_pow = __dmul_rn(sc->beta2_pow, beta2);
+  sc->good_steps += 1;
+  if (dynamic && sc->good_steps >= growth_interval) {
+    sc->scale = __fmul_rn(sc->scale, 2.0f);
+    sc->good_steps = 0;
+  }
+  if (flip_sets) sc->state_index ^= 1;
+}
+
 // -------------------------------------------------------------- prologue --
 
 template <int MODE>
@@ -550,7 +579,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
   if (threadIdx.x == 0) compute_step_scalars<MODE>(a, &sh_s);
   __syncthreads();
   const StepScalars s = sh_s;
-  if (s.skip) return;
+  if (s.skip) {
+    // no overflow: nothing to re-cast; the step's bookkeeping, once
+    if (MODE == kCast && (a.mode_flags & kFlagFinish) && blockIdx.x == 0 && threadIdx.x == 0)
+      step_bookkeeping(a.scaler, a.beta1, a.beta2, a.bk_dynamic, a.bk_growth, a.bk_flip);
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   uint32_t tile_no = 0;  // tiles done by this CTA
@@ -601,6 +635,21 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
         if (warp == static_cast<int>(tile_no % kWarps)) {
           const float4 rec = tile_norm_record(sh_norm, par, kWarps, lane);
           if (lane == 0) a.partials[sg.tile_global0 + (g - sg.tile_local0)] = rec;
+        }
+      }
+    }
+  }
+  if constexpr (MODE == kCast) {
+    if (a.mode_flags & kFlagFinish) {
+      // overflow path: the last CTA to finish its re-cast does the bookkeeping
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t done = atomicAdd(&a.scaler->finish_count, 1u);
+        if (done == gridDim.x - 1) {
+          __threadfence();
+          step_bookkeeping(a.scaler, a.beta1, a.beta2, a.bk_dynamic, a.bk_growth, a.bk_flip);
+          a.scaler->finish_count = 0;
         }
       }
     }
@@ -687,12 +736,12 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // true when the phase of the given parity has completed; false after the limit
-__device__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -1206,33 +1255,22 @@ int launch_norm_finish(const float4* records, int64_t t0, int64_t t1, float4* bl
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
-// Loss scale, skip and step-count bookkeeping at the end of a step
-// ("Training models too big for one GPU: ZeRO & FSDP", "Mixed-precision
-// training": pick the scale dynamically and skip a step on overflow).
+// Bookkeeping alone (two-pass path, and plans without elements).
 __global__ void scaler_finish_kernel(zero_scaler* sc, double beta1, double beta2, int dynamic,
                                      int growth_interval, int flip_sets) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  const uint32_t ov = sc->pending;
-  sc->pending = 0;
-  sc->overflow = ov ? 1u : 0u;
-  if (ov) {
-    if (dynamic) {
-      const float half = __fmul_rn(sc->scale, 0.5f);
-      sc->scale = half < 1.0f ? 1.0f : half;
-    }
-    sc->good_steps = 0;
-    sc->n_skipped += 1;
-    return;
+  step_bookkeeping(sc, beta1, beta2, dynamic, growth_interval, flip_sets);
+}
+
+// Self-test of the bounded wait: nothing ever arrives on the barrier.
+__global__ void wait_timeout_probe_kernel(zero_scaler* sc, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
   }
-  sc->t += 1;
-  sc->beta1_pow = __dmul_rn(sc->beta1_pow, beta1);
-  sc->beta2_pow = __dmul_rn(sc->beta2_pow, beta2);
-  sc->good_steps += 1;
-  if (dynamic && sc->good_steps >= growth_interval) {
-    sc->scale = __fmul_rn(sc->scale, 2.0f);
-    sc->good_steps = 0;
-  }
-  if (flip_sets) sc->state_index ^= 1;
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, limit_ns)) set_error(sc, ZERO_DEVERR_TIMEOUT);
 }
 
 // ----------------------------------------------------------- launch layer --
@@ -1331,11 +1369,24 @@ template <int MODE, bool kBf16>
 int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
                 cudaStream_t stream) {
   constexpr bool kBulk = MODE == kFused || MODE == kReduce || MODE == kUpdate;
+  const bool finish = MODE == kCast && (a.mode_flags & kFlagFinish);
   int grid_cap = 1;
   if constexpr (!kBulk) grid_cap = grid_size<MODE, kBf16>();
   if (grid_cap <= 0) return ZERO_ECUDA;
+  if (finish) {
+    // one CTA per SM: the no-overflow case exits at once, the rare re-cast
+    // still has every SM
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ZERO_ECUDA;
+    grid_cap = std::min(grid_cap, sms);
+  }
+  const int flags = a.mode_flags;
   for (int32_t s0 = seg_begin; s0 < seg_end; s0 += kMaxSegs) {
     const int32_t s1 = std::min(seg_end, s0 + kMaxSegs);
+    // the bookkeeping rides on the last launch only
+    a.mode_flags = (finish && s1 < seg_end) ? (flags & ~kFlagFinish) : flags;
     int64_t tiles = 0;
     for (int32_t s = s0; s < s1; ++s) {
       Seg& d = a.segs[s - s0];
@@ -1602,16 +1653,29 @@ ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t ra
   if (rc) return rc;
   const bool fused = grad_shards == nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (fused) {
-    // skip path: re-cast the parameters from the kept master set
-    a->mode_flags = kFlagIfPending | kFlagUseScalerSet;
-    const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+  const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
+  if (fused && s0 < s1) {
+    // one launch: re-cast the parameters from the kept master set if the
+    // step overflowed, and the bookkeeping
+    a->mode_flags = kFlagIfPending | kFlagUseScalerSet | kFlagFinish;
+    a->bk_dynamic = hp->dynamic_scale;
+    a->bk_growth = hp->growth_interval;
+    a->bk_flip = 1;
     rc = launch<kCast>(plan, *a, s0, s1, st);
+    delete a;
+    return rc;
   }
   delete a;
-  if (rc) return rc;
   scaler_finish_kernel<<<1, 32, 0, st>>>(d_scaler, hp->beta1, hp->beta2, hp->dynamic_scale,
                                          hp->growth_interval, fused ? 1 : 0);
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns, void* stream) {
+  if (!d_scaler || limit_ns < 1000 || limit_ns > 10000000000ll) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler)) return ZERO_EALIGN;
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      d_scaler, static_cast<uint64_t>(limit_ns));
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 

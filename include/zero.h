@@ -192,7 +192,7 @@ typedef struct zero_scaler {
   int32_t norm_step;    /* t + 1 of the step zero_grad_norm was computed for */
   int32_t n_skipped;    /* steps skipped so far */
   int32_t error;        /* device error word: 0 = ok, else a ZERO_DEVERR_* code */
-  int32_t reserved;
+  uint32_t finish_count;/* library-internal CTA counter of the step's last kernel; 0 between calls */
 } zero_scaler;
 
 /* device error codes written to zero_scaler.error (first error wins) */
@@ -309,10 +309,19 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
                               const float* const* master, void* flat_params,
                               int64_t window_base, void* stream);
 
+/* Self-test of the failure detection: launches one CTA that waits on a
+ * pipeline barrier nobody ever completes, with the same bounded wait the
+ * step kernels use but a limit of limit_ns nanoseconds (1e3 .. 1e10). When
+ * the wait expires the kernel writes ZERO_DEVERR_TIMEOUT to d_scaler->error
+ * and returns, leaving the context usable. Returns ZERO_EINVAL for a limit
+ * outside the range. */
+ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns, void* stream);
+
 /* Kernels launched per call, for accounting (L = ceil(segments processed /
- * 128), empty launches skipped): fused zero_step 2L + 1 (update, overflow
- * re-cast check, bookkeeping), two-pass zero_step L + 1, zero_reduce_scatter
- * L, zero_grad_norm 1 (+ L when it recomputes the partials), zero_cast_params L. */
+ * 128), empty launches skipped): fused zero_step L + L (update; overflow
+ * re-cast check merged with the bookkeeping in the last), two-pass zero_step
+ * L + 1, zero_reduce_scatter L, zero_grad_norm 2 (+ L when it recomputes the
+ * partials), zero_cast_params L. */
 
 /* Maximum number of norm tiles (ZERO_TILE_ELEMS elements each, counted per
  * segment) that one zero_grad_norm_noalloc call may cover: 2^19 tiles, about

@@ -120,4 +120,8 @@ def test_host_validation_without_gpu():
     with pytest.raises(Z.ZeroError) as e:
         Z.zero_grad_norm(p, 0, 4, None, hp, 16, 16)
     assert e.value.status == -1
+    for bad_limit in (0, 999, 10**11):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_selftest_wait_timeout(16, bad_limit)
+        assert e.value.status == -1
     Z.zero_plan_destroy(p)

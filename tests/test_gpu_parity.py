@@ -201,3 +201,22 @@ def test_widening_all_16bit_patterns(bf16):
     assert np.array_equal(g.flags_u32() != 0, bad_bucket)
     assert g.read_scaler().pending == 1
     g.close()
+
+
+def test_bounded_wait_times_out_without_fault():
+    """The pipeline's bounded barrier wait, driven to expiry on purpose (a
+    barrier nobody completes, 5 ms limit): the kernel records
+    ZERO_DEVERR_TIMEOUT and returns; the context stays usable for a normal
+    step afterwards."""
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    wl = W.Workload("timeout", [10_000], 2, 0, True, 1, 1e-3, steps=1)
+    g = harness.Group(wl)
+    g.init_state()
+    Z.zero_selftest_wait_timeout(g.scaler.data_ptr(), 5_000_000, g.sptr)
+    assert g.read_scaler().error == 3
+    g.init_state()  # fresh scaler
+    g.gen_grads(1)
+    g.step()
+    s = g.read_scaler()
+    assert s.error == 0 and s.t == 1
+    g.close()
