@@ -178,6 +178,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# --------------------------------------------------------- multi-GPU glue ----
+
+def max_over_ranks(dist, ms):
+    """Slowest rank's time for the timed region (identity on one process)."""
+    if not dist:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(psi_per_rank_step, steps, world, total_ms):
+    """Whole-job Gparams/s: every rank updates psi_per_rank_step parameters
+    per step (weak scaling), over the slowest rank's time."""
+    return psi_per_rank_step * steps * world / (total_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------ libzero arm ----
 
 def run_libzero(args, rank, world, dist):
@@ -273,14 +291,10 @@ def run_libzero(args, rank, world, dist):
     total_ms = t0.elapsed_time(t1)
     phase_ms = {name: statistics.mean(a.elapsed_time(b) for a, b in evs[name]) for name, _ in ph}
 
-    # max over ranks of the timed region
-    if dist:
-        tt = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(dist, total_ms)
     ms_per_step = total_ms / K
     pstep = psi_step(wl)
-    value = pstep * K * world / (total_ms / 1e3) / 1e9
+    value = job_throughput(pstep, K, world, total_ms)
 
     # roofline of the dominant kernel
     peak, peak_kind = peaks()
@@ -329,12 +343,8 @@ def run_libzero(args, rank, world, dist):
             host_scaler.copy_(g.scaler, non_blocking=True)
         e1.record(g.stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": round(pstep * E * world / (e2e_ms / 1e3) / 1e9, 4), "unit": UNIT,
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    e2e = {"value": round(job_throughput(pstep, E, world, e2e_ms), 4), "unit": UNIT,
            "steps": E, "h2d_bytes_per_step": int(g.replicas.numel() * 2),
            "d2h_bytes_per_step": int(g.flat.numel() * 2 + g.scaler.numel())}
     sk = g.read_scaler()
