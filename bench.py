@@ -318,35 +318,84 @@ def run_libzero(args, rank, world, dist):
                 "north_star_frac_2n26": round((2 * N + 26) * pstep / (ms_per_step / 1e3) / 1e9
                                               / peak, 4)}
 
-    # end to end through the C ABI: replicas from pinned host memory, updated
-    # parameters and scaler read back every step
+    # end to end through the C ABI: every step copies that step's replicas from
+    # pinned host memory and reads the updated parameters and the scaler back.
+    # Steps are pipelined over two replica buffers and two parameter buffers:
+    # the host->device copy of step k+1 (split over two copy streams) runs
+    # while step k computes, and step k's read-back runs on a third stream.
     E = max(1, min(args.e2e_steps, K))
     host_reps = torch.empty(g.replicas.shape, dtype=torch.int16, pin_memory=True)
     host_reps.copy_(g.replicas)
-    host_params = torch.empty(g.flat.shape, dtype=torch.int16, pin_memory=True)
-    host_scaler = torch.empty(g.scaler.shape, dtype=torch.uint8, pin_memory=True)
+    host_params = [torch.empty(g.flat.shape, dtype=torch.int16, pin_memory=True) for _ in range(2)]
+    host_scaler = [torch.empty(g.scaler.shape, dtype=torch.uint8, pin_memory=True)
+                   for _ in range(2)]
+    dev_reps = [g.replicas, torch.empty_like(g.replicas)]
+    dev_flat = [g.flat, torch.empty_like(g.flat)]
+    scaler_snap = [torch.empty_like(g.scaler) for _ in range(2)]
+    rep_ptrs = [g.rep_ptrs(dev_reps[0]), g.rep_ptrs(dev_reps[1])]
+    h2d = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    d2h = torch.cuda.Stream(device=dev)
+    half = N // 2 if N > 1 else N
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    landed = [ev(), ev()]       # replicas of buffer b on the device
+    computed = [ev(), ev()]     # step that used buffer b finished
+    read_back = [ev(), ev()]    # parameters of buffer b copied to the host
+
+    def copy_in(b):
+        for i, (lo_r, hi_r) in enumerate(((0, half), (half, N))):
+            if hi_r <= lo_r:
+                continue
+            with torch.cuda.stream(h2d[i]):
+                h2d[i].wait_event(computed[b])
+                dev_reps[b][lo_r:hi_r].copy_(host_reps[lo_r:hi_r], non_blocking=True)
+        h2d[0].wait_stream(h2d[1])
+        landed[b].record(h2d[0])
+
+    def step_on(b):
+        rp, fp = rep_ptrs[b], dev_flat[b].data_ptr()
+        if not g.two_pass:
+            Z.zero_step(g.plan, lo, hi, m, v, w, 2, None, rp, g.wbase, fp, g.hp, sc, fl, st)
+        else:
+            Z.zero_reduce_scatter(g.plan, -1, lo, hi, rp, g.wbase, gp, sc, fl, ws if clip else 0,
+                                  st)
+            if clip:
+                Z.zero_grad_norm(g.plan, lo, hi, None, g.hp, sc, ws, st)
+            Z.zero_step(g.plan, lo, hi, m, v, w, 1, gp, None, g.wbase, fp, g.hp, sc, fl, st)
+
+    for e in computed + read_back:
+        e.record(g.stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
-    with torch.cuda.stream(g.stream):
-        e0.record(g.stream)
-        for _ in range(E):
-            g.replicas.copy_(host_reps, non_blocking=True)
-            if not g.two_pass:
-                Z.zero_step(g.plan, lo, hi, m, v, w, 2, None, reps, g.wbase, flat, g.hp, sc, fl,
-                            st)
-            else:
-                for name, f in ph:
-                    f()
-            host_params.copy_(g.flat, non_blocking=True)
-            host_scaler.copy_(g.scaler, non_blocking=True)
-        e1.record(g.stream)
+    e0.record(g.stream)
+    h2d[0].wait_event(e0)
+    h2d[1].wait_event(e0)
+    copy_in(0)
+    for k in range(E):
+        b = k % 2
+        if k + 1 < E:
+            copy_in(1 - b)
+        g.stream.wait_event(landed[b])
+        g.stream.wait_event(read_back[b])   # parameters buffer b free again
+        step_on(b)
+        with torch.cuda.stream(g.stream):
+            scaler_snap[b].copy_(g.scaler, non_blocking=True)  # this step's scaler
+        computed[b].record(g.stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(computed[b])
+            host_params[b].copy_(dev_flat[b], non_blocking=True)
+            host_scaler[b].copy_(scaler_snap[b], non_blocking=True)
+        read_back[b].record(d2h)
+    g.stream.wait_stream(d2h)
+    e1.record(g.stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
     e2e = {"value": round(job_throughput(pstep, E, world, e2e_ms), 4), "unit": UNIT,
            "steps": E, "h2d_bytes_per_step": int(g.replicas.numel() * 2),
-           "d2h_bytes_per_step": int(g.flat.numel() * 2 + g.scaler.numel())}
+           "d2h_bytes_per_step": int(g.flat.numel() * 2 + g.scaler.numel()),
+           "pipelined": "two replica and parameter buffers; H2D of step k+1 overlaps step k"}
+    del dev_reps, host_reps
     sk = g.read_scaler()
     g.close()
 
