@@ -18,7 +18,8 @@ __all__ = [
     "zero_plan_create", "zero_plan_destroy", "zero_plan_get_info", "zero_plan_tensor_offsets",
     "zero_plan_segments", "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
     "zero_reduce_scatter", "zero_grad_norm", "zero_step", "zero_step_update", "zero_step_finish",
-    "zero_cast_params", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
+    "zero_cast_params", "zero_accumulate", "zero_reduce_scatter_accum", "zero_step_accum",
+    "zero_step_update_accum", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
     "zero_version", "lib",
 ]
 
@@ -101,6 +102,15 @@ def lib():
         L.zero_step_finish.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), C.c_int32, _P(_VP),
                                        C.c_int64, _VP, _P(ZeroHParams), _VP, _VP]
         L.zero_cast_params.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _VP, C.c_int64, _VP]
+        L.zero_accumulate.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), C.c_int64,
+                                      C.c_int32, _VP]
+        L.zero_reduce_scatter_accum.argtypes = [_VP, C.c_int32, C.c_int32, C.c_int32, _P(_VP),
+                                                _P(_VP), C.c_int32, C.c_int64, _P(_VP), _VP,
+                                                _VP, _VP, _VP]
+        L.zero_step_accum.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _P(_VP),
+                                      C.c_int32, _P(_VP), _P(_VP), _P(_VP), C.c_int32,
+                                      C.c_int64, _VP, _P(ZeroHParams), _VP, _VP, _VP]
+        L.zero_step_update_accum.argtypes = L.zero_step_accum.argtypes
         L.zero_grad_norm_noalloc.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP),
                                              _P(ZeroHParams), _VP, _VP]
         L.zero_selftest_wait_timeout.argtypes = [_VP, C.c_int64, _VP]
@@ -220,6 +230,38 @@ def zero_step_finish(plan, rank_lo, rank_hi, master, n_sets, grad_shards, window
 def zero_cast_params(plan, rank_lo, rank_hi, master, flat_params, window_base, stream=0):
     _check("zero_cast_params", lib().zero_cast_params(
         plan, rank_lo, rank_hi, _ptrs(master), _vp(flat_params), window_base, _vp(stream)))
+
+
+def zero_accumulate(plan, rank_lo, rank_hi, micro, accum, window_base, first, stream=0):
+    _check("zero_accumulate", lib().zero_accumulate(
+        plan, rank_lo, rank_hi, _ptrs(micro), _ptrs(accum), window_base, int(bool(first)),
+        _vp(stream)))
+
+
+def zero_reduce_scatter_accum(plan, bucket, rank_lo, rank_hi, replicas, accum, n_micro,
+                              window_base, grad_shards, d_scaler, d_bucket_flags=0,
+                              d_workspace=0, stream=0):
+    _check("zero_reduce_scatter_accum", lib().zero_reduce_scatter_accum(
+        plan, bucket, rank_lo, rank_hi, _ptrs(replicas), _ptrs(accum), n_micro, window_base,
+        _ptrs(grad_shards), _vp(d_scaler), _vp(d_bucket_flags), _vp(d_workspace), _vp(stream)))
+
+
+def zero_step_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
+                    replicas, accum, n_micro, window_base, flat_params, hp, d_scaler,
+                    d_bucket_flags=0, stream=0):
+    _check("zero_step_accum", lib().zero_step_accum(
+        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
+        _ptrs(grad_shards), _ptrs(replicas), _ptrs(accum), n_micro, window_base,
+        _vp(flat_params), C.byref(hp), _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
+
+
+def zero_step_update_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
+                           grad_shards, replicas, accum, n_micro, window_base, flat_params, hp,
+                           d_scaler, d_bucket_flags=0, stream=0):
+    _check("zero_step_update_accum", lib().zero_step_update_accum(
+        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
+        _ptrs(grad_shards), _ptrs(replicas), _ptrs(accum), n_micro, window_base,
+        _vp(flat_params), C.byref(hp), _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
 
 
 def zero_grad_norm_noalloc(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, stream=0):

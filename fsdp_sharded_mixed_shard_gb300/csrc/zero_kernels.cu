@@ -88,7 +88,8 @@ struct StagePlan {
 };
 
 struct Args {
-  const uint16_t* rep[ZERO_MAX_RANKS];      // replica windows
+  const uint16_t* rep[ZERO_MAX_RANKS];      // replica windows (the last micro-batch's gradients)
+  const float* acc[ZERO_MAX_RANKS];         // fp32 accumulators of the earlier micro-batches
   float* master[2][ZERO_MAX_RANKS];
   float* mom[2][ZERO_MAX_RANKS];
   float* var[2][ZERO_MAX_RANKS];
@@ -102,6 +103,9 @@ struct Args {
   // step constants rounded once from the fp64 hyperparameters
   float b1, omb1, b2, omb2, lr, decay, eps;
   int32_t bk_dynamic, bk_growth, bk_flip;  // bookkeeping (kFlagFinish)
+  int32_t n_micro;                          // micro-batches in this step (>= 1)
+  int32_t has_acc;                          // 1: replica value = acc + 16-bit micro-batch value
+  int32_t pad1;
   double beta1, beta2;
   StagePlan plan;  // bulk pipeline: stages of one element range
   Seg segs[kMaxSegs];
@@ -400,7 +404,10 @@ __device__ void compute_step_scalars(const Args& a, StepScalars* out) {
   s.src = 0;
   s.dst = 0;
   if (MODE == kFused || MODE == kReduce) {
-    const double denom = __dmul_rn(static_cast<double>(sc->scale), static_cast<double>(a.n_ranks));
+    // average over the N ranks and the k micro-batches of each, after the loss scale
+    const double denom = __dmul_rn(
+        __dmul_rn(static_cast<double>(sc->scale), static_cast<double>(a.n_ranks)),
+        static_cast<double>(a.n_micro));
     s.inv = __double2float_rn(__ddiv_rn(1.0, denom));
   }
   if (MODE == kFused || MODE == kUpdate) {
@@ -547,6 +554,7 @@ __device__ __forceinline__ void do_scalar(const Args& a, const StepScalars& s, i
       int rr = first_rep + p;
       if (rr >= N) rr -= N;
       float x = widen<kBf16>(a.rep[rr][w]);
+      if (a.has_acc) x = __fadd_rn(a.acc[rr][w], x);  // accumulated replica value
       acc = p == 0 ? x : __fadd_rn(acc, x);
     }
     g = __fmul_rn(acc, s.inv);
@@ -808,6 +816,52 @@ struct HalfVec<8> {
   }
 };
 
+// d0 = a0 + low half of w, d1 = a1 + high half of w (same mixed-precision add)
+template <bool kBf16>
+__device__ __forceinline__ void add_halves_to(float& d0, float& d1, uint32_t w, float a0,
+                                              float a1) {
+  if constexpr (kBf16) {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+        " add.rn.f32.bf16 %0, l, %3;\n add.rn.f32.bf16 %1, h, %4;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(w), "f"(a0), "f"(a1));
+  } else {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n"
+        " add.rn.f32.f16 %0, l, %3;\n add.rn.f32.f16 %1, h, %4;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(w), "f"(a0), "f"(a1));
+  }
+}
+
+// With fp32 accumulators of earlier micro-batches: replica value
+// A = acc + widen(micro) (one rounding), then the ring sum sum += A.
+// micro chunks are 2E bytes apart, accumulator chunks 4E bytes apart.
+template <bool kBf16, int EPT>
+__device__ __forceinline__ void acc_stage_accum(const unsigned char* mp, const unsigned char* ap,
+                                                int E, int n, float (&sum)[EPT]) {
+#pragma unroll 2
+  for (int p = 0; p < n; ++p) {
+    HalfVec<EPT> w;
+    w.load(mp + static_cast<size_t>(p) * (2 * E));
+    float av[EPT];
+#pragma unroll
+    for (int i = 0; i < EPT / 4; ++i) {
+      const float4 q = reinterpret_cast<const float4*>(ap + static_cast<size_t>(p) * (4 * E))[i];
+      av[4 * i] = q.x;
+      av[4 * i + 1] = q.y;
+      av[4 * i + 2] = q.z;
+      av[4 * i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < EPT / 2; ++i) {
+      float v0, v1;
+      add_halves_to<kBf16>(v0, v1, w.word(i), av[2 * i], av[2 * i + 1]);
+      sum[2 * i] = __fadd_rn(sum[2 * i], v0);
+      sum[2 * i + 1] = __fadd_rn(sum[2 * i + 1], v1);
+    }
+  }
+}
+
 // acc[e] += replica chunks 0..R-1 of this thread's EPT elements, in ring
 // order; all R shared-memory loads are issued before the adds. `stride` is
 // the chunk size in bytes.
@@ -906,11 +960,12 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
   return t;
 }
 
-template <int MODE, bool kBf16, int EPT>
+template <int MODE, bool kBf16, int EPT, bool kAcc>
 __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
                                                                int n_slots,
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
+  constexpr int kRepBytes = kAcc ? 6 : 2;  // per replica and element: 16-bit value (+ fp32 accumulator)
   __shared__ StepScalars sh_s;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -973,14 +1028,21 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
           const int r_lo = a.plan.r_lo[st], r_hi = a.plan.r_hi[st];
           const int n_rep = r_hi - r_lo;
           const int n_state = a.plan.states[st] ? (MODE == kUpdate ? 4 : 3) : 0;
-          for (int c = lane; c < n_rep + n_state; c += 32) {
+          const int n_rep_chunks = kAcc ? 2 * n_rep : n_rep;
+          for (int c = lane; c < n_rep_chunks + n_state; c += 32) {
             if (c < n_rep) {
               int rr = t.first_rep + r_lo + c;
               if (rr >= N) rr -= N;
               bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
                        &full_bar[slot], pol);
+            } else if (kAcc && c < n_rep_chunks) {
+              int rr = t.first_rep + r_lo + (c - n_rep);
+              if (rr >= N) rr -= N;
+              bulk_g2s(buf + static_cast<size_t>(n_rep) * (2 * E) +
+                           static_cast<size_t>(c - n_rep) * (4 * E),
+                       a.acc[rr] + w, len * 4, &full_bar[slot], pol);
             } else {
-              const int q = c - n_rep;
+              const int q = c - n_rep_chunks;
               const float* src;
               if (MODE == kUpdate) {
                 src = q == 0 ? a.ghat[t.rank]
@@ -990,7 +1052,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                 src = q == 0 ? a.master[s.src][t.rank]
                              : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
               }
-              bulk_g2s(buf + static_cast<size_t>(n_rep) * (2 * E) + static_cast<size_t>(q) * (4 * E),
+              bulk_g2s(buf + static_cast<size_t>(n_rep) * (kRepBytes * E) +
+                           static_cast<size_t>(q) * (4 * E),
                        src + kk, len * 4, &full_bar[slot], pol);
             }
           }
@@ -1072,7 +1135,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if constexpr (MODE == kFused || MODE == kReduce) {
           const bool completes = r_hi == N && r_lo < r_hi;  // stage ends the range's sum
           if (mine) {
-            acc_stage<kBf16, EPT>(buf + t_off * 2, 2 * E, r_hi - r_lo, acc);
+            if constexpr (kAcc)
+              acc_stage_accum<kBf16, EPT>(buf + t_off * 2,
+                                          buf + static_cast<size_t>(r_hi - r_lo) * (2 * E) +
+                                              t_off * 4,
+                                          E, r_hi - r_lo, acc);
+            else
+              acc_stage<kBf16, EPT>(buf + t_off * 2, 2 * E, r_hi - r_lo, acc);
             if (completes) {
               const uint64_t inv2 = f2_pack(s.inv, s.inv);
 #pragma unroll
@@ -1108,7 +1177,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if (mine) {
           if constexpr (MODE == kFused || MODE == kUpdate) {
             if (a.plan.states[st]) {
-              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (2 * E);
+              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (kRepBytes * E);
               if constexpr (MODE == kUpdate) {
                 lds_fv<EPT>(sb + t_off * 4, gv);
                 sb += 4 * E;
@@ -1291,7 +1360,8 @@ int grid_size() {
 // each) in ring order, then the indivisible state block (kFused 12, kUpdate
 // 16 bytes per element) in the last stage if it fits, else in a stage of
 // its own.
-inline StagePlan make_stage_plan(int mode, int n_ranks, int E, uint32_t* slot_bytes) {
+inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
+                                 uint32_t* slot_bytes) {
   StagePlan pl{};
   const int budget = kStageBudget / E;  // bytes per element
   const int n_rep = mode == kUpdate ? 0 : n_ranks;
@@ -1299,7 +1369,7 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, uint32_t* slot_by
   int lo = 0, cur = 0;
   int max_bpe = 0;
   auto close = [&](int hi, int with_states) {
-    const int bpe = 2 * (hi - lo) + (with_states ? state_bpe : 0);
+    const int bpe = rep_bytes * (hi - lo) + (with_states ? state_bpe : 0);
     pl.r_lo[pl.n] = static_cast<int16_t>(lo);
     pl.r_hi[pl.n] = static_cast<int16_t>(hi);
     pl.states[pl.n] = with_states;
@@ -1310,8 +1380,8 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, uint32_t* slot_by
     cur = 0;
   };
   for (int p = 0; p < n_rep; ++p) {
-    if (cur + 2 > budget) close(p, 0);
-    cur += 2;
+    if (cur + rep_bytes > budget) close(p, 0);
+    cur += rep_bytes;
   }
   if (state_bpe > 0) {
     if (cur > 0 && cur + state_bpe <= budget) {
@@ -1327,16 +1397,16 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, uint32_t* slot_by
   return pl;
 }
 
-template <int MODE, bool kBf16, int EPT>
+template <int MODE, bool kBf16, int EPT, bool kAcc>
 int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
   constexpr int E = kConsumers * EPT;
   uint32_t slot_bytes = 0;
-  a.plan = make_stage_plan(MODE, a.n_ranks, E, &slot_bytes);
+  a.plan = make_stage_plan(MODE, a.n_ranks, E, kAcc ? 6 : 2, &slot_bytes);
   if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
   const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));
   if (slots < 2) return ZERO_ERANGE;
   const size_t smem = static_cast<size_t>(slots) * slot_bytes;
-  auto kern = bulk_kernel<MODE, kBf16, EPT>;
+  auto kern = bulk_kernel<MODE, kBf16, EPT, kAcc>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return ZERO_ECUDA;
@@ -1360,9 +1430,12 @@ int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
 // ranges and more, smaller slots.
 template <int MODE, bool kBf16>
 int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+  if constexpr (MODE == kFused || MODE == kReduce) {
+    if (a.has_acc) return launch_bulk_ept<MODE, kBf16, 4, true>(a, tiles, stream);
+  }
   if (MODE == kReduce && 2 * a.n_ranks * kConsumers * 8 <= kStageBudget)
-    return launch_bulk_ept<MODE, kBf16, 8>(a, tiles, stream);
-  return launch_bulk_ept<MODE, kBf16, 4>(a, tiles, stream);
+    return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
+  return launch_bulk_ept<MODE, kBf16, 4, false>(a, tiles, stream);
 }
 
 template <int MODE, bool kBf16>
@@ -1455,6 +1528,19 @@ int set_replicas(Args& a, const zero_plan* p, const void* const* replicas) {
   return ZERO_OK;
 }
 
+// Earlier micro-batches' fp32 accumulators (all N replicas) when n_micro > 1.
+int set_accumulators(Args& a, const zero_plan* p, const float* const* accum, int32_t n_micro) {
+  if (n_micro < 1) return ZERO_EINVAL;
+  a.n_micro = n_micro;
+  a.has_acc = n_micro > 1 ? 1 : 0;
+  if (!a.has_acc) return ZERO_OK;
+  const int32_t N = p->info.n_ranks;
+  int rc = check_ptr_array(reinterpret_cast<const void* const*>(accum), 0, N, N, 1);
+  if (rc) return rc;
+  for (int32_t r = 0; r < N; ++r) a.acc[r] = accum[r];
+  return ZERO_OK;
+}
+
 int window_ok(const zero_plan* p, int32_t rank_lo, int64_t wbase) {
   return wbase >= 0 && wbase <= static_cast<int64_t>(rank_lo) * p->info.shard_elems;
 }
@@ -1465,6 +1551,7 @@ Args* new_args(const zero_plan* p) {
   std::memset(a, 0, sizeof(Args));
   a->n_ranks = p->info.n_ranks;
   a->shard = p->info.shard_elems;
+  a->n_micro = 1;
   return a;
 }
 
@@ -1498,6 +1585,17 @@ ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t 
                                  int64_t window_base, float* const* grad_shards,
                                  zero_scaler* d_scaler, uint32_t* d_bucket_flags,
                                  void* d_workspace, void* stream) {
+  return zero_reduce_scatter_accum(plan, bucket, rank_lo, rank_hi, replicas, nullptr, 1,
+                                   window_base, grad_shards, d_scaler, d_bucket_flags,
+                                   d_workspace, stream);
+}
+
+ZERO_API int zero_reduce_scatter_accum(const zero_plan* plan, int32_t bucket, int32_t rank_lo,
+                                       int32_t rank_hi, const void* const* replicas,
+                                       const float* const* accum, int32_t n_micro,
+                                       int64_t window_base, float* const* grad_shards,
+                                       zero_scaler* d_scaler, uint32_t* d_bucket_flags,
+                                       void* d_workspace, void* stream) {
   if (!ranks_ok(plan, rank_lo, rank_hi) || !d_scaler) return ZERO_EINVAL;
   if (bucket < -1 || bucket >= plan->info.n_buckets) return ZERO_EINVAL;
   if (!window_ok(plan, rank_lo, window_base)) return ZERO_EINVAL;
@@ -1510,6 +1608,7 @@ ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t 
   Args* a = new_args(plan);
   if (!a) return ZERO_ENOMEM;
   rc = set_replicas(*a, plan, replicas);
+  if (!rc) rc = set_accumulators(*a, plan, accum, n_micro);
   if (!rc) {
     for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = grad_shards[i];
     a->wbase = window_base;
@@ -1628,11 +1727,28 @@ ZERO_API int zero_step_update(const zero_plan* plan, int32_t rank_lo, int32_t ra
                               const float* const* grad_shards, const void* const* replicas,
                               int64_t window_base, void* flat_params, const zero_hparams* hp,
                               zero_scaler* d_scaler, uint32_t* d_bucket_flags, void* stream) {
+  return zero_step_update_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
+                                grad_shards, replicas, nullptr, 1, window_base, flat_params, hp,
+                                d_scaler, d_bucket_flags, stream);
+}
+
+ZERO_API int zero_step_update_accum(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                                    float* const* master, float* const* exp_avg,
+                                    float* const* exp_avg_sq, int32_t n_sets,
+                                    const float* const* grad_shards, const void* const* replicas,
+                                    const float* const* accum, int32_t n_micro,
+                                    int64_t window_base, void* flat_params,
+                                    const zero_hparams* hp, zero_scaler* d_scaler,
+                                    uint32_t* d_bucket_flags, void* stream) {
   Args* a = nullptr;
   int rc = prepare_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
                         replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags, true,
                         true, &a);
   if (rc) return rc;
+  if (grad_shards == nullptr && (rc = set_accumulators(*a, plan, accum, n_micro))) {
+    delete a;
+    return rc;
+  }
   const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = grad_shards == nullptr ? launch<kFused>(plan, *a, s0, s1, st)
@@ -1685,9 +1801,21 @@ ZERO_API int zero_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
                        const void* const* replicas, int64_t window_base, void* flat_params,
                        const zero_hparams* hp, zero_scaler* d_scaler,
                        uint32_t* d_bucket_flags, void* stream) {
-  int rc = zero_step_update(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
-                            grad_shards, replicas, window_base, flat_params, hp, d_scaler,
-                            d_bucket_flags, stream);
+  return zero_step_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
+                         grad_shards, replicas, nullptr, 1, window_base, flat_params, hp,
+                         d_scaler, d_bucket_flags, stream);
+}
+
+ZERO_API int zero_step_accum(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                             float* const* master, float* const* exp_avg,
+                             float* const* exp_avg_sq, int32_t n_sets,
+                             const float* const* grad_shards, const void* const* replicas,
+                             const float* const* accum, int32_t n_micro, int64_t window_base,
+                             void* flat_params, const zero_hparams* hp, zero_scaler* d_scaler,
+                             uint32_t* d_bucket_flags, void* stream) {
+  int rc = zero_step_update_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
+                                  grad_shards, replicas, accum, n_micro, window_base,
+                                  flat_params, hp, d_scaler, d_bucket_flags, stream);
   if (rc) return rc;
   return zero_step_finish(plan, rank_lo, rank_hi, master, n_sets, grad_shards, window_base,
                           flat_params, hp, d_scaler, stream);
@@ -1718,6 +1846,99 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
 }
 
 }  // extern "C"
+
+// ------------------------------------------- micro-batch accumulation --
+//
+// "How far does splitting the batch get you?", "What does gradient
+// accumulation actually buy?": run k micro-batches, accumulate each rank's
+// gradients locally in fp32, reduce once. accumulate_kernel adds one
+// micro-batch's 16-bit gradients of every replica into the fp32
+// accumulators (first micro-batch: the widened values themselves); the last
+// micro-batch is added inside the reduce pass (bulk_kernel<.., kAcc>), so
+// the accumulators are never written for it.
+
+struct AccArgs {
+  const uint16_t* micro[ZERO_MAX_RANKS];
+  float* acc[ZERO_MAX_RANKS];
+  int64_t off, len;  // window elements [off, off + len) of every replica
+  int32_t n_ranks, first;
+  int32_t vec;       // 1: off is on the 8-element grid (16-byte vectors)
+  int32_t pad;
+};
+
+template <bool kBf16>
+__global__ void __launch_bounds__(256) accumulate_kernel(const __grid_constant__ AccArgs a) {
+  const int64_t nvec = a.vec ? (a.len >> 3) : 0;
+  const int64_t total = nvec * a.n_ranks;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+       q += stride) {
+    const int r = static_cast<int>(q / nvec);
+    const int64_t j = a.off + ((q - static_cast<int64_t>(r) * nvec) << 3);
+    float x[8];
+    widen8<kBf16>(__ldcs(reinterpret_cast<const uint4*>(a.micro[r] + j)), x);
+    float* dst = a.acc[r] + j;
+    if (!a.first) {
+      float y[8];
+      load8f(dst, y);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(y[e], x[e]);
+    }
+    store8f(dst, x);
+  }
+  // ragged tail of each replica's window
+  const int64_t tail = a.len - (nvec << 3);
+  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       q < tail * a.n_ranks; q += stride) {
+    const int r = static_cast<int>(q / tail);
+    const int64_t j = a.off + (nvec << 3) + (q - static_cast<int64_t>(r) * tail);
+    const float x = widen<kBf16>(a.micro[r][j]);
+    a.acc[r][j] = a.first ? x : __fadd_rn(a.acc[r][j], x);
+  }
+}
+
+extern "C" ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                                        const void* const* micro, float* const* accum,
+                                        int64_t window_base, int32_t first, void* stream) {
+  if (!ranks_ok(plan, rank_lo, rank_hi)) return ZERO_EINVAL;
+  if (!window_ok(plan, rank_lo, window_base)) return ZERO_EINVAL;
+  const int32_t N = plan->info.n_ranks;
+  int rc = check_ptr_array(micro, 0, N, N, 1);
+  if (rc) return rc;
+  if ((rc = check_ptr_array(reinterpret_cast<const void* const*>(accum), 0, N, N, 1))) return rc;
+  AccArgs* a = new (std::nothrow) AccArgs;
+  if (!a) return ZERO_ENOMEM;
+  std::memset(a, 0, sizeof(AccArgs));
+  for (int32_t r = 0; r < N; ++r) {
+    a->micro[r] = static_cast<const uint16_t*>(micro[r]);
+    a->acc[r] = accum[r];
+  }
+  const int64_t S = plan->info.shard_elems;
+  a->off = static_cast<int64_t>(rank_lo) * S - window_base;
+  a->len = static_cast<int64_t>(rank_hi - rank_lo) * S;
+  a->n_ranks = N;
+  a->first = first ? 1 : 0;
+  // the vector body needs the window offset on the 8-element grid of both
+  // arrays; otherwise the whole window takes the element-wise loop
+  a->vec = (a->off & 7) == 0 ? 1 : 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    delete a;
+    return ZERO_ECUDA;
+  }
+  rc = ZERO_OK;
+  if (a->len > 0) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (plan->info.grad_dtype == ZERO_BF16)
+      accumulate_kernel<true><<<sms * 8, 256, 0, st>>>(*a);
+    else
+      accumulate_kernel<false><<<sms * 8, 256, 0, st>>>(*a);
+    if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
+  }
+  delete a;
+  return rc;
+}
 
 // ------------------------------------------------ no-allocation norm entry --
 //

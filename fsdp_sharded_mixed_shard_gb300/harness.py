@@ -19,9 +19,10 @@ import ctypes as C
 
 import torch
 
-from . import (ZERO_BF16, ZERO_FP16, ZeroHParams, ZeroScaler, zero_cast_params, zero_grad_norm,
-               zero_plan_create, zero_plan_destroy, zero_plan_get_info, zero_reduce_scatter,
-               zero_scaler_init, zero_step, zero_workspace_bytes)
+from . import (ZERO_BF16, ZERO_FP16, ZeroHParams, ZeroScaler, zero_accumulate, zero_cast_params,
+               zero_grad_norm, zero_plan_create, zero_plan_destroy, zero_plan_get_info,
+               zero_reduce_scatter_accum, zero_scaler_init, zero_step, zero_step_accum,
+               zero_workspace_bytes)
 from . import synth
 
 
@@ -64,6 +65,10 @@ class Group:
                                  device=dev)
         self.ghat = (torch.zeros((n_own, self.srow), dtype=torch.float32, device=dev)
                      if self.two_pass else None)
+        # fp32 accumulators of the earlier micro-batches (one per replica)
+        self.n_micro = wl.n_micro
+        self.accum = (torch.zeros((self.N, self.row), dtype=torch.float32, device=dev)
+                      if wl.n_micro > 1 else None)
         self.scaler = torch.zeros(C.sizeof(ZeroScaler), dtype=torch.uint8, device=dev)
         self.flags = torch.zeros(max(self.info.n_buckets, 1), dtype=torch.int32, device=dev)
         ws = zero_workspace_bytes(self.plan)
@@ -124,46 +129,71 @@ class Group:
         return synth.grad_spec(seed=wl.seed, sigma=wl.sigma, bias_sigma=wl.bias_sigma,
                                loss_scale=scale, outliers=wl.outliers, psi=wl.psi)
 
-    def gen_grads(self, step, scale=None, replicas=None):
-        """Fill the replicas with step `step`'s gradients at the device's
-        current loss scale (read back from the scaler unless given)."""
+    def gen_grads(self, step, scale=None, replicas=None, micro=None):
+        """Fill the replicas with step `step`'s gradients (micro-batch `micro`,
+        default the last) at the device's current loss scale (read back from
+        the scaler unless given)."""
         if scale is None:
             scale = self.read_scaler().scale
+        micro = self.n_micro if micro is None else micro
         t = self.replicas if replicas is None else replicas
         spec = self.grad_spec(scale)
         ptrs = self.rep_ptrs(t)
+        key = self.wl.gen_step(step, micro)
         for r in range(self.N):
-            synth.gpu_fill_grad(ptrs[r], self.wlen, self.wbase, spec, step, r, self.is_bf16,
+            synth.gpu_fill_grad(ptrs[r], self.wlen, self.wbase, spec, key, r, self.is_bf16,
                                 self.sptr)
         inj = self.wl.inject
-        if inj is not None and inj[0] == step:
+        if inj is not None and inj[0] == step and micro == self.n_micro:
             _, r, e, bits = inj
             if self.wbase <= e < self.wbase + self.wlen:
                 with torch.cuda.stream(self.stream):
                     t[r, e - self.wbase] = bits - 65536 if bits >= 32768 else bits
 
     # ----------------------------------------------------------------- step
+    def accum_ptrs(self):
+        base, rb = self.accum.data_ptr(), self.row * 4
+        return [base + r * rb for r in range(self.N)]
+
+    def accumulate(self, first):
+        """Add the replicas (one micro-batch) into the fp32 accumulators."""
+        zero_accumulate(self.plan, self.lo, self.hi, self.rep_ptrs(), self.accum_ptrs(),
+                        self.wbase, first, self.sptr)
+
+    def step_micro(self, step, per_bucket=False):
+        """A whole optimizer step of n_micro micro-batches: generate and
+        accumulate the first n_micro - 1, generate the last, then step (the
+        last micro-batch is added inside the reduce)."""
+        for mb in range(1, self.n_micro):
+            self.gen_grads(step, micro=mb)
+            self.accumulate(first=(mb == 1))
+        self.gen_grads(step, micro=self.n_micro)
+        self.step(per_bucket=per_bucket)
+
     def step(self, per_bucket=False, replicas=None, clear_flags=True):
-        """One optimizer step through the C ABI (fused or two-pass)."""
+        """One optimizer step through the C ABI (fused or two-pass), with the
+        accumulators of the earlier micro-batches when n_micro > 1."""
         st = self.sptr
         if clear_flags:
             with torch.cuda.stream(self.stream):
                 self.flags.zero_()
         reps = self.rep_ptrs(replicas)
+        acc = self.accum_ptrs() if self.n_micro > 1 else None
+        k = self.n_micro
         m, v, w = self._state_ptrs(0), self._state_ptrs(1), self._state_ptrs(2)
         sc = self.scaler.data_ptr()
         fl = self.flags.data_ptr()
         if not self.two_pass:
-            zero_step(self.plan, self.lo, self.hi, m, v, w, self.n_sets, None, reps, self.wbase,
-                      self.flat.data_ptr(), self.hp, sc, fl, st)
+            zero_step_accum(self.plan, self.lo, self.hi, m, v, w, self.n_sets, None, reps, acc, k,
+                            self.wbase, self.flat.data_ptr(), self.hp, sc, fl, st)
             return
         clip = self.hp.max_grad_norm > 0
         ws = self.workspace.data_ptr() if clip else 0
         gp = self.ghat_ptrs()
         buckets = range(self.info.n_buckets) if per_bucket else [-1]
         for b in buckets:
-            zero_reduce_scatter(self.plan, b, self.lo, self.hi, reps, self.wbase, gp, sc, fl, ws,
-                                st)
+            zero_reduce_scatter_accum(self.plan, b, self.lo, self.hi, reps, acc, k, self.wbase,
+                                      gp, sc, fl, ws, st)
         if clip:
             zero_grad_norm(self.plan, self.lo, self.hi, None, self.hp, sc, ws, st)
         zero_step(self.plan, self.lo, self.hi, m, v, w, self.n_sets, gp, None, self.wbase,

@@ -58,7 +58,10 @@ class Workload:
     rank_lo: int = 0
     rank_hi: Optional[int] = None           # None = all ranks
     # (step, rank, element, 16-bit pattern) written into one replica element
+    # (of the step's last micro-batch)
     inject: Optional[Tuple[int, int, int, int]] = None
+    # micro-batches per optimizer step, accumulated in fp32 before the reduce
+    n_micro: int = 1
 
     @property
     def psi(self) -> int:
@@ -70,6 +73,11 @@ class Workload:
 
     def scaled(self, **kw) -> "Workload":
         return replace(self, **kw)
+
+    def gen_step(self, step: int, micro: int) -> int:
+        """Generator step index of micro-batch `micro` (1-based) of optimizer
+        step `step`: the step itself when there is one micro-batch."""
+        return step if self.n_micro == 1 else step * 64 + micro
 
 
 FP16_POS_INF = 0x7C00

@@ -302,6 +302,52 @@ ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t ra
                               void* flat_params, const zero_hparams* hp, zero_scaler* d_scaler,
                               void* stream);
 
+/* ---------------------------------------------- micro-batch accumulation --
+ * "How far does splitting the batch get you?", "What does gradient
+ * accumulation actually buy?": run k micro-batches, accumulate each rank's
+ * gradients locally in fp32, then reduce once (an fp32 reduce-scatter).
+ *
+ * zero_accumulate: for every replica r (all N) and every element j of the
+ * window [rank_lo*S, rank_hi*S): accum[r][j] = first ? widen(micro[r][j])
+ *   : accum[r][j] + widen(micro[r][j]) (fp32, round to nearest even).
+ *   micro: N device pointers (16-bit, at flat element window_base);
+ *   accum: N device pointers (fp32, same window). 10 bytes per replica and
+ *   element (6 when first).
+ * zero_reduce_scatter_accum / zero_step_accum / zero_step_update_accum: as
+ *   the calls without the suffix, for a step of n_micro >= 1 micro-batches.
+ *   `replicas` holds the last micro-batch's 16-bit gradients and, when
+ *   n_micro > 1, `accum` the fp32 sums of the earlier n_micro - 1 (from
+ *   zero_accumulate). Each replica's value is accum + widen(replica), one
+ *   rounding, added in ring order; the unscale becomes fp32(1/(S_l*N*n_micro))
+ *   (the average over every micro-batch of every rank). The accumulators are
+ *   read, never written: the fused step reads 6N + 26 bytes per element.
+ *   With n_micro == 1 they equal the calls without the suffix (accum may be
+ *   NULL). zero_step_accum's accumulators only matter on the fused path. */
+ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                             const void* const* micro, float* const* accum, int64_t window_base,
+                             int32_t first, void* stream);
+ZERO_API int zero_reduce_scatter_accum(const zero_plan* plan, int32_t bucket, int32_t rank_lo,
+                                       int32_t rank_hi, const void* const* replicas,
+                                       const float* const* accum, int32_t n_micro,
+                                       int64_t window_base, float* const* grad_shards,
+                                       zero_scaler* d_scaler, uint32_t* d_bucket_flags,
+                                       void* d_workspace, void* stream);
+ZERO_API int zero_step_accum(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                             float* const* master, float* const* exp_avg,
+                             float* const* exp_avg_sq, int32_t n_sets,
+                             const float* const* grad_shards, const void* const* replicas,
+                             const float* const* accum, int32_t n_micro, int64_t window_base,
+                             void* flat_params, const zero_hparams* hp, zero_scaler* d_scaler,
+                             uint32_t* d_bucket_flags, void* stream);
+ZERO_API int zero_step_update_accum(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                                    float* const* master, float* const* exp_avg,
+                                    float* const* exp_avg_sq, int32_t n_sets,
+                                    const float* const* grad_shards, const void* const* replicas,
+                                    const float* const* accum, int32_t n_micro,
+                                    int64_t window_base, void* flat_params,
+                                    const zero_hparams* hp, zero_scaler* d_scaler,
+                                    uint32_t* d_bucket_flags, void* stream);
+
 /* Write the 16-bit working copy of the owners' slices from one fp32 master
  * set (round to nearest even): master[i] is rank i's shard (N entries).
  * Used to initialise the parameters; 6 bytes per element. */

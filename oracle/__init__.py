@@ -102,6 +102,14 @@ def lib():
                                       C.c_void_p, C.c_void_p, C.c_void_p, P(HParams),
                                       P(Scaler)]
         L.orc_step_arrays.restype = C.c_int
+        L.orc_step_arrays_f32.argtypes = [P(Plan), C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+                                          C.c_int32, C.c_int64, C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                          P(HParams), P(Scaler)]
+        L.orc_step_arrays_f32.restype = C.c_int
+        L.orc_unscale_factor_k.argtypes = [C.c_float, C.c_int32, C.c_int32]
+        L.orc_unscale_factor_k.restype = C.c_float
+        L.orc_accumulate.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_int32]
         L.orc_gen_step.argtypes = [P(Plan), C.c_int32, C.c_int32, P(Gen), C.c_uint32,
                                    C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_void_p, P(HParams), P(Scaler)]
@@ -224,6 +232,31 @@ def step_arrays(plan, rank_lo, rank_hi, is_bf16, replicas, wbase, master, m, v, 
                                _ptr(ghat), _ptr(bucket_flags), C.byref(hp), C.byref(sc))
     if rc != 0:
         raise ValueError("orc_step_arrays failed")
+
+
+def unscale_factor_k(scale, n_ranks, n_micro):
+    return np.float32(lib().orc_unscale_factor_k(scale, n_ranks, n_micro))
+
+
+def accumulate(micro, acc, is_bf16, first):
+    """acc (fp32, modified in place) += widen(micro); first: acc = widen(micro)."""
+    micro = np.ascontiguousarray(micro, dtype=np.uint16)
+    assert acc.dtype == np.float32 and acc.flags.c_contiguous and acc.size == micro.size
+    lib().orc_accumulate(_ptr(micro), _ptr(acc), micro.size, int(bool(is_bf16)),
+                         int(bool(first)))
+
+
+def step_arrays_f32(plan, rank_lo, rank_hi, is_bf16, replicas_f32, n_micro, wbase, master, m, v,
+                    params, hp, sc, bucket_flags=None, ghat=None):
+    """One step whose replica values are fp32 accumulated gradients of
+    n_micro micro-batches."""
+    reps = [np.ascontiguousarray(r, dtype=np.float32) for r in replicas_f32]
+    ptrs = (C.c_void_p * len(reps))(*[r.ctypes.data for r in reps])
+    rc = lib().orc_step_arrays_f32(C.byref(plan), rank_lo, rank_hi, int(bool(is_bf16)), ptrs,
+                                   n_micro, wbase, _ptr(master), _ptr(m), _ptr(v), _ptr(params),
+                                   _ptr(ghat), _ptr(bucket_flags), C.byref(hp), C.byref(sc))
+    if rc != 0:
+        raise ValueError("orc_step_arrays_f32 failed")
 
 
 def gen(spec, is_bf16, inject=None):

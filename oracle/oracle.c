@@ -203,8 +203,21 @@ float orc_ring_sum(const float* vals, int32_t n_ranks, int32_t owner) {
 }
 
 float orc_unscale_factor(float scale, int32_t n_ranks) {
+  return orc_unscale_factor_k(scale, n_ranks, 1);
+}
+
+float orc_unscale_factor_k(float scale, int32_t n_ranks, int32_t n_micro) {
   double denom = (double)scale * (double)n_ranks;
+  denom = denom * (double)n_micro;
   return (float)(1.0 / denom);
+}
+
+void orc_accumulate(const uint16_t* micro, float* acc, int64_t n, int32_t is_bf16,
+                    int32_t first) {
+  for (int64_t k = 0; k < n; ++k) {
+    float x = widen16(micro[k], is_bf16);
+    acc[k] = first ? x : acc[k] + x;
+  }
 }
 
 orc_adam_scalars orc_adam_scalars_make(const orc_hparams* hp, int32_t t) {
@@ -289,11 +302,23 @@ static int64_t bucket_of(const orc_plan* p, int64_t j) {
   return p->bucket_elems == 0 ? 0 : j / p->bucket_elems;
 }
 
-int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t is_bf16,
-                    const uint16_t* const* replicas, int64_t wbase, float* master,
-                    float* m, float* v, uint16_t* params, float* ghat,
-                    uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc) {
-  if (!p || !replicas || !hp || !sc) return -1;
+/* Replica value of rank r at window index w: 16-bit arrays or fp32 arrays. */
+typedef struct replica_reader {
+  const uint16_t* const* h16;
+  const float* const* f32;
+  int32_t is_bf16;
+} replica_reader;
+
+static float read_replica(const replica_reader* rd, int32_t r, int64_t w) {
+  return rd->f32 ? rd->f32[r][w] : widen16(rd->h16[r][w], rd->is_bf16);
+}
+
+static int step_arrays_impl(const orc_plan* p, int32_t rank_lo, int32_t rank_hi,
+                            const replica_reader* rd, int32_t n_micro, int32_t is_bf16,
+                            int64_t wbase, float* master, float* m, float* v, uint16_t* params,
+                            float* ghat, uint32_t* bucket_flags, const orc_hparams* hp,
+                            orc_scaler* sc) {
+  if (!p || !hp || !sc || n_micro < 1) return -1;
   if (rank_lo < 0 || rank_hi > p->n_ranks || rank_lo > rank_hi) return -1;
   const int32_t N = p->n_ranks;
   const int64_t lo = (int64_t)rank_lo * p->shard;
@@ -308,11 +333,11 @@ int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t
     return -1;
   }
   /* reduce-scatter with unscale and the non-finite check */
-  const float inv = orc_unscale_factor(sc->scale, N);
+  const float inv = orc_unscale_factor_k(sc->scale, N, n_micro);
   int32_t overflow = 0;
   for (int64_t j = lo; j < hi; ++j) {
     int32_t owner = (int32_t)(j / p->shard);
-    for (int32_t r = 0; r < N; ++r) vals[r] = widen16(replicas[r][j - wbase], is_bf16);
+    for (int32_t r = 0; r < N; ++r) vals[r] = read_replica(rd, r, j - wbase);
     float acc = orc_ring_sum(vals, N, owner);
     float gj = acc * inv;
     g[j - lo] = gj;
@@ -361,6 +386,26 @@ int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t
   free(g);
   free(vals);
   return 0;
+}
+
+int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t is_bf16,
+                    const uint16_t* const* replicas, int64_t wbase, float* master,
+                    float* m, float* v, uint16_t* params, float* ghat,
+                    uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc) {
+  if (!replicas) return -1;
+  replica_reader rd = {replicas, NULL, is_bf16};
+  return step_arrays_impl(p, rank_lo, rank_hi, &rd, 1, is_bf16, wbase, master, m, v, params,
+                          ghat, bucket_flags, hp, sc);
+}
+
+int orc_step_arrays_f32(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t is_bf16,
+                        const float* const* replicas, int32_t n_micro, int64_t wbase,
+                        float* master, float* m, float* v, uint16_t* params, float* ghat,
+                        uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc) {
+  if (!replicas) return -1;
+  replica_reader rd = {NULL, replicas, is_bf16};
+  return step_arrays_impl(p, rank_lo, rank_hi, &rd, n_micro, is_bf16, wbase, master, m, v,
+                          params, ghat, bucket_flags, hp, sc);
 }
 
 /* ---------------------------------------------- generator-driven driver ---- */

@@ -133,6 +133,18 @@ float orc_ring_sum(const float* vals, int32_t n_ranks, int32_t owner);
  * all-reduce"). */
 float orc_unscale_factor(float scale, int32_t n_ranks);
 
+/* fp32(1 / (S * N * k)) for a step of k micro-batches per rank: the average
+ * over every micro-batch of every rank ([SB] "What does gradient
+ * accumulation actually buy?": run k micro-batches, accumulate, reduce
+ * once). k = 1 is orc_unscale_factor. */
+float orc_unscale_factor_k(float scale, int32_t n_ranks, int32_t n_micro);
+
+/* FP32 gradient accumulation over micro-batches ([SB] "What does gradient
+ * accumulation actually buy?": the accumulator has to be fp32):
+ * acc[k] = first ? widen(micro[k]) : acc[k] + widen(micro[k]). */
+void orc_accumulate(const uint16_t* micro, float* acc, int64_t n, int32_t is_bf16,
+                    int32_t first);
+
 /* Adam scalars for optimizer step t (t >= 1). [ZF] "Adam, and why it's
  * expensive" (bias corrections 1 - beta^t). */
 orc_adam_scalars orc_adam_scalars_make(const orc_hparams* hp, int32_t t);
@@ -174,6 +186,15 @@ int orc_step_arrays(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t
                     const uint16_t* const* replicas, int64_t wbase, float* master,
                     float* m, float* v, uint16_t* params, float* ghat,
                     uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc);
+
+/* orc_step_arrays for a step of n_micro micro-batches: replicas[r][j - wbase]
+ * is rank r's fp32 accumulated gradient (sum of its micro-batches, from
+ * orc_accumulate); the unscale is orc_unscale_factor_k; is_bf16 selects the
+ * working copy's format. */
+int orc_step_arrays_f32(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, int32_t is_bf16,
+                        const float* const* replicas, int32_t n_micro, int64_t wbase,
+                        float* master, float* m, float* v, uint16_t* params, float* ghat,
+                        uint32_t* bucket_flags, const orc_hparams* hp, orc_scaler* sc);
 
 /* Input recipe for the generator-driven driver: replica r's element j at
  * step s is cast16(zs_grad_value(spec with loss_scale = current S, s, r, j)),

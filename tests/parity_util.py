@@ -98,19 +98,36 @@ def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True):
         params = oracle.cast16(master, bf)
         assert np.array_equal(g.params_u16(), params), "initial working copy"
         stats = []
+        k_micro = wl.n_micro
         for step in range(1, wl.steps + 1):
             spec = synth.grad_spec(seed=wl.seed, sigma=wl.sigma, bias_sigma=wl.bias_sigma,
                                    loss_scale=sc.scale, outliers=wl.outliers, psi=wl.psi)
-            reps = [oracle.cast16(synth.grad_f32(wlen, wbase, spec, step, r), bf)
-                    for r in range(wl.n_ranks)]
-            if wl.inject is not None and wl.inject[0] == step:
-                _, r, e, bits = wl.inject
-                if wbase <= e < wbase + wlen:
-                    reps[r][e - wbase] = bits
-            g.gen_grads(step)
-            g.step(per_bucket=per_bucket)
+            # checker side: every micro-batch generated on the host, accumulated in fp32
+            acc = [np.empty(wlen, np.float32) for _ in range(wl.n_ranks)]
+            for mb in range(1, k_micro + 1):
+                key = wl.gen_step(step, mb)
+                reps = [oracle.cast16(synth.grad_f32(wlen, wbase, spec, key, r), bf)
+                        for r in range(wl.n_ranks)]
+                if mb == k_micro and wl.inject is not None and wl.inject[0] == step:
+                    _, r, e, bits = wl.inject
+                    if wbase <= e < wbase + wlen:
+                        reps[r][e - wbase] = bits
+                if k_micro > 1:
+                    for r in range(wl.n_ranks):
+                        oracle.accumulate(reps[r], acc[r], bf, first=(mb == 1))
+            # device side: the same micro-batches, the last one fused into the reduce
+            if k_micro > 1:
+                g.step_micro(step, per_bucket=per_bucket)
+            else:
+                g.gen_grads(step)
+                g.step(per_bucket=per_bucket)
             flags = np.zeros(max(p.n_buckets, 1), np.uint32)
-            oracle.step_arrays(p, lo, hi, bf, reps, wbase, master, m, v, params, hp, sc, flags)
+            if k_micro > 1:
+                oracle.step_arrays_f32(p, lo, hi, bf, acc, k_micro, wbase, master, m, v, params,
+                                       hp, sc, flags)
+            else:
+                oracle.step_arrays(p, lo, hi, bf, reps, wbase, master, m, v, params, hp, sc,
+                                   flags)
             if check_replicas and wlen:
                 assert np.array_equal(g.replicas_u16(), np.stack(reps)), "generator parity"
             dev = g.read_scaler()

@@ -220,3 +220,25 @@ def test_bounded_wait_times_out_without_fault():
     s = g.read_scaler()
     assert s.error == 0 and s.t == 1
     g.close()
+
+
+@pytest.mark.parametrize("k,two_pass,bf16,n", [(2, False, True, 8), (3, False, False, 4),
+                                              (2, True, True, 16), (4, True, False, 8),
+                                              (3, False, True, 64)])
+def test_micro_batch_accumulation(k, two_pass, bf16, n):
+    """k micro-batches accumulated in fp32 (zero_accumulate), the last one
+    added inside the reduce (zero_step_accum / zero_reduce_scatter_accum),
+    unscale 1/(S N k); fused and two-pass paths, against the checker."""
+    psi = n * 4096 * 2 + 77
+    wl = W.Workload("accum", [psi], n, 30_000, bf16, 41, 1e-3,
+                    init_scale=1.0 if bf16 else 1024.0, steps=3, n_micro=k,
+                    max_grad_norm=0.5 if two_pass else 0.0)
+    run_small(wl, two_pass=two_pass)
+
+
+def test_micro_batch_accumulation_overflow_in_last_micro_batch():
+    psi = 8 * 4096 + 5
+    wl = W.Workload("accum_inf", [psi], 8, 0, False, 42, 1e-4, init_scale=2048.0,
+                    dynamic_scale=True, steps=3, n_micro=3, inject=(2, 3, psi // 2, 0x7C00))
+    stats, dev, orc = run_small(wl)
+    assert dev.t == 2 and dev.scale == 1024.0
