@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--micro", type=int, default=1,
+                    help="micro-batches per optimizer step, accumulated in fp32 (>= 1)")
     ap.add_argument("--numel-cap", type=int, default=0,
                     help="run the workload's first N flat parameters only (small profiling case)")
     return ap.parse_args()
@@ -209,6 +211,8 @@ def run_libzero(args, rank, world, dist):
     wl = workload(args.workload)
     if args.numel_cap:
         wl = truncated(wl, args.numel_cap)
+    if args.micro > 1:
+        wl = wl.scaled(name="%s_micro%d" % (wl.name, args.micro), n_micro=args.micro)
     g = harness.Group(wl, device=dev)
     path = "two_pass" if g.two_pass else "fused"
     g.init_state()
@@ -225,15 +229,27 @@ def run_libzero(args, rank, world, dist):
     gp = g.ghat_ptrs() if g.two_pass else None
 
     # phases of one step (each a C-ABI call on stream st); for the fused path
-    # the update is one kernel launch per 128 segments
+    # the update is one kernel launch per 128 segments. With k micro-batches
+    # the first k - 1 are accumulated in fp32 and the last is added inside
+    # the reduce (the same replica buffer stands for every micro-batch).
+    k_micro = wl.n_micro
+    acc = g.accum_ptrs() if k_micro > 1 else None
+
     def phases():
+        pre = []
+        for mb in range(1, k_micro):
+            name = "accumulate_first" if mb == 1 else "accumulate"
+            pre.append((name, (lambda first: lambda: Z.zero_accumulate(
+                g.plan, lo, hi, reps, acc, g.wbase, first, st))(mb == 1)))
         if not g.two_pass:
-            return [("fused_update", lambda: Z.zero_step_update(
-                        g.plan, lo, hi, m, v, w, 2, None, reps, g.wbase, flat, g.hp, sc, fl, st)),
+            return pre + [("fused_update", lambda: Z.zero_step_update_accum(
+                        g.plan, lo, hi, m, v, w, 2, None, reps, acc, k_micro, g.wbase, flat, g.hp,
+                        sc, fl, st)),
                     ("finish", lambda: Z.zero_step_finish(
                         g.plan, lo, hi, m, 2, None, g.wbase, flat, g.hp, sc, st))]
-        out = [("reduce_scatter", lambda: Z.zero_reduce_scatter(
-                    g.plan, -1, lo, hi, reps, g.wbase, gp, sc, fl, ws if clip else 0, st))]
+        out = pre + [("reduce_scatter", lambda: Z.zero_reduce_scatter_accum(
+                    g.plan, -1, lo, hi, reps, acc, k_micro, g.wbase, gp, sc, fl,
+                    ws if clip else 0, st))]
         if clip:
             out.append(("grad_norm", lambda: Z.zero_grad_norm(g.plan, lo, hi, None, g.hp, sc, ws,
                                                               st)))
@@ -250,7 +266,8 @@ def run_libzero(args, rank, world, dist):
     L = -(-segs // 128)
     # fused: update + (re-cast check merged with bookkeeping); two-pass:
     # reduce + norm finish (2) + update + bookkeeping
-    launches_per_step = (2 * L) if not g.two_pass else (L + (2 if clip else 0) + L + 1)
+    launches_per_step = ((2 * L) if not g.two_pass else (L + (2 if clip else 0) + L + 1)) + \
+        (k_micro - 1)
 
     for _ in range(args.warmup):
         for _, f in ph:
@@ -259,7 +276,8 @@ def run_libzero(args, rank, world, dist):
 
     K = args.steps
     evs = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(K)] for name, _ in ph}
+                  for _ in range(K * max(1, k_micro))] for name, _ in ph}
+    ev_i = {name: 0 for name, _ in ph}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -278,7 +296,8 @@ def run_libzero(args, rank, world, dist):
     t0.record(g.stream)
     for k in range(K):
         for name, f in ph:
-            a, b = evs[name][k]
+            a, b = evs[name][ev_i[name]]
+            ev_i[name] += 1
             a.record(g.stream)
             f()
             b.record(g.stream)
@@ -289,7 +308,8 @@ def run_libzero(args, rank, world, dist):
     if dist:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    phase_ms = {name: statistics.mean(a.elapsed_time(b) for a, b in evs[name]) for name, _ in ph}
+    phase_ms = {name: statistics.mean(a.elapsed_time(b) for a, b in evs[name][:ev_i[name]])
+                for name, _ in ph}
 
     total_ms = max_over_ranks(dist, total_ms)
     ms_per_step = total_ms / K
@@ -298,15 +318,23 @@ def run_libzero(args, rank, world, dist):
 
     # roofline of the dominant kernel
     peak, peak_kind = peaks()
-    bytes_per_param = {"fused_update": 2 * N + 26, "reduce_scatter": 2 * N + 4,
-                       "update": 30, "grad_norm": 0, "finish": 0}
+    extra = 4 * N if k_micro > 1 else 0  # fp32 accumulators read by the reduce
+    bytes_per_param = {"fused_update": 2 * N + 26 + extra, "reduce_scatter": 2 * N + 4 + extra,
+                       "update": 30, "grad_norm": 0, "finish": 0,
+                       "accumulate_first": 6 * N, "accumulate": 10 * N}
     dom = max((n for n, _ in ph if bytes_per_param[n] > 0), key=lambda n: phase_ms[n])
     alg_bytes = bytes_per_param[dom] * pstep
     achieved = alg_bytes / (phase_ms[dom] / 1e3) / 1e9
     kernel_name = {"fused_update": "bulk_kernel<kFused>", "reduce_scatter": "bulk_kernel<kReduce>",
-                   "update": "bulk_kernel<kUpdate>"}[dom]
+                   "update": "bulk_kernel<kUpdate>", "accumulate": "accumulate_kernel",
+                   "accumulate_first": "accumulate_kernel"}[dom]
+    if k_micro > 1 and dom in ("fused_update", "reduce_scatter"):
+        kernel_name = kernel_name[:-1] + ", accumulators>"
+    kernel_gbs = {n: round(bytes_per_param[n] * pstep / (phase_ms[n] / 1e3) / 1e9, 1)
+                  for n, _ in ph if bytes_per_param[n] > 0}
     traffic = profiled_traffic(kernel_name, wl.name)
-    step_bytes = (2 * N + (34 if g.two_pass else 26)) * pstep
+    step_bytes = (2 * N + (34 if g.two_pass else 26) + extra
+                  + (6 * N + 10 * N * (k_micro - 2) if k_micro > 1 else 0)) * pstep
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_kind": peak_kind + " (copy bandwidth, burst)",
@@ -316,7 +344,8 @@ def run_libzero(args, rank, world, dist):
                 "step_achieved_gbs": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
                 "step_frac": round(step_bytes / (ms_per_step / 1e3) / 1e9 / peak, 4),
                 "north_star_frac_2n26": round((2 * N + 26) * pstep / (ms_per_step / 1e3) / 1e9
-                                              / peak, 4)}
+                                              / peak, 4),
+                "kernel_gbs": kernel_gbs}
 
     # end to end through the C ABI: every step copies that step's replicas from
     # pinned host memory and reads the updated parameters and the scaler back.
@@ -351,13 +380,15 @@ def run_libzero(args, rank, world, dist):
         h2d[0].wait_stream(h2d[1])
         landed[b].record(h2d[0])
 
-    def step_on(b):
-        rp, fp = rep_ptrs[b], dev_flat[b].data_ptr()
+    def step_on(b, p):
+        """Last micro-batch of a step: replicas in buffer b, parameters into buffer p."""
+        rp, fp = rep_ptrs[b], dev_flat[p].data_ptr()
         if not g.two_pass:
-            Z.zero_step(g.plan, lo, hi, m, v, w, 2, None, rp, g.wbase, fp, g.hp, sc, fl, st)
+            Z.zero_step_accum(g.plan, lo, hi, m, v, w, 2, None, rp, acc, k_micro, g.wbase, fp,
+                              g.hp, sc, fl, st)
         else:
-            Z.zero_reduce_scatter(g.plan, -1, lo, hi, rp, g.wbase, gp, sc, fl, ws if clip else 0,
-                                  st)
+            Z.zero_reduce_scatter_accum(g.plan, -1, lo, hi, rp, acc, k_micro, g.wbase, gp, sc, fl,
+                                        ws if clip else 0, st)
             if clip:
                 Z.zero_grad_norm(g.plan, lo, hi, None, g.hp, sc, ws, st)
             Z.zero_step(g.plan, lo, hi, m, v, w, 1, gp, None, g.wbase, fp, g.hp, sc, fl, st)
@@ -372,27 +403,36 @@ def run_libzero(args, rank, world, dist):
     h2d[0].wait_event(e0)
     h2d[1].wait_event(e0)
     copy_in(0)
-    for k in range(E):
-        b = k % 2
-        if k + 1 < E:
+    # one slot per micro-batch: every micro-batch's replicas cross the host
+    # link; the first k - 1 are accumulated, the last one completes the step
+    slots = E * k_micro
+    for j in range(slots):
+        b = j % 2
+        if j + 1 < slots:
             copy_in(1 - b)
         g.stream.wait_event(landed[b])
-        g.stream.wait_event(read_back[b])   # parameters buffer b free again
-        step_on(b)
+        mb = j % k_micro + 1
+        if mb < k_micro:
+            Z.zero_accumulate(g.plan, lo, hi, rep_ptrs[b], acc, g.wbase, 1 if mb == 1 else 0, st)
+            computed[b].record(g.stream)
+            continue
+        p = (j // k_micro) % 2
+        g.stream.wait_event(read_back[p])   # parameters buffer p free again
+        step_on(b, p)
         with torch.cuda.stream(g.stream):
-            scaler_snap[b].copy_(g.scaler, non_blocking=True)  # this step's scaler
+            scaler_snap[p].copy_(g.scaler, non_blocking=True)  # this step's scaler
         computed[b].record(g.stream)
         with torch.cuda.stream(d2h):
             d2h.wait_event(computed[b])
-            host_params[b].copy_(dev_flat[b], non_blocking=True)
-            host_scaler[b].copy_(scaler_snap[b], non_blocking=True)
-        read_back[b].record(d2h)
+            host_params[p].copy_(dev_flat[p], non_blocking=True)
+            host_scaler[p].copy_(scaler_snap[p], non_blocking=True)
+        read_back[p].record(d2h)
     g.stream.wait_stream(d2h)
     e1.record(g.stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
     e2e = {"value": round(job_throughput(pstep, E, world, e2e_ms), 4), "unit": UNIT,
-           "steps": E, "h2d_bytes_per_step": int(g.replicas.numel() * 2),
+           "steps": E, "h2d_bytes_per_step": int(g.replicas.numel() * 2 * k_micro),
            "d2h_bytes_per_step": int(g.flat.numel() * 2 + g.scaler.numel()),
            "pipelined": "two replica and parameter buffers; H2D of step k+1 overlaps step k"}
     del dev_reps, host_reps

@@ -79,7 +79,8 @@ struct Seg {
 // stage i carries the replica chunks of ring positions [r_lo[i], r_hi[i])
 // and, when states[i] is set, the state block (kFused: master, m, v;
 // kUpdate: g, master, m, v) after them.
-constexpr int kMaxStagePlan = 8;
+// 64 ranks with fp32 accumulators need 13 replica stages plus one state stage
+constexpr int kMaxStagePlan = 16;
 struct StagePlan {
   int32_t n;
   int16_t r_lo[kMaxStagePlan], r_hi[kMaxStagePlan];
@@ -1357,7 +1358,7 @@ int grid_size() {
 
 // Greedy packing of one element range's chunks (range of E elements) into
 // stages of at most kStageBudget bytes: replica chunks (2 bytes per element
-// each) in ring order, then the indivisible state block (kFused 12, kUpdate
+// each, 6 with the fp32 accumulator beside it) in ring order, then the indivisible state block (kFused 12, kUpdate
 // 16 bytes per element) in the last stage if it fits, else in a stage of
 // its own.
 inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
@@ -1368,8 +1369,13 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
   const int state_bpe = mode == kFused ? 12 : (mode == kUpdate ? 16 : 0);
   int lo = 0, cur = 0;
   int max_bpe = 0;
+  bool overflow = false;
   auto close = [&](int hi, int with_states) {
     const int bpe = rep_bytes * (hi - lo) + (with_states ? state_bpe : 0);
+    if (pl.n >= kMaxStagePlan) {  // reported through n = 0 below
+      overflow = true;
+      return;
+    }
     pl.r_lo[pl.n] = static_cast<int16_t>(lo);
     pl.r_hi[pl.n] = static_cast<int16_t>(hi);
     pl.states[pl.n] = with_states;
@@ -1393,6 +1399,7 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
   } else if (cur > 0) {
     close(n_rep, 0);
   }
+  if (overflow) pl.n = 0;
   *slot_bytes = static_cast<uint32_t>((max_bpe * E + 127) & ~127);
   return pl;
 }
