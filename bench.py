@@ -326,10 +326,10 @@ def run_libzero(args, rank, world, dist):
     alg_bytes = bytes_per_param[dom] * pstep
     achieved = alg_bytes / (phase_ms[dom] / 1e3) / 1e9
     kernel_name = {"fused_update": "bulk_kernel<kFused>", "reduce_scatter": "bulk_kernel<kReduce>",
-                   "update": "bulk_kernel<kUpdate>", "accumulate": "accumulate_kernel",
-                   "accumulate_first": "accumulate_kernel"}[dom]
+                   "update": "bulk_kernel<kUpdate>", "accumulate": "accumulate_kernel:add",
+                   "accumulate_first": "accumulate_kernel:first"}[dom]
     if k_micro > 1 and dom in ("fused_update", "reduce_scatter"):
-        kernel_name = kernel_name[:-1] + ", accumulators>"
+        kernel_name = kernel_name[:-1] + ",acc>"
     kernel_gbs = {n: round(bytes_per_param[n] * pstep / (phase_ms[n] / 1e3) / 1e9, 1)
                   for n, _ in ph if bytes_per_param[n] > 0}
     traffic = profiled_traffic(kernel_name, wl.name)

@@ -1869,38 +1869,69 @@ struct AccArgs {
   float* acc[ZERO_MAX_RANKS];
   int64_t off, len;  // window elements [off, off + len) of every replica
   int32_t n_ranks, first;
-  int32_t vec;       // 1: off is on the 8-element grid (16-byte vectors)
+  int32_t vec;       // 1: off is on the 4-element grid (8- and 16-byte vectors)
   int32_t pad;
 };
 
+// Quads (4 elements) in flight per thread: eight 8-byte loads (and, after
+// the first micro-batch, eight 16-byte accumulator loads) are issued before
+// the first store, which the write-heavy first pass needs to keep HBM busy.
+constexpr int kAccQuads = 8;
+constexpr int kAccThreads = 256;
+
 template <bool kBf16>
-__global__ void __launch_bounds__(256) accumulate_kernel(const __grid_constant__ AccArgs a) {
-  const int64_t nvec = a.vec ? (a.len >> 3) : 0;
-  const int64_t total = nvec * a.n_ranks;
+__device__ __forceinline__ float4 widen4(const uint2& w) {
+  return make_float4(widen<kBf16>(w.x & 0xFFFFu), widen<kBf16>(w.x >> 16),
+                     widen<kBf16>(w.y & 0xFFFFu), widen<kBf16>(w.y >> 16));
+}
+
+// grid: x strides over one replica's window, y = replica
+template <bool kBf16>
+__global__ void __launch_bounds__(kAccThreads)
+    accumulate_kernel(const __grid_constant__ AccArgs a) {
+  const int r = blockIdx.y;
+  const uint16_t* src = a.micro[r] + a.off;
+  float* dst = a.acc[r] + a.off;
+  const int64_t nq = a.vec ? (a.len >> 2) : 0;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
-       q += stride) {
-    const int r = static_cast<int>(q / nvec);
-    const int64_t j = a.off + ((q - static_cast<int64_t>(r) * nvec) << 3);
-    float x[8];
-    widen8<kBf16>(__ldcs(reinterpret_cast<const uint4*>(a.micro[r] + j)), x);
-    float* dst = a.acc[r] + j;
-    if (!a.first) {
-      float y[8];
-      load8f(dst, y);
+  const uint2* src4 = reinterpret_cast<const uint2*>(src);
+  float4* dst4 = reinterpret_cast<float4*>(dst);
+  for (int64_t q0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q0 < nq;
+       q0 += stride * kAccQuads) {
+    uint2 w[kAccQuads];
+    float4 y[kAccQuads];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(y[e], x[e]);
+    for (int u = 0; u < kAccQuads; ++u) {
+      const int64_t q = q0 + u * stride;
+      if (q < nq) w[u] = __ldcs(src4 + q);
     }
-    store8f(dst, x);
+    if (!a.first) {
+#pragma unroll
+      for (int u = 0; u < kAccQuads; ++u) {
+        const int64_t q = q0 + u * stride;
+        if (q < nq) y[u] = __ldcs(dst4 + q);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAccQuads; ++u) {
+      const int64_t q = q0 + u * stride;
+      if (q < nq) {
+        float4 x = widen4<kBf16>(w[u]);
+        if (!a.first) {
+          x.x = __fadd_rn(y[u].x, x.x);
+          x.y = __fadd_rn(y[u].y, x.y);
+          x.z = __fadd_rn(y[u].z, x.z);
+          x.w = __fadd_rn(y[u].w, x.w);
+        }
+        __stcs(dst4 + q, x);
+      }
+    }
   }
-  // ragged tail of each replica's window
-  const int64_t tail = a.len - (nvec << 3);
-  for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-       q < tail * a.n_ranks; q += stride) {
-    const int r = static_cast<int>(q / tail);
-    const int64_t j = a.off + (nvec << 3) + (q - static_cast<int64_t>(r) * tail);
-    const float x = widen<kBf16>(a.micro[r][j]);
-    a.acc[r][j] = a.first ? x : __fadd_rn(a.acc[r][j], x);
+  // ragged tail of the window (or all of it when off is off the grid)
+  for (int64_t j = (nq << 2) + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       j < a.len; j += stride) {
+    const float x = widen<kBf16>(src[j]);
+    dst[j] = a.first ? x : __fadd_rn(dst[j], x);
   }
 }
 
@@ -1925,9 +1956,10 @@ extern "C" ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, 
   a->len = static_cast<int64_t>(rank_hi - rank_lo) * S;
   a->n_ranks = N;
   a->first = first ? 1 : 0;
-  // the vector body needs the window offset on the 8-element grid of both
-  // arrays; otherwise the whole window takes the element-wise loop
-  a->vec = (a->off & 7) == 0 ? 1 : 0;
+  // the vector body needs the window offset on the 4-element grid of both
+  // arrays (8-byte source, 16-byte accumulator vectors); otherwise the whole
+  // window takes the element-wise loop
+  a->vec = (a->off & 3) == 0 ? 1 : 0;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -1937,10 +1969,12 @@ extern "C" ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, 
   rc = ZERO_OK;
   if (a->len > 0) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // about 8 CTAs per SM in all, split evenly over the replicas
+    const dim3 grid(static_cast<unsigned>(std::max(1, sms * 8 / N)), static_cast<unsigned>(N));
     if (plan->info.grad_dtype == ZERO_BF16)
-      accumulate_kernel<true><<<sms * 8, 256, 0, st>>>(*a);
+      accumulate_kernel<true><<<grid, kAccThreads, 0, st>>>(*a);
     else
-      accumulate_kernel<false><<<sms * 8, 256, 0, st>>>(*a);
+      accumulate_kernel<false><<<grid, kAccThreads, 0, st>>>(*a);
     if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
   }
   delete a;
