@@ -57,6 +57,23 @@ class GradSpec(C.Structure):
                 ("loss_scale", C.c_float), ("outliers", C.c_int32), ("psi", C.c_int64)]
 
 
+class Unit(C.Structure):
+    _fields_ = [("psi", C.c_int64), ("pad", C.c_int64), ("psi_pad", C.c_int64),
+                ("shard", C.c_int64), ("shard_offset", C.c_int64), ("flat_offset", C.c_int64),
+                ("n_tensors", C.c_int32), ("first_slot", C.c_int32)]
+
+
+class UnitPlan(C.Structure):
+    _fields_ = [("psi", C.c_int64), ("psi_pad", C.c_int64), ("shard", C.c_int64),
+                ("max_unit_psi_pad", C.c_int64), ("n_units", C.c_int32),
+                ("n_ranks", C.c_int32), ("n_tensors", C.c_int32), ("align_elems", C.c_int32),
+                ("persistent_bytes", C.c_double), ("peak_one_bytes", C.c_double),
+                ("peak_two_bytes", C.c_double), ("peak_backward_bytes", C.c_double),
+                ("max_unit_fraction", C.c_double), ("comm_elems", C.c_double),
+                ("comm_bytes", C.c_double), ("ring_bytes", C.c_double),
+                ("n_gathers", C.c_int32), ("reserved", C.c_int32)]
+
+
 class Gen(C.Structure):
     _fields_ = [("spec", GradSpec), ("is_bf16", C.c_int32), ("inject_step", C.c_int32),
                 ("inject_rank", C.c_int32), ("inject_bits", C.c_uint32),
@@ -117,6 +134,12 @@ def lib():
         L.orc_gen_ghat.argtypes = [P(Plan), P(Gen), C.c_uint32, C.c_float, C.c_void_p,
                                    C.c_int64, C.c_void_p]
         L.orc_gen_ghat.restype = C.c_int
+        L.orc_unit_plan_make.argtypes = [P(C.c_int64), C.c_int32, P(C.c_int32), C.c_int32,
+                                         C.c_int32, C.c_int32, P(UnitPlan), P(Unit),
+                                         P(C.c_int32), P(C.c_int64)]
+        L.orc_unit_plan_make.restype = C.c_int
+        L.orc_gather_unit.argtypes = [P(Unit), C.c_int32, C.c_void_p, C.c_void_p]
+        L.orc_shard_unit.argtypes = [P(Unit), C.c_int32, C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -292,3 +315,51 @@ def gen_ghat(plan, g, step, scale, elems):
     if rc != 0:
         raise ValueError("orc_gen_ghat failed")
     return out
+
+
+# ------------------------------------------------------ stage-3 FSDP units ----
+
+def make_unit_plan(numels, unit_of_tensor, n_units, n_ranks, align_elems=1):
+    """Returns (UnitPlan, [Unit], slot_tensor ndarray, tensor_offset ndarray)."""
+    L = lib()
+    arr = np.ascontiguousarray(np.asarray(numels, dtype=np.int64))
+    uot = np.ascontiguousarray(np.asarray(unit_of_tensor, dtype=np.int32))
+    if len(arr) != len(uot):
+        raise ValueError("numels and unit_of_tensor differ in length")
+    units = (Unit * max(n_units, 1))()
+    slots = np.zeros(max(len(arr), 1), dtype=np.int32)
+    offs = np.zeros(max(len(arr), 1), dtype=np.int64)
+    p = UnitPlan()
+    rc = L.orc_unit_plan_make(arr.ctypes.data_as(C.POINTER(C.c_int64)), len(arr),
+                              uot.ctypes.data_as(C.POINTER(C.c_int32)), n_units, n_ranks,
+                              align_elems, C.byref(p), units,
+                              slots.ctypes.data_as(C.POINTER(C.c_int32)),
+                              offs.ctypes.data_as(C.POINTER(C.c_int64)))
+    if rc != 0:
+        raise ValueError("orc_unit_plan_make failed: %d" % rc)
+    return p, list(units)[:n_units], slots[:len(arr)], offs[:len(arr)]
+
+
+def _ptr_array(arrays):
+    ptrs = (C.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+    return ptrs
+
+
+def gather_unit(unit, shards):
+    """All-gather of one unit from the N ranks' 16-bit shard buffers."""
+    for a in shards:
+        assert a.dtype == np.uint16 and a.flags.c_contiguous
+        assert a.size >= unit.shard_offset + unit.shard
+    full = np.empty(unit.psi_pad, dtype=np.uint16)
+    lib().orc_gather_unit(C.byref(unit), len(shards), _ptr_array(shards), _ptr(full))
+    return full
+
+
+def shard_unit(unit, full, shards):
+    """Write one gathered unit's slices into the N ranks' shard buffers."""
+    full = np.ascontiguousarray(full, dtype=np.uint16)
+    assert full.size == unit.psi_pad
+    for a in shards:
+        assert a.dtype == np.uint16 and a.flags.c_contiguous
+        assert a.size >= unit.shard_offset + unit.shard
+    lib().orc_shard_unit(C.byref(unit), len(shards), _ptr(full), _ptr_array(shards))

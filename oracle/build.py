@@ -1,6 +1,6 @@
 """Build the CPU checker library (test infrastructure only).
 
-Compiles oracle.c with gcc into oracle/_build/liboracle.so. Flags: -O2,
+Compiles oracle.c and units.c with gcc into oracle/_build/liboracle.so. Flags: -O2,
 -ffp-contract=off and no fast-math, so every C statement of the checker is one
 IEEE operation rounded to nearest-even (gcc would otherwise fuse multiply-adds
 on Arm hosts).
@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 SYNTH_DIR = os.path.join(ROOT, "fsdp_sharded_mixed_shard_gb300", "synth")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboracle.so")
-SOURCES = [os.path.join(HERE, "oracle.c")]
+SOURCES = [os.path.join(HERE, "oracle.c"), os.path.join(HERE, "units.c")]
 HEADERS = [os.path.join(HERE, "oracle.h"), os.path.join(SYNTH_DIR, "synth.h")]
 
 CFLAGS = ["-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fno-fast-math",

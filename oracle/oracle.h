@@ -224,6 +224,73 @@ int orc_gen_step(const orc_plan* p, int32_t rank_lo, int32_t rank_hi, const orc_
 int orc_gen_ghat(const orc_plan* p, const orc_gen* g, uint32_t step, float scale,
                  const int64_t* elems, int64_t n_elems, float* ghat);
 
+/* -------------------------------------------------- stage-3 FSDP units ---- */
+
+typedef struct orc_unit {
+  int64_t psi;          /* parameters of the unit's tensors */
+  int64_t pad;          /* zeros appended so that psi_pad is a multiple of N * align */
+  int64_t psi_pad;
+  int64_t shard;        /* psi_pad / N: elements of the unit each rank holds */
+  int64_t shard_offset; /* where the unit's slice starts in every rank's shard buffer */
+  int64_t flat_offset;  /* where the padded unit starts in the concatenation of all units */
+  int32_t n_tensors;    /* tensors of the unit */
+  int32_t first_slot;   /* its first entry in slot_tensor */
+} orc_unit;
+
+typedef struct orc_unit_plan {
+  int64_t psi;          /* all parameters */
+  int64_t psi_pad;      /* sum of the units' psi_pad */
+  int64_t shard;        /* elements each rank holds: sum of the units' shard */
+  int64_t max_unit_psi_pad;
+  int32_t n_units, n_ranks, n_tensors, align_elems;
+  /* per-rank bytes, K = 12 (16 bytes per held element) */
+  double persistent_bytes;     /* 16 * shard */
+  double peak_one_bytes;       /* persistent + one gathered unit (2 bytes per element) */
+  double peak_two_bytes;       /* persistent + two adjacent gathered units (prefetch) */
+  double peak_backward_bytes;  /* persistent + one unit's parameters and full gradient */
+  double max_unit_fraction;    /* largest unit's psi / psi */
+  /* wire per rank per step */
+  double comm_elems;           /* 3 psi_pad: two all-gathers and one reduce-scatter */
+  double comm_bytes;           /* 2 bytes per element of comm_elems */
+  double ring_bytes;           /* ring collectives: 3 (N-1) shard elements of 2 bytes */
+  int32_t n_gathers;           /* 2 per unit: forward and backward */
+  int32_t reserved;
+} orc_unit_plan;
+
+/* Per-unit flatten, pad and shard of a tensor list for stage 3.
+ * [ZF] "FSDP: the same idea, one unit at a time" (each unit's parameters are
+ * flattened and sharded; peak = sharded states + one or two gathered units);
+ * [Z3] "Just-in-time all-gather: how the weights reappear" (units of one
+ * layer, gathered before the layer's forward and again before its backward)
+ * and "Peak transient memory" (peak = persistent 16 psi / N + one layer's
+ * full parameters + activations; activations need a model and are left out);
+ * [SB] "What does each stage cost on the wire?" (stage 3 moves 3 psi).
+ * unit_of_tensor[k] in [0, n_units) names tensor k's unit; a unit's tensors
+ * keep their list order and every unit needs at least one. Unit u is padded
+ * with zeros to a multiple of N * align_elems and rank r holds its elements
+ * [r S_u, (r+1) S_u); a rank's shard buffer is its slices of units 0..U-1 in
+ * order. Units are numbered in forward order; the two-unit peak takes the
+ * largest pair of adjacent units (the next unit prefetched while one runs).
+ * units: n_units entries or NULL; slot_tensor: n_tensors entries or NULL
+ * (tensor ids unit by unit); tensor_offset: n_tensors entries or NULL
+ * (offset of tensor k inside its gathered unit). Returns 0 or -1. */
+int orc_unit_plan_make(const int64_t* numels, int32_t n_tensors, const int32_t* unit_of_tensor,
+                       int32_t n_units, int32_t n_ranks, int32_t align_elems,
+                       orc_unit_plan* out, orc_unit* units, int32_t* slot_tensor,
+                       int64_t* tensor_offset);
+
+/* The all-gather of one unit ([Z3] "Just-in-time all-gather": every rank
+ * reconstructs the layer's full parameters): full[r S_u + j] =
+ * shards[r][shard_offset_u + j] for every rank r and j < S_u. */
+void orc_gather_unit(const orc_unit* u, int32_t n_ranks, const uint16_t* const* shards,
+                     uint16_t* full);
+
+/* The inverse: rank r keeps full[r S_u .. (r+1) S_u) at shard_offset_u of its
+ * shard buffer ([ZF] "FSDP: the same idea, one unit at a time": the unit's
+ * flattened parameters are sharded across the GPUs). */
+void orc_shard_unit(const orc_unit* u, int32_t n_ranks, const uint16_t* full,
+                    uint16_t* const* shards);
+
 #ifdef __cplusplus
 }
 #endif
