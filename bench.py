@@ -54,6 +54,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--micro", type=int, default=1,
                     help="micro-batches per optimizer step, accumulated in fp32 (>= 1)")
+    ap.add_argument("--gather", action="store_true",
+                    help="time the stage-3 unit all-gather (forward and backward gathers of "
+                         "every unit) on the 8.81B-parameter layout at 64 ranks instead")
+    ap.add_argument("--units-align", type=int, default=1,
+                    help="unit padding grain in elements for --gather (1: multiple of N)")
     ap.add_argument("--numel-cap", type=int, default=0,
                     help="run the workload's first N flat parameters only (small profiling case)")
     return ap.parse_args()
@@ -97,19 +102,19 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha():
-    p = os.path.join(ROOT, "fsdp_sharded_mixed_shard_gb300", "csrc", "zero_kernels.cu")
+def kernel_source_sha(source="zero_kernels.cu"):
+    p = os.path.join(ROOT, "fsdp_sharded_mixed_shard_gb300", "csrc", source)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
-def profiled_traffic(kernel, wl_name):
+def profiled_traffic(kernel, wl_name, source="zero_kernels.cu"):
     """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
     the current kernel source (line: `traffic: kernel=<k> workload=<w>
     bytes_per_launch=<b> source_sha=<sha>`); otherwise None."""
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(source)
     pat = re.compile(r"traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=([0-9.eE+]+)"
                      r"\s+source_sha=(\w+)")
     for f in sorted(os.listdir(d)):
@@ -178,6 +183,15 @@ class ClockSampler:
                 "sm_max_mhz": max(r[1] for r in rows),
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows),
                 "reasons": sorted(reasons)}
+
+
+def device_uuid(dev):
+    import torch
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if not uuid or uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        return None
 
 
 # --------------------------------------------------------- multi-GPU glue ----
@@ -279,14 +293,7 @@ def run_libzero(args, rank, world, dist):
                   for _ in range(K * max(1, k_micro))] for name, _ in ph}
     ev_i = {name: 0 for name, _ in ph}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        if uuid and not uuid.startswith("GPU-"):
-            uuid = "GPU-" + uuid
-    except Exception:
-        uuid = None
-    clocks = ClockSampler(uuid)
+    clocks = ClockSampler(device_uuid(dev))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -452,6 +459,95 @@ def run_libzero(args, rank, world, dist):
     return line
 
 
+# ------------------------------------------------ stage-3 unit all-gather ----
+
+GATHER_METRIC = "stage-3 unit all-gather Gparams/s (forward + backward gathers of every unit)"
+
+
+def run_gather(args, rank, world, dist):
+    """One step = the all-gathers of stage 3 on one rank's view: every unit
+    gathered before its forward (units 0..U-1) and again before its backward
+    (U-1..0), one call per unit into a ring of two unit buffers. Each
+    gathered element moves 4 bytes (2 read from a shard, 2 written)."""
+    import torch
+    from fsdp_sharded_mixed_shard_gb300 import harness, workloads as W
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    uw = W.stage3_8p81b_units(64, args.units_align)
+    if args.numel_cap:
+        # a small case with the same unit sizes: the first units (root + blocks)
+        # whose parameters fit the cap, at least two
+        k, tot = 0, 0
+        while k < uw.n_units and (k < 2 or tot + uw.numels[k] <= args.numel_cap):
+            tot += uw.numels[k]
+            k += 1
+        uw = W.UnitWorkload(uw.name + "_first%d" % k, uw.numels[:k], list(range(k)), k,
+                            uw.n_ranks, uw.align_elems, uw.seed)
+    g = harness.UnitGroup(uw, device=dev, window=2)
+    g.fill_shards()
+    U = uw.n_units
+    order = list(range(U)) + list(reversed(range(U)))
+    calls = [(u, i % 2) for i, u in enumerate(order)]
+    gathered = 2 * g.info.psi_pad
+    for _ in range(args.warmup):
+        for u, slot in calls:
+            g.gather(u, u + 1, slot)
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in calls] for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device_uuid(dev))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0.record(g.stream)
+    for k in range(K):
+        for (u, slot), (a, b) in zip(calls, evs[k]):
+            a.record(g.stream)
+            g.gather(u, u + 1, slot)
+            b.record(g.stream)
+    t1.record(g.stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = max_over_ranks(dist, t0.elapsed_time(t1))
+    ms_per_step = total_ms / K
+    # per-unit launch durations of the block units (the root unit differs in size)
+    block = [i for i, (u, _) in enumerate(calls) if g.units[u].psi_pad == g.info.max_unit_psi_pad]
+    blk_ms = statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(K)
+                             for i in block)
+    peak, peak_kind = peaks()
+    unit_bytes = 4 * g.info.max_unit_psi_pad
+    achieved = unit_bytes / (blk_ms / 1e3) / 1e9
+    # one launch per call (64 slices, at most 256 per launch) for a non-empty unit
+    launches = sum(1 for u, _ in calls if g.units[u].shard_elems)
+    traffic = profiled_traffic("copy_kernel", uw.name, "gather.cu")
+    line = {"metric": GATHER_METRIC, "value": round(gathered * K * world / (total_ms / 1e3) / 1e9, 4),
+            "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic: seeded generator bf16 "
+            "patterns in every shard",
+            "config": {"workload": uw.name, "n_units": U, "n_ranks": 64,
+                       "align_elems": uw.align_elems, "psi": g.info.psi,
+                       "psi_pad": g.info.psi_pad, "block_unit_elems": g.info.max_unit_psi_pad,
+                       "gathers_per_step": len(calls),
+                       "l2": "inputs larger than L2 (%.1f GB of shards)" % (2 * g.info.psi_pad / 1e9)},
+            "roofline": {"bound": "hbm", "kernel": "copy_kernel", "achieved": round(achieved, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_kind": peak_kind + " (copy bandwidth, burst)", "traffic": traffic,
+                         "algorithmic_bytes_per_launch": unit_bytes,
+                         "kernel_ms": round(blk_ms, 5),
+                         "step_achieved_gbs": round(4 * gathered / (ms_per_step / 1e3) / 1e9, 1),
+                         "step_frac": round(4 * gathered / (ms_per_step / 1e3) / 1e9 / peak, 4)},
+            "e2e": None, "gpu_launches": launches * K, "clocks": clk}
+    g.close()
+    return line
+
+
 # ---------------------------------------------------------- CPU checker ----
 
 def truncated(wl, n_elems):
@@ -562,6 +658,14 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
+    if args.gather:
+        line = run_gather(args, rank, world, dist)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
     line = run_libzero(args, rank, world, dist)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:

@@ -21,12 +21,16 @@ __all__ = [
     "zero_cast_params", "zero_accumulate", "zero_reduce_scatter_accum", "zero_step_accum",
     "zero_step_update_accum", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
     "zero_version", "lib",
+    "ZeroUnit", "ZeroUnitPlanInfo", "ZERO_UNIT_MAX_ALIGN", "zero_unit_plan_create",
+    "zero_unit_plan_destroy", "zero_unit_plan_get_info", "zero_unit_plan_units",
+    "zero_unit_plan_tensors", "zero_gather_units", "zero_shard_units",
 ]
 
 ZERO_BF16 = 0
 ZERO_FP16 = 1
 ZERO_MAX_RANKS = 64
 ZERO_TILE_ELEMS = 4096
+ZERO_UNIT_MAX_ALIGN = 4096
 
 
 class ZeroError(RuntimeError):
@@ -66,6 +70,24 @@ class ZeroScaler(C.Structure):
                 ("norm", C.c_double), ("clip_coef", C.c_float), ("clip_apply", C.c_int32),
                 ("norm_step", C.c_int32), ("n_skipped", C.c_int32), ("error", C.c_int32),
                 ("finish_count", C.c_uint32)]
+
+
+class ZeroUnit(C.Structure):
+    """zero_units.h zero_unit: one stage-3 FSDP unit of a unit plan."""
+    _fields_ = [("psi", C.c_int64), ("pad", C.c_int64), ("psi_pad", C.c_int64),
+                ("shard_elems", C.c_int64), ("shard_offset", C.c_int64),
+                ("flat_offset", C.c_int64), ("n_tensors", C.c_int32), ("first_slot", C.c_int32)]
+
+
+class ZeroUnitPlanInfo(C.Structure):
+    _fields_ = [("psi", C.c_int64), ("psi_pad", C.c_int64), ("shard_elems", C.c_int64),
+                ("max_unit_psi_pad", C.c_int64), ("n_units", C.c_int32), ("n_ranks", C.c_int32),
+                ("n_tensors", C.c_int32), ("align_elems", C.c_int32),
+                ("persistent_bytes", C.c_double), ("peak_one_bytes", C.c_double),
+                ("peak_two_bytes", C.c_double), ("peak_backward_bytes", C.c_double),
+                ("max_unit_fraction", C.c_double), ("comm_elems", C.c_double),
+                ("comm_bytes", C.c_double), ("ring_bytes", C.c_double),
+                ("n_gathers", C.c_int32), ("reserved", C.c_int32)]
 
 
 _lib = None
@@ -117,6 +139,15 @@ def lib():
         L.zero_strerror.argtypes = [C.c_int]
         L.zero_strerror.restype = C.c_char_p
         L.zero_version.argtypes = []
+        L.zero_unit_plan_create.argtypes = [_P(C.c_int64), C.c_int32, _P(C.c_int32), C.c_int32,
+                                            C.c_int32, C.c_int32, _P(_VP)]
+        L.zero_unit_plan_destroy.argtypes = [_VP]
+        L.zero_unit_plan_destroy.restype = None
+        L.zero_unit_plan_get_info.argtypes = [_VP, _P(ZeroUnitPlanInfo)]
+        L.zero_unit_plan_units.argtypes = [_VP, _P(ZeroUnit), C.c_int32]
+        L.zero_unit_plan_tensors.argtypes = [_VP, _P(C.c_int32), _P(C.c_int64), C.c_int32]
+        L.zero_gather_units.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _VP]
+        L.zero_shard_units.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _VP]
         _lib = L
     return _lib
 
@@ -282,3 +313,53 @@ def zero_strerror(status):
 
 def zero_version():
     return lib().zero_version()
+
+
+# ------------------------------------------------------ stage-3 FSDP units ----
+
+def zero_unit_plan_create(numels, unit_of_tensor, n_units, n_ranks, align_elems=1):
+    if len(numels) != len(unit_of_tensor):
+        raise ValueError("numels and unit_of_tensor differ in length")
+    n = len(numels)
+    arr = (C.c_int64 * max(n, 1))(*[int(x) for x in numels])
+    uot = (C.c_int32 * max(n, 1))(*[int(x) for x in unit_of_tensor])
+    out = _VP()
+    _check("zero_unit_plan_create", lib().zero_unit_plan_create(
+        arr, n, uot, n_units, n_ranks, align_elems, C.byref(out)))
+    return out
+
+
+def zero_unit_plan_destroy(plan):
+    lib().zero_unit_plan_destroy(plan)
+
+
+def zero_unit_plan_get_info(plan):
+    info = ZeroUnitPlanInfo()
+    _check("zero_unit_plan_get_info", lib().zero_unit_plan_get_info(plan, C.byref(info)))
+    return info
+
+
+def zero_unit_plan_units(plan):
+    n = zero_unit_plan_get_info(plan).n_units
+    out = (ZeroUnit * n)()
+    _check("zero_unit_plan_units", lib().zero_unit_plan_units(plan, out, n))
+    return list(out)
+
+
+def zero_unit_plan_tensors(plan):
+    """(slot_tensor, tensor_offset) as lists."""
+    n = zero_unit_plan_get_info(plan).n_tensors
+    slots = (C.c_int32 * n)()
+    offs = (C.c_int64 * n)()
+    _check("zero_unit_plan_tensors", lib().zero_unit_plan_tensors(plan, slots, offs, n))
+    return list(slots), list(offs)
+
+
+def zero_gather_units(plan, unit_lo, unit_hi, shards, unit_buffers, stream=0):
+    _check("zero_gather_units", lib().zero_gather_units(
+        plan, unit_lo, unit_hi, _ptrs(shards), _ptrs(unit_buffers), _vp(stream)))
+
+
+def zero_shard_units(plan, unit_lo, unit_hi, unit_buffers, shards, stream=0):
+    _check("zero_shard_units", lib().zero_shard_units(
+        plan, unit_lo, unit_hi, _ptrs(unit_buffers), _ptrs(shards), _vp(stream)))

@@ -20,9 +20,10 @@ import ctypes as C
 import torch
 
 from . import (ZERO_BF16, ZERO_FP16, ZeroHParams, ZeroScaler, zero_accumulate, zero_cast_params,
-               zero_grad_norm, zero_plan_create, zero_plan_destroy, zero_plan_get_info,
-               zero_reduce_scatter_accum, zero_scaler_init, zero_step, zero_step_accum,
-               zero_workspace_bytes)
+               zero_gather_units, zero_grad_norm, zero_plan_create, zero_plan_destroy,
+               zero_plan_get_info, zero_reduce_scatter_accum, zero_scaler_init, zero_shard_units,
+               zero_step, zero_step_accum, zero_unit_plan_create, zero_unit_plan_destroy,
+               zero_unit_plan_get_info, zero_unit_plan_units, zero_workspace_bytes)
 from . import synth
 
 
@@ -218,3 +219,61 @@ class Group:
     def flags_u32(self):
         self.stream.synchronize()
         return self.flags[:self.info.n_buckets].cpu().numpy().view("uint32")
+
+
+class UnitGroup:
+    """Device state of a stage-3 unit layout on one GPU: the N ranks' 16-bit
+    shard buffers and a ring of `window` unit buffers, each large enough for
+    the biggest gathered unit (only a window of units is ever resident).
+
+      shards   int16 [N, row]            rank r's slices of every unit, row =
+                                         shard elements rounded up to 8
+      buffers  int16 [window, urow]      gathered units, urow = largest unit
+                                         rounded up to 8
+    """
+
+    def __init__(self, uwl, device="cuda", window=2, stream=None):
+        self.wl = uwl
+        self.dev = torch.device(device)
+        self.N = uwl.n_ranks
+        self.plan = zero_unit_plan_create(uwl.numels, uwl.unit_of_tensor, uwl.n_units, self.N,
+                                          uwl.align_elems)
+        self.info = zero_unit_plan_get_info(self.plan)
+        self.units = zero_unit_plan_units(self.plan)
+        self.row = _round_up(max(self.info.shard_elems, 1), 8)
+        self.urow = _round_up(max(self.info.max_unit_psi_pad, 1), 8)
+        self.window = window
+        self.stream = stream if stream is not None else torch.cuda.Stream(device=self.dev)
+        self.sptr = self.stream.cuda_stream
+        self.shards = torch.zeros((self.N, self.row), dtype=torch.int16, device=self.dev)
+        self.buffers = torch.zeros((window, self.urow), dtype=torch.int16, device=self.dev)
+
+    def close(self):
+        if self.plan:
+            zero_unit_plan_destroy(self.plan)
+            self.plan = None
+
+    def shard_ptrs(self):
+        base, rb = self.shards.data_ptr(), self.row * 2
+        return [base + r * rb for r in range(self.N)]
+
+    def buffer_ptr(self, slot):
+        return self.buffers.data_ptr() + (slot % self.window) * self.urow * 2
+
+    def fill_shards(self, seed=None):
+        """Seeded 16-bit patterns in every shard buffer (the generator's bf16
+        normal stream, one stream per rank)."""
+        spec = synth.grad_spec(seed=self.wl.seed if seed is None else seed, sigma=1.0,
+                               psi=self.row)
+        for r, ptr in enumerate(self.shard_ptrs()):
+            synth.gpu_fill_grad(ptr, self.row, 0, spec, 1, r, True, self.sptr)
+
+    def gather(self, unit_lo, unit_hi, slot0=0):
+        """All-gather units [unit_lo, unit_hi) into buffer slots slot0, slot0 + 1, ..."""
+        ptrs = [self.buffer_ptr(slot0 + i) for i in range(unit_hi - unit_lo)]
+        zero_gather_units(self.plan, unit_lo, unit_hi, self.shard_ptrs(), ptrs, self.sptr)
+
+    def shard(self, unit_lo, unit_hi, slot0=0):
+        """Write buffer slots slot0, ... back into the units' slices."""
+        ptrs = [self.buffer_ptr(slot0 + i) for i in range(unit_hi - unit_lo)]
+        zero_shard_units(self.plan, unit_lo, unit_hi, ptrs, self.shard_ptrs(), self.sptr)

@@ -111,3 +111,59 @@ LLAMA_2B = Workload("llama_2B_n16_bf16_clip", llama_2b_numels(), 16, 50_000_000,
                     1e-3, outliers=True, weight_decay=0.1, max_grad_norm=1.0, steps=5)
 
 ALL = [TINY_FLAT, GPT2_SMALL, FLAT_1P5B, STAGE3_SLICE, LLAMA_2B]
+
+
+# ------------------------------------------------------ stage-3 FSDP units ----
+
+@dataclass
+class UnitWorkload:
+    """A tensor list wrapped into stage-3 FSDP units (forward order), the
+    number N of simulated ranks and the unit alignment grain in elements."""
+    name: str
+    numels: List[int]
+    unit_of_tensor: List[int]
+    n_units: int
+    n_ranks: int
+    align_elems: int = 1
+    seed: int = 0
+
+
+def _blocks_with_root(numels: List[int], root: List[int], per_block: int) -> Tuple[List[int], int]:
+    """Unit ids for a list laid out as root tensors + equal blocks: unit 0 is
+    the root (embeddings, final norm, head), unit b + 1 is block b."""
+    uot = []
+    body = [k for k in range(len(numels)) if k not in root]
+    assert len(body) % per_block == 0
+    ids = {}
+    for i, k in enumerate(body):
+        ids[k] = 1 + i // per_block
+    for k in range(len(numels)):
+        uot.append(0 if k in root else ids[k])
+    return uot, 1 + len(body) // per_block
+
+
+def gpt2_small_units(n_ranks=8, align_elems=1) -> UnitWorkload:
+    """GPT-2 small: one unit per transformer block, the root unit holding the
+    token and position embeddings and the final layer norm."""
+    numels = gpt2_small_numels()
+    uot, n_units = _blocks_with_root(numels, [0, 1, len(numels) - 2, len(numels) - 1], 12)
+    return UnitWorkload("gpt2_small_124M_units_n%d_a%d" % (n_ranks, align_elems), numels, uot,
+                        n_units, n_ranks, align_elems, seed=5)
+
+
+def llama_2b_units(n_ranks=16, align_elems=1) -> UnitWorkload:
+    """The Llama-style list: one unit per block, the root unit holding the
+    tied embedding and the final norm."""
+    numels = llama_2b_numels()
+    uot, n_units = _blocks_with_root(numels, [0, len(numels) - 1], 9)
+    return UnitWorkload("llama_2B_units_n%d_a%d" % (n_ranks, align_elems), numels, uot, n_units,
+                        n_ranks, align_elems, seed=6)
+
+
+def stage3_8p81b_units(n_ranks=64, align_elems=1) -> UnitWorkload:
+    """The 8.81B-parameter data-parallel share at 64 ranks, wrapped one block
+    per unit: blocks of 110,000,000 parameters (220 MB gathered in BF16) and
+    a root unit with the remaining 10,000,000 (80 blocks + root = 8.81e9)."""
+    numels = [10_000_000] + [110_000_000] * 80
+    return UnitWorkload("stage3_8p81B_units_n%d_a%d" % (n_ranks, align_elems), numels,
+                        list(range(81)), 81, n_ranks, align_elems, seed=7)

@@ -39,6 +39,8 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_struct_sizes():
+    assert C.sizeof(Z.ZeroUnit) == 56
+    assert C.sizeof(Z.ZeroUnitPlanInfo) == 120
     assert C.sizeof(Z.ZeroScaler) == 80
     assert C.sizeof(Z.ZeroPlanInfo) == 168
     assert C.sizeof(Z.ZeroHParams) == 64
@@ -125,3 +127,67 @@ def test_host_validation_without_gpu():
             Z.zero_selftest_wait_timeout(16, bad_limit)
         assert e.value.status == -1
     Z.zero_plan_destroy(p)
+
+
+def _compare_units(numels, uot, n_units, n, align):
+    p = Z.zero_unit_plan_create(numels, uot, n_units, n, align)
+    try:
+        info = Z.zero_unit_plan_get_info(p)
+        units = Z.zero_unit_plan_units(p)
+        slots, offs = Z.zero_unit_plan_tensors(p)
+        op, ounits, oslots, ooffs = oracle.make_unit_plan(numels, uot, n_units, n, align)
+        for f in ("psi", "psi_pad", "max_unit_psi_pad", "n_units", "n_ranks", "n_tensors",
+                  "align_elems", "persistent_bytes", "peak_one_bytes", "peak_two_bytes",
+                  "peak_backward_bytes", "max_unit_fraction", "comm_elems", "comm_bytes",
+                  "ring_bytes", "n_gathers"):
+            assert getattr(info, f) == getattr(op, f), f
+        assert info.shard_elems == op.shard
+        for a, b in zip(units, ounits):
+            assert (a.psi, a.pad, a.psi_pad, a.shard_elems, a.shard_offset, a.flat_offset,
+                    a.n_tensors, a.first_slot) == (b.psi, b.pad, b.psi_pad, b.shard,
+                                                   b.shard_offset, b.flat_offset, b.n_tensors,
+                                                   b.first_slot)
+        assert slots == list(oslots) and offs == list(ooffs)
+    finally:
+        Z.zero_unit_plan_destroy(p)
+
+
+def test_unit_planner_matches_checker():
+    for uw in (W.gpt2_small_units(), W.gpt2_small_units(8, 8), W.llama_2b_units(),
+               W.stage3_8p81b_units(), W.stage3_8p81b_units(64, 8)):
+        _compare_units(uw.numels, uw.unit_of_tensor, uw.n_units, uw.n_ranks, uw.align_elems)
+    rng = random.Random(3)
+    for _ in range(300):
+        n_t = rng.randint(1, 9)
+        n_units = rng.randint(1, n_t)
+        uot = list(range(n_units)) + [rng.randrange(n_units) for _ in range(n_t - n_units)]
+        rng.shuffle(uot)
+        numels = [rng.choice([0, 1, 3, 8, 255, 4096, 10007]) for _ in range(n_t)]
+        _compare_units(numels, uot, n_units, rng.choice([1, 2, 3, 8, 13, 64]),
+                       rng.choice([1, 2, 8, 64]))
+
+
+def test_unit_planner_and_gather_reject_bad_arguments():
+    for args, status in ((([4], [1], 1, 2, 1), -1), (([4, 4], [0, 0], 2, 2, 1), -1),
+                         (([4], [0], 1, 65, 1), -3), (([4], [0], 1, 2, 0), -1),
+                         (([4], [0], 1, 2, 8192), -3), (([-4], [0], 1, 2, 1), -1)):
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_unit_plan_create(*args)
+        assert e.value.status == status
+    p = Z.zero_unit_plan_create([100, 50], [0, 1], 2, 4, 1)
+    try:
+        for lo, hi in ((0, 0), (1, 3), (-1, 1), (2, 1)):
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_gather_units(p, lo, hi, [16] * 4, [16] * 2)
+            assert e.value.status == -1
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_gather_units(p, 0, 2, [16, 16, None, 16], [16, 16])
+        assert e.value.status == -1
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_gather_units(p, 0, 2, [16, 16, 18, 16], [16, 16])
+        assert e.value.status == -2
+        with pytest.raises(Z.ZeroError) as e:
+            Z.zero_shard_units(p, 0, 2, [16, 24], [16] * 4)
+        assert e.value.status == -2
+    finally:
+        Z.zero_unit_plan_destroy(p)
