@@ -526,6 +526,17 @@ def run_gather(args, rank, world, dist):
     # one launch per call (64 slices, at most 256 per launch) for a non-empty unit
     launches = sum(1 for u, _ in calls if g.units[u].shard_elems)
     traffic = profiled_traffic("copy_kernel", uw.name, "gather.cu")
+    # per-rank accounting of the layout under each sharding strategy (host)
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    accounting = {}
+    for name, strat, reps in (("FULL_SHARD", Z.ZERO_FULL_SHARD, 1),
+                              ("SHARD_GRAD_OP", Z.ZERO_SHARD_GRAD_OP, 1),
+                              ("NO_SHARD", Z.ZERO_NO_SHARD, 1),
+                              ("NO_RESHARD_AFTER_FORWARD", Z.ZERO_NO_RESHARD_AFTER_FORWARD, 1)):
+        c = Z.zero_unit_plan_strategy_cost(g.plan, strat, reps)
+        accounting[name] = {"persistent_gb": round(c.persistent_bytes / 1e9, 4),
+                            "peak_gb": round(c.peak_bytes / 1e9, 4),
+                            "wire_gb_per_step": round(2 * c.comm_elems / 1e9, 4)}
     line = {"metric": GATHER_METRIC, "value": round(gathered * K * world / (total_ms / 1e3) / 1e9, 4),
             "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -543,6 +554,7 @@ def run_gather(args, rank, world, dist):
                          "kernel_ms": round(blk_ms, 5),
                          "step_achieved_gbs": round(4 * gathered / (ms_per_step / 1e3) / 1e9, 1),
                          "step_frac": round(4 * gathered / (ms_per_step / 1e3) / 1e9 / peak, 4)},
+            "accounting_per_rank": accounting,
             "e2e": None, "gpu_launches": launches * K, "clocks": clk}
     g.close()
     return line

@@ -24,6 +24,8 @@ __all__ = [
     "ZeroUnit", "ZeroUnitPlanInfo", "ZERO_UNIT_MAX_ALIGN", "zero_unit_plan_create",
     "zero_unit_plan_destroy", "zero_unit_plan_get_info", "zero_unit_plan_units",
     "zero_unit_plan_tensors", "zero_gather_units", "zero_shard_units",
+    "ZeroStrategyCost", "zero_unit_plan_strategy_cost", "ZERO_FULL_SHARD", "ZERO_SHARD_GRAD_OP",
+    "ZERO_NO_SHARD", "ZERO_HYBRID_SHARD", "ZERO_NO_RESHARD_AFTER_FORWARD",
 ]
 
 ZERO_BF16 = 0
@@ -31,6 +33,8 @@ ZERO_FP16 = 1
 ZERO_MAX_RANKS = 64
 ZERO_TILE_ELEMS = 4096
 ZERO_UNIT_MAX_ALIGN = 4096
+(ZERO_FULL_SHARD, ZERO_SHARD_GRAD_OP, ZERO_NO_SHARD, ZERO_HYBRID_SHARD,
+ ZERO_NO_RESHARD_AFTER_FORWARD) = range(5)
 
 
 class ZeroError(RuntimeError):
@@ -90,6 +94,13 @@ class ZeroUnitPlanInfo(C.Structure):
                 ("n_gathers", C.c_int32), ("reserved", C.c_int32)]
 
 
+class ZeroStrategyCost(C.Structure):
+    _fields_ = [("persistent_bytes", C.c_double), ("peak_bytes", C.c_double),
+                ("comm_elems", C.c_double), ("comm_elems_inter", C.c_double),
+                ("ring_bytes", C.c_double), ("ring_bytes_inter", C.c_double),
+                ("shard_ranks", C.c_int32), ("gathers_per_unit", C.c_int32)]
+
+
 _lib = None
 _VP = C.c_void_p
 _P = C.POINTER
@@ -146,6 +157,8 @@ def lib():
         L.zero_unit_plan_get_info.argtypes = [_VP, _P(ZeroUnitPlanInfo)]
         L.zero_unit_plan_units.argtypes = [_VP, _P(ZeroUnit), C.c_int32]
         L.zero_unit_plan_tensors.argtypes = [_VP, _P(C.c_int32), _P(C.c_int64), C.c_int32]
+        L.zero_unit_plan_strategy_cost.argtypes = [_VP, C.c_int32, C.c_int32,
+                                                   _P(ZeroStrategyCost)]
         L.zero_gather_units.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _VP]
         L.zero_shard_units.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _VP]
         _lib = L
@@ -363,3 +376,10 @@ def zero_gather_units(plan, unit_lo, unit_hi, shards, unit_buffers, stream=0):
 def zero_shard_units(plan, unit_lo, unit_hi, unit_buffers, shards, stream=0):
     _check("zero_shard_units", lib().zero_shard_units(
         plan, unit_lo, unit_hi, _ptrs(unit_buffers), _ptrs(shards), _vp(stream)))
+
+
+def zero_unit_plan_strategy_cost(plan, strategy, n_replicas=1):
+    out = ZeroStrategyCost()
+    _check("zero_unit_plan_strategy_cost", lib().zero_unit_plan_strategy_cost(
+        plan, strategy, n_replicas, C.byref(out)))
+    return out

@@ -22,6 +22,7 @@
 
 static_assert(sizeof(zero_unit) == 56, "zero_unit layout is part of the ABI");
 static_assert(sizeof(zero_unit_plan_info) == 120, "zero_unit_plan_info layout is part of the ABI");
+static_assert(sizeof(zero_strategy_cost) == 56, "zero_strategy_cost layout is part of the ABI");
 
 extern "C" {
 
@@ -135,6 +136,67 @@ ZERO_API int zero_unit_plan_tensors(const zero_unit_plan* plan, int32_t* slot_te
   if (slot_tensor) std::copy(plan->slot_tensor.begin(), plan->slot_tensor.end(), slot_tensor);
   if (tensor_offset)
     std::copy(plan->tensor_offset.begin(), plan->tensor_offset.end(), tensor_offset);
+  return ZERO_OK;
+}
+
+ZERO_API int zero_unit_plan_strategy_cost(const zero_unit_plan* plan, int32_t strategy,
+                                          int32_t n_replicas, zero_strategy_cost* out) {
+  if (!plan || !out || n_replicas < 1) return ZERO_EINVAL;
+  if (strategy != ZERO_HYBRID_SHARD && n_replicas != 1) return ZERO_EINVAL;
+  const zero_unit_plan_info& I = plan->info;
+  const double g = I.n_ranks, reps = n_replicas;
+  const double held = static_cast<double>(I.shard_elems);
+  const double padded = static_cast<double>(I.psi_pad);
+  const double params = static_cast<double>(I.psi);
+  const double largest = static_cast<double>(I.max_unit_psi_pad);
+  zero_strategy_cost c{};
+  c.shard_ranks = I.n_ranks;
+  switch (strategy) {
+    case ZERO_FULL_SHARD:
+    case ZERO_HYBRID_SHARD:
+      // stage 3 in the group: gathered for the forward and again for the
+      // backward, reduce-scattered after it
+      c.persistent_bytes = 16.0 * held;
+      c.peak_bytes = c.persistent_bytes + 2.0 * largest;
+      c.comm_elems = 3.0 * padded;
+      c.ring_bytes = 6.0 * (g - 1.0) * held;
+      c.gathers_per_unit = 2;
+      if (strategy == ZERO_HYBRID_SHARD && n_replicas > 1) {
+        // the groups are replicas: all-reduce each rank's reduced shard
+        c.comm_elems_inter = 2.0 * held;
+        c.ring_bytes_inter = 4.0 * held * (reps - 1.0) / reps;
+        c.comm_elems += c.comm_elems_inter;
+        c.ring_bytes += c.ring_bytes_inter;
+      }
+      break;
+    case ZERO_SHARD_GRAD_OP:
+      // stage 2: the 16-bit weights stay resident
+      c.persistent_bytes = 2.0 * padded + 14.0 * held;
+      c.peak_bytes = c.persistent_bytes;
+      c.comm_elems = 2.0 * padded;
+      c.ring_bytes = 4.0 * (g - 1.0) * held;
+      c.gathers_per_unit = 1;
+      break;
+    case ZERO_NO_SHARD:
+      c.persistent_bytes = 16.0 * params;
+      c.peak_bytes = c.persistent_bytes;
+      c.comm_elems = 2.0 * params;
+      c.ring_bytes = 2.0 * (g - 1.0) * (2.0 * params) / g;
+      c.shard_ranks = 1;
+      c.gathers_per_unit = 0;
+      break;
+    case ZERO_NO_RESHARD_AFTER_FORWARD:
+      // one gather per unit, kept from its forward to its backward
+      c.persistent_bytes = 16.0 * held;
+      c.peak_bytes = c.persistent_bytes + 2.0 * padded;
+      c.comm_elems = 2.0 * padded;
+      c.ring_bytes = 4.0 * (g - 1.0) * held;
+      c.gathers_per_unit = 1;
+      break;
+    default:
+      return ZERO_EINVAL;
+  }
+  *out = c;
   return ZERO_OK;
 }
 

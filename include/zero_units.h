@@ -110,6 +110,54 @@ ZERO_API int zero_unit_plan_units(const zero_unit_plan* plan, zero_unit* out, in
 ZERO_API int zero_unit_plan_tensors(const zero_unit_plan* plan, int32_t* slot_tensor,
                                     int64_t* tensor_offset, int32_t capacity);
 
+/* Sharding strategies ("Training models too big for one GPU: ZeRO & FSDP",
+ * "FSDP: the same idea, one unit at a time": FULL_SHARD is stage 3,
+ * SHARD_GRAD_OP is close to stage 2, NO_SHARD is ordinary DDP, HYBRID_SHARD
+ * shards inside a node and replicates across nodes; "How far does splitting
+ * the batch get you?", "What does each stage cost on the wire?": Llama 3 kept
+ * the gathered parameters from the forward pass for the backward pass --
+ * stage 3's memory for the forward, stage 2's traffic). */
+typedef enum zero_strategy {
+  ZERO_FULL_SHARD = 0,
+  ZERO_SHARD_GRAD_OP = 1,
+  ZERO_NO_SHARD = 2,
+  ZERO_HYBRID_SHARD = 3,
+  ZERO_NO_RESHARD_AFTER_FORWARD = 4
+} zero_strategy;
+
+/* Per-rank cost of one step under a strategy (56 bytes). */
+typedef struct zero_strategy_cost {
+  double persistent_bytes;  /* model states held between steps */
+  double peak_bytes;        /* persistent + the largest gathered-parameter transient */
+  double comm_elems;        /* elements sent per step, counted as the pages count them */
+  double comm_elems_inter;  /* of which between shard groups (HYBRID_SHARD) */
+  double ring_bytes;        /* bytes sent per step when every collective is a ring */
+  double ring_bytes_inter;  /* of which between shard groups */
+  int32_t shard_ranks;      /* ranks one copy of the states is sharded over */
+  int32_t gathers_per_unit; /* all-gathers of each unit per step */
+} zero_strategy_cost;
+
+/* Cost of a step under `strategy` for the plan's layout. The plan's n_ranks
+ * is the shard group g; n_replicas R >= 1 is the number of groups holding
+ * replicas of the same shards (HYBRID_SHARD; R must be 1 for every other
+ * strategy). With the plan's psi, psi_pad P, held elements S and largest
+ * unit U, 16-bit parameters and gradients, K = 12:
+ *   FULL_SHARD     persistent 16S, peak +2U, 3P elements, ring 3(g-1)S x 2 bytes,
+ *                  2 gathers per unit;
+ *   SHARD_GRAD_OP  persistent 2P + 14S, no transient, 2P elements,
+ *                  ring 2(g-1)S x 2, 1 gather;
+ *   NO_SHARD       persistent 16 psi, 2 psi elements, ring 2(g-1)/g x 2 psi, 0 gathers;
+ *   HYBRID_SHARD   FULL_SHARD inside the group plus, for R > 1, an all-reduce
+ *                  of each rank's S reduced gradient elements over the R groups:
+ *                  2S elements and 2(R-1)/R x 2S bytes between groups;
+ *   NO_RESHARD_AFTER_FORWARD  persistent 16S, peak +2P (every unit gathered in
+ *                  the forward pass is held until its backward), 2P elements,
+ *                  ring 2(g-1)S x 2, 1 gather.
+ * Host only. Returns ZERO_EINVAL for a NULL argument, an unknown strategy or
+ * a bad n_replicas. */
+ZERO_API int zero_unit_plan_strategy_cost(const zero_unit_plan* plan, int32_t strategy,
+                                          int32_t n_replicas, zero_strategy_cost* out);
+
 /* All-gather of units [unit_lo, unit_hi) (a forward or backward prefetch
  * window), one kernel launch per 256 slices (N slices per unit). A window
  * larger than half of L2 is written with evict-first stores, a smaller one

@@ -74,6 +74,16 @@ class UnitPlan(C.Structure):
                 ("n_gathers", C.c_int32), ("reserved", C.c_int32)]
 
 
+class StrategyCost(C.Structure):
+    _fields_ = [("persistent_bytes", C.c_double), ("peak_bytes", C.c_double),
+                ("comm_elems", C.c_double), ("comm_elems_inter", C.c_double),
+                ("ring_bytes", C.c_double), ("ring_bytes_inter", C.c_double),
+                ("shard_ranks", C.c_int32), ("gathers_per_unit", C.c_int32)]
+
+
+FULL_SHARD, SHARD_GRAD_OP, NO_SHARD, HYBRID_SHARD, NO_RESHARD_AFTER_FORWARD = range(5)
+
+
 class Gen(C.Structure):
     _fields_ = [("spec", GradSpec), ("is_bf16", C.c_int32), ("inject_step", C.c_int32),
                 ("inject_rank", C.c_int32), ("inject_bits", C.c_uint32),
@@ -140,6 +150,9 @@ def lib():
         L.orc_unit_plan_make.restype = C.c_int
         L.orc_gather_unit.argtypes = [P(Unit), C.c_int32, C.c_void_p, C.c_void_p]
         L.orc_shard_unit.argtypes = [P(Unit), C.c_int32, C.c_void_p, C.c_void_p]
+        L.orc_strategy_cost_make.argtypes = [P(UnitPlan), C.c_int32, C.c_int32,
+                                             P(StrategyCost)]
+        L.orc_strategy_cost_make.restype = C.c_int
         _lib = L
     return _lib
 
@@ -363,3 +376,11 @@ def shard_unit(unit, full, shards):
         assert a.dtype == np.uint16 and a.flags.c_contiguous
         assert a.size >= unit.shard_offset + unit.shard
     lib().orc_shard_unit(C.byref(unit), len(shards), _ptr(full), _ptr_array(shards))
+
+
+def strategy_cost(unit_plan, strategy, n_replicas=1):
+    out = StrategyCost()
+    rc = lib().orc_strategy_cost_make(C.byref(unit_plan), strategy, n_replicas, C.byref(out))
+    if rc != 0:
+        raise ValueError("orc_strategy_cost_make failed: %d" % rc)
+    return out

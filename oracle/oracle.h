@@ -291,6 +291,50 @@ void orc_gather_unit(const orc_unit* u, int32_t n_ranks, const uint16_t* const* 
 void orc_shard_unit(const orc_unit* u, int32_t n_ranks, const uint16_t* full,
                     uint16_t* const* shards);
 
+/* Sharding strategies: [ZF] "FSDP: the same idea, one unit at a time" (FULL_SHARD
+ * is stage 3, SHARD_GRAD_OP is close to stage 2, NO_SHARD is ordinary DDP,
+ * HYBRID_SHARD shards inside a node and replicates across nodes); [SB] "What
+ * does each stage cost on the wire?" (Llama 3: states and gradients sharded,
+ * parameters not resharded after the forward pass -- stage 3's memory,
+ * stage 2's traffic). */
+enum {
+  ORC_FULL_SHARD = 0,
+  ORC_SHARD_GRAD_OP = 1,
+  ORC_NO_SHARD = 2,
+  ORC_HYBRID_SHARD = 3,
+  ORC_NO_RESHARD_AFTER_FORWARD = 4
+};
+
+typedef struct orc_strategy_cost {
+  double persistent_bytes;  /* model states held between steps, per rank */
+  double peak_bytes;        /* persistent + the largest gathered-parameter transient */
+  double comm_elems;        /* elements per rank per step, the pages' counting */
+  double comm_elems_inter;  /* of which between shard groups (HYBRID_SHARD) */
+  double ring_bytes;        /* bytes each rank sends per step over rings */
+  double ring_bytes_inter;  /* of which between shard groups */
+  int32_t shard_ranks;      /* ranks one copy of the states is sharded over */
+  int32_t gathers_per_unit; /* all-gathers of each unit per step */
+} orc_strategy_cost;
+
+/* Per-rank cost of one step under a strategy, for a unit plan whose n_ranks
+ * is the shard group g; n_replicas R is the number of shard groups (HYBRID_SHARD
+ * only; every other strategy takes R = 1). With psi, psi_pad P, held elements
+ * S and largest unit U of the plan, 16-bit parameters and gradients and
+ * K = 12:
+ *   FULL_SHARD     16S; +2U; 3P elements; ring 3 (g-1) S x 2 bytes; 2 gathers
+ *   SHARD_GRAD_OP  2P + 14S; no transient; 2P; ring 2 (g-1) S x 2; 1 gather
+ *   NO_SHARD       16 psi; 2 psi; ring all-reduce 2 (g-1)/g x 2 psi; 0 gathers
+ *   HYBRID_SHARD   FULL_SHARD inside the group, plus an all-reduce of each
+ *                  rank's S gradient elements over the R groups: 2S elements
+ *                  and 2 (R-1)/R x 2S bytes between groups (none when R = 1)
+ *   NO_RESHARD_AFTER_FORWARD  16S; +2P (every unit gathered in the forward
+ *                  pass is kept for its backward); 2P; ring 2 (g-1) S x 2;
+ *                  1 gather
+ * Returns 0, or -1 for an unknown strategy or R < 1 (R != 1 outside
+ * HYBRID_SHARD). */
+int orc_strategy_cost_make(const orc_unit_plan* p, int32_t strategy, int32_t n_replicas,
+                           orc_strategy_cost* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -102,3 +102,68 @@ void orc_shard_unit(const orc_unit* u, int32_t n_ranks, const uint16_t* full,
     for (int64_t j = 0; j < u->shard; ++j)
       shards[r][u->shard_offset + j] = full[(int64_t)r * u->shard + j];
 }
+
+int orc_strategy_cost_make(const orc_unit_plan* p, int32_t strategy, int32_t n_replicas,
+                           orc_strategy_cost* out) {
+  if (!p || !out || n_replicas < 1) return -1;
+  if (strategy != ORC_HYBRID_SHARD && n_replicas != 1) return -1;
+  memset(out, 0, sizeof(*out));
+  const double g = (double)p->n_ranks;
+  const double R = (double)n_replicas;
+  const double psi = (double)p->psi;
+  const double P = (double)p->psi_pad;
+  const double S = (double)p->shard;
+  const double U = (double)p->max_unit_psi_pad;
+  switch (strategy) {
+    case ORC_FULL_SHARD:
+    case ORC_HYBRID_SHARD:
+      /* stage 3 inside the shard group: gather before the forward and again
+       * before the backward, reduce-scatter after it */
+      out->persistent_bytes = 16.0 * S;
+      out->peak_bytes = out->persistent_bytes + 2.0 * U;
+      out->comm_elems = 3.0 * P;
+      out->ring_bytes = 3.0 * (g - 1.0) * S * 2.0;
+      out->shard_ranks = p->n_ranks;
+      out->gathers_per_unit = 2;
+      if (strategy == ORC_HYBRID_SHARD && n_replicas > 1) {
+        /* the groups hold replicas of the same shard: all-reduce each
+         * rank's S reduced gradient elements across the R groups */
+        out->comm_elems_inter = 2.0 * S;
+        out->ring_bytes_inter = 2.0 * (R - 1.0) / R * (2.0 * S);
+        out->comm_elems += out->comm_elems_inter;
+        out->ring_bytes += out->ring_bytes_inter;
+      }
+      return 0;
+    case ORC_SHARD_GRAD_OP:
+      /* stage 2: 16-bit parameters resident, gradients and optimizer states
+       * sharded; reduce-scatter, then all-gather of the updated parameters */
+      out->persistent_bytes = 2.0 * P + 14.0 * S;
+      out->peak_bytes = out->persistent_bytes;
+      out->comm_elems = 2.0 * P;
+      out->ring_bytes = 2.0 * (g - 1.0) * S * 2.0;
+      out->shard_ranks = p->n_ranks;
+      out->gathers_per_unit = 1;
+      return 0;
+    case ORC_NO_SHARD:
+      /* plain data parallelism: everything replicated, one all-reduce */
+      out->persistent_bytes = 16.0 * psi;
+      out->peak_bytes = out->persistent_bytes;
+      out->comm_elems = 2.0 * psi;
+      out->ring_bytes = orc_ring_bytes(2.0 * psi, p->n_ranks);
+      out->shard_ranks = 1;
+      out->gathers_per_unit = 0;
+      return 0;
+    case ORC_NO_RESHARD_AFTER_FORWARD:
+      /* stage-3 shards; each unit gathered once, in the forward pass, and
+       * kept until its backward: at the turn every unit is gathered */
+      out->persistent_bytes = 16.0 * S;
+      out->peak_bytes = out->persistent_bytes + 2.0 * P;
+      out->comm_elems = 2.0 * P;
+      out->ring_bytes = 2.0 * (g - 1.0) * S * 2.0;
+      out->shard_ranks = p->n_ranks;
+      out->gathers_per_unit = 1;
+      return 0;
+    default:
+      return -1;
+  }
+}

@@ -41,6 +41,7 @@ def test_every_declared_symbol_is_exported():
 def test_struct_sizes():
     assert C.sizeof(Z.ZeroUnit) == 56
     assert C.sizeof(Z.ZeroUnitPlanInfo) == 120
+    assert C.sizeof(Z.ZeroStrategyCost) == 56
     assert C.sizeof(Z.ZeroScaler) == 80
     assert C.sizeof(Z.ZeroPlanInfo) == 168
     assert C.sizeof(Z.ZeroHParams) == 64
@@ -148,6 +149,16 @@ def _compare_units(numels, uot, n_units, n, align):
                                                    b.shard_offset, b.flat_offset, b.n_tensors,
                                                    b.first_slot)
         assert slots == list(oslots) and offs == list(ooffs)
+        for strat in range(5):
+            for reps in ((1, 2, 5) if strat == Z.ZERO_HYBRID_SHARD else (1,)):
+                a = Z.zero_unit_plan_strategy_cost(p, strat, reps)
+                b = oracle.strategy_cost(op, strat, reps)
+                for f, _ in Z.ZeroStrategyCost._fields_:
+                    assert getattr(a, f) == pytest.approx(getattr(b, f), rel=1e-15, abs=0), f
+        for strat, reps in ((5, 1), (-1, 1), (Z.ZERO_FULL_SHARD, 2), (Z.ZERO_HYBRID_SHARD, 0)):
+            with pytest.raises(Z.ZeroError) as e:
+                Z.zero_unit_plan_strategy_cost(p, strat, reps)
+            assert e.value.status == -1
     finally:
         Z.zero_unit_plan_destroy(p)
 
