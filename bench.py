@@ -578,9 +578,12 @@ def truncated(wl, n_elems):
 oracle_sample = truncated
 
 
-def time_oracle_steps(wl_s, steps):
+def time_oracle_steps(wl_s, steps, threads=1):
     """Runs `steps` checker steps on wl_s; returns seconds of checker time
-    (input generation excluded)."""
+    (input generation excluded). With threads > 1 the owners are split into
+    contiguous rank ranges, one host thread each (the C checker runs without
+    the interpreter lock); every range has its own scaler and flags, so this
+    is for workloads without a global clip (the fused path)."""
     import numpy as np
     import oracle
     from fsdp_sharded_mixed_shard_gb300 import synth
@@ -601,10 +604,29 @@ def time_oracle_steps(wl_s, steps):
             for r in range(wl_s.n_ranks)]
     flags = np.zeros(max(p.n_buckets, 1), np.uint32)
     t = 0.0
+    if threads <= 1:
+        for _ in range(steps):
+            a = time.perf_counter()
+            oracle.step_arrays(p, 0, wl_s.n_ranks, wl_s.is_bf16, reps, 0, master, m, v, params,
+                               hp, sc, flags)
+            t += time.perf_counter() - a
+        return t
+    import threading
+    n = wl_s.n_ranks
+    cuts = [n * k // threads for k in range(threads + 1)]
+    ranges = [(cuts[k], cuts[k + 1]) for k in range(threads) if cuts[k + 1] > cuts[k]]
+    scalers = [oracle.scaler(wl_s.init_scale) for _ in ranges]
+    flag_sets = [np.zeros_like(flags) for _ in ranges]
     for _ in range(steps):
+        work = [threading.Thread(target=oracle.step_arrays,
+                                 args=(p, lo, hi, wl_s.is_bf16, reps, 0, master, m, v, params, hp,
+                                       scalers[i], flag_sets[i]))
+                for i, (lo, hi) in enumerate(ranges)]
         a = time.perf_counter()
-        oracle.step_arrays(p, 0, wl_s.n_ranks, wl_s.is_bf16, reps, 0, master, m, v, params, hp,
-                           sc, flags)
+        for w in work:
+            w.start()
+        for w in work:
+            w.join()
         t += time.perf_counter() - a
     return t
 
@@ -623,13 +645,23 @@ def cpu_baseline(wl, seconds):
     n, _ = calibrate_oracle(wl, seconds, steps)
     s = oracle_sample(wl, n)
     t = time_oracle_steps(s, steps)
-    return {"value": round(s.psi * steps / t / 1e9, 6), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": "first %d flat parameters of %s (same N=%d, buckets, format and "
-                      "hyperparameters), %d steps, plain single-threaded C checker, inputs "
-                      "materialised in host memory, generation untimed" % (
-                          s.psi, wl.name, wl.n_ranks, steps),
-            "seconds": round(t, 2)}
+    out = {"value": round(s.psi * steps / t / 1e9, 6), "unit": UNIT, "cores": 1,
+           "kind": "oracle",
+           "sample": "first %d flat parameters of %s (same N=%d, buckets, format and "
+                     "hyperparameters), %d steps, plain single-threaded C checker, inputs "
+                     "materialised in host memory, generation untimed" % (
+                         s.psi, wl.name, wl.n_ranks, steps),
+           "seconds": round(t, 2)}
+    # the same checker on every host core the ranks can use (one rank range
+    # per thread; no global clip on this path)
+    threads = min(os.cpu_count() or 1, wl.n_ranks)
+    if threads > 1 and wl.max_grad_norm <= 0:
+        t_all = time_oracle_steps(s, steps, threads)
+        out["all_cores"] = {"value": round(s.psi * steps / t_all / 1e9, 6), "unit": UNIT,
+                            "cores": threads, "seconds": round(t_all, 2),
+                            "sample": "the same sample, ranks split over %d host threads"
+                                      % threads}
+    return out
 
 
 def run_reference(args):
