@@ -345,6 +345,32 @@ __device__ __forceinline__ float4 tile_norm_record(const NormSlots& sl, int par,
   return make_float4(t.hi, t.lo, t.bhi, t.blo);
 }
 
+// Tile record from per-thread sums in shared memory (the bulk reduce pass):
+// lane l merges the in-range sums of threads l, l + 32, ..., in that order,
+// takes warp l's sums of big squares (lanes < n_warps), then the fixed
+// shuffle tree merges the 32 lanes.
+__device__ __forceinline__ float4 tile_norm_record_lanes(const float2* sums, const NormSlots& sl,
+                                                         int par, int n_warps, int lane) {
+  NormAcc t;
+  for (int i = 0; i < n_warps; ++i) {
+    const float2 x = sums[lane + 32 * i];
+    ff_merge(t.hi, t.lo, x.x, x.y);
+  }
+  if (lane < n_warps) {
+    t.bhi = sl.bhi[par][lane];
+    t.blo = sl.blo[par][lane];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float h2 = __shfl_down_sync(0xFFFFFFFFu, t.hi, off);
+    float l2 = __shfl_down_sync(0xFFFFFFFFu, t.lo, off);
+    float bh2 = __shfl_down_sync(0xFFFFFFFFu, t.bhi, off);
+    float bl2 = __shfl_down_sync(0xFFFFFFFFu, t.blo, off);
+    if (lane < off) t.merge(h2, l2, bh2, bl2);
+  }
+  return make_float4(t.hi, t.lo, t.bhi, t.blo);
+}
+
 __device__ __forceinline__ void raise_flag(const Args& a, int32_t bucket) {
   atomicOr(&a.scaler->pending, 1u);
   if (a.flags) atomicOr(&a.flags[bucket], 1u);
@@ -971,6 +997,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
   __shared__ NormSlots sh_norm;
+  // reduce pass: every consumer thread's in-range tile sums (hi, lo), by
+  // tile parity (8 KB)
+  __shared__ float2 sh_sums[MODE == kReduce ? 2 : 1][MODE == kReduce ? kConsumers : 1];
   __shared__ int sh_abort;
   extern __shared__ __align__(128) unsigned char stage_mem[];
 
@@ -1217,11 +1246,29 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     }
     if constexpr (MODE == kReduce) {
       if (a.mode_flags & kFlagPartials) {
+        // Each thread leaves its in-range sums in shared memory; only the
+        // rare sums of big (or non-finite) squares are merged per warp, and
+        // only in a warp that has any. One barrier, then the tile's record
+        // warp merges everything in a fixed order.
         const int par = tile_no & 1;
-        tile_norm_publish(nacc, sh_norm, par, warp, lane);
+        sh_sums[par][tid] = make_float2(nacc.hi, nacc.lo);
+        float bh = nacc.bhi, bl = nacc.blo;
+        if (__any_sync(0xFFFFFFFFu, bh != 0.f || bl != 0.f)) {
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float h2 = __shfl_down_sync(0xFFFFFFFFu, bh, off);
+            const float l2 = __shfl_down_sync(0xFFFFFFFFu, bl, off);
+            if (lane < off) ff_merge(bh, bl, h2, l2);
+          }
+        }
+        if (lane == 0) {
+          sh_norm.bhi[par][warp] = bh;
+          sh_norm.blo[par][warp] = bl;
+        }
         consumer_sync();
         if (warp == static_cast<int>(tile_no % kConsumerWarps)) {
-          const float4 rec = tile_norm_record(sh_norm, par, kConsumerWarps, lane);
+          const float4 rec =
+              tile_norm_record_lanes(sh_sums[par], sh_norm, par, kConsumerWarps, lane);
           if (lane == 0) a.partials[t.partial] = rec;
         }
       }
