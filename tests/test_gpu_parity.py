@@ -242,3 +242,44 @@ def test_micro_batch_accumulation_overflow_in_last_micro_batch():
                     dynamic_scale=True, steps=3, n_micro=3, inject=(2, 3, psi // 2, 0x7C00))
     stats, dev, orc = run_small(wl)
     assert dev.t == 2 and dev.scale == 1024.0
+
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+def test_clip_with_big_squares_in_some_warps(n):
+    """Gradients with |g| >= 2^56 (their squares go through the scaled
+    accumulator pair) in a few tiles and warps only, clip active: the
+    two-pass norm and the whole state match the checker."""
+    from parity_util import assert_params, assert_state, norm_tol, oracle_hp
+    psi = 3 * 4096 * n + 1001
+    wl = W.Workload("bigsq", [psi], n, 0, True, 31, 1e-3, max_grad_norm=1.0, steps=1)
+    g = harness.Group(wl)
+    g.init_state()
+    g.gen_grads(1)
+    torch.cuda.synchronize()
+    # bf16 patterns of 2^60, -2^100 and 2^75 planted in one replica each
+    plant = [(1, 5, 0x5D80), (0, 4096 + 600, 0xF180), (n - 1, g.S + 7, 0x6500),
+             (2 % n, 2 * g.S + 4096 + 3000, 0x5D80)]
+    for r, e, bits in plant:
+        g.replicas[r, e] = bits - 65536 if bits >= 32768 else bits
+    torch.cuda.synchronize()
+    reps_host = [np.ascontiguousarray(x) for x in g.replicas_u16()]
+    g.step()
+    torch.cuda.synchronize()
+    dev = g.read_scaler()
+    p, _, _ = oracle.make_plan(wl.numels, n, 0)
+    hp = oracle_hp(wl)
+    sc = oracle.scaler(wl.init_scale)
+    from fsdp_sharded_mixed_shard_gb300 import synth
+    master = synth.master_f32(p.psi_pad, 0, wl.seed, psi)
+    m = np.zeros(p.psi_pad, np.float32)
+    v = np.zeros(p.psi_pad, np.float32)
+    params = oracle.cast16(master, True)
+    oracle.step_arrays(p, 0, n, True, reps_host, 0, master, m, v, params, hp, sc)
+    assert sc.norm_sq > 2.0 ** 190 and dev.clip_apply == 1 and dev.overflow == 0
+    assert abs(dev.norm_sq - sc.norm_sq) <= norm_tol(p.psi_pad) * sc.norm_sq
+    got_master, got_m, got_v = (x.numpy() for x in g.current_state())
+    assert_state(got_master[:psi], master[:psi], "master")
+    assert_state(got_m[:psi], m[:psi], "exp_avg")
+    assert_state(got_v[:psi], v[:psi], "exp_avg_sq")
+    assert_params(g.params_u16()[:psi], params[:psi])
+    g.close()
