@@ -20,6 +20,7 @@ __all__ = [
     "zero_reduce_scatter", "zero_grad_norm", "zero_step", "zero_step_update", "zero_step_finish",
     "zero_cast_params", "zero_accumulate", "zero_reduce_scatter_accum", "zero_step_accum",
     "zero_step_update_accum", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
+    "zero_checked_status", "zero_selftest_check", "use_checked_library",
     "zero_version", "lib",
     "ZeroUnit", "ZeroUnitPlanInfo", "ZERO_UNIT_MAX_ALIGN", "zero_unit_plan_create",
     "zero_unit_plan_destroy", "zero_unit_plan_get_info", "zero_unit_plan_units",
@@ -102,15 +103,27 @@ class ZeroStrategyCost(C.Structure):
 
 
 _lib = None
+_variant = "release"
 _VP = C.c_void_p
 _P = C.POINTER
 
 
+def use_checked_library():
+    """Make this process load libzero_checked.so, the build whose kernels test
+    every memory range they touch (see zero_checked_status), instead of
+    libzero.so. Call it before the first library call."""
+    global _variant
+    if _lib is not None and _variant != "checked":
+        raise RuntimeError("libzero.so is already loaded in this process")
+    _variant = "checked"
+
+
 def lib():
-    """The loaded libzero.so (raises if it has not been built)."""
+    """The loaded libzero.so, or libzero_checked.so after use_checked_library()
+    (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        path = _build.ZERO_LIB
+        path = _build.ZERO_CHECKED_LIB if _variant == "checked" else _build.ZERO_LIB
         if not os.path.exists(path):
             raise RuntimeError("libzero.so is not built (%s); run __graft_entry__.build()" % path)
         L = C.CDLL(path)
@@ -147,6 +160,8 @@ def lib():
         L.zero_grad_norm_noalloc.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP),
                                              _P(ZeroHParams), _VP, _VP]
         L.zero_selftest_wait_timeout.argtypes = [_VP, C.c_int64, _VP]
+        L.zero_checked_status.argtypes = [_P(C.c_int64), _P(C.c_int64), _VP]
+        L.zero_selftest_check.argtypes = [_VP]
         L.zero_strerror.argtypes = [C.c_int]
         L.zero_strerror.restype = C.c_char_p
         L.zero_version.argtypes = []
@@ -383,3 +398,19 @@ def zero_unit_plan_strategy_cost(plan, strategy, n_replicas=1):
     _check("zero_unit_plan_strategy_cost", lib().zero_unit_plan_strategy_cost(
         plan, strategy, n_replicas, C.byref(out)))
     return out
+
+
+# ------------------------------------------------------------ checked build --
+
+def zero_checked_status(stream=0):
+    """(violations, first) recorded by a checked build since the last call;
+    first = site << 48 | low 48 bits of the index. Raises ZeroError (status
+    ZERO_ESTATE) in the release build."""
+    n, first = C.c_int64(), C.c_int64()
+    _check("zero_checked_status", lib().zero_checked_status(C.byref(n), C.byref(first),
+                                                            _vp(stream)))
+    return n.value, first.value
+
+
+def zero_selftest_check(stream=0):
+    _check("zero_selftest_check", lib().zero_selftest_check(_vp(stream)))

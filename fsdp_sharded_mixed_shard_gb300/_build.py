@@ -1,6 +1,8 @@
 """In-tree build of the native libraries (no pip install, no cmake).
 
   _lib/libzero.so          the C-ABI library: host planner + sm_103a kernels
+  _lib/libzero_checked.so  the same built with -DZERO_CHECKED: every kernel tests
+                           the memory ranges it touches and counts violations
   _lib/libzsynth_gpu.so    synthetic-input generator kernels (harness only)
   _lib/libzsynth_host.so   host build of the same generator (harness only)
 
@@ -25,6 +27,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-shared"
                      "-Xcompiler", "-fPIC,-ffp-contract=off,-fvisibility=hidden"]
 
 ZERO_LIB = os.path.join(LIBDIR, "libzero.so")
+ZERO_CHECKED_LIB = os.path.join(LIBDIR, "libzero_checked.so")
 SYNTH_GPU_LIB = os.path.join(LIBDIR, "libzsynth_gpu.so")
 SYNTH_HOST_LIB = os.path.join(LIBDIR, "libzsynth_host.so")
 
@@ -49,6 +52,9 @@ def _jobs():
     if zero_src:
         jobs.append((ZERO_LIB, zero_dep,
                      [NVCC] + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + zero_src))
+        jobs.append((ZERO_CHECKED_LIB, zero_dep,
+                     [NVCC] + NVCC_FLAGS + ["-DZERO_CHECKED", "-I", INCLUDE, "-I", CSRC] +
+                     zero_src))
     jobs += [
         (SYNTH_GPU_LIB, [os.path.join(SYNTH, "synth_gpu.cu"), synth_h, __file__],
          [NVCC] + NVCC_FLAGS + ["-I", SYNTH, os.path.join(SYNTH, "synth_gpu.cu")]),

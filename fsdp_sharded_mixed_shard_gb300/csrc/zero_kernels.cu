@@ -108,6 +108,8 @@ struct Args {
   int32_t has_acc;                          // 1: replica value = acc + 16-bit micro-batch value
   int32_t pad1;
   double beta1, beta2;
+  int64_t wend;       // window indices of this launch lie in [0, wend) (checked builds)
+  int64_t n_records;  // norm records the workspace holds (checked builds)
   StagePlan plan;  // bulk pipeline: stages of one element range
   Seg segs[kMaxSegs];
 };
@@ -124,6 +126,42 @@ struct StepScalars {
   int dst;         // optimizer set written
   int skip;        // 1: nothing to do in this launch
 };
+
+// ----------------------------------------------------- checked builds --
+//
+// Built with -DZERO_CHECKED (libzero_checked.so), every kernel tests the
+// global and shared-memory ranges it is about to touch against the extents
+// the plan gives (window, shard, records, stage slot). A failing test skips
+// the access, counts the violation and keeps the first one (site << 48 |
+// low 48 bits of the index) for zero_checked_status; nothing traps. The
+// release build compiles every test away.
+enum CheckSite : int {
+  kSiteSelftest = 1,
+  kSiteScalar = 2,
+  kSiteVector = 3,
+  kSiteRepCopy = 4,
+  kSiteAccCopy = 5,
+  kSiteStateCopy = 6,
+  kSiteStageBytes = 7,
+  kSiteStore = 8,
+  kSiteRecord = 9,
+};
+#ifdef ZERO_CHECKED
+__device__ unsigned long long g_check_first;
+__device__ unsigned int g_check_count;
+__device__ __noinline__ bool check_failed(int site, int64_t where) {
+  atomicAdd(&g_check_count, 1u);
+  atomicCAS(&g_check_first, 0ull,
+            (static_cast<unsigned long long>(site) << 48) |
+                (static_cast<unsigned long long>(where) & 0xFFFFFFFFFFFFull));
+  return false;
+}
+#define ZCHECK(cond, site, where) ((cond) ? true : check_failed((site), (where)))
+// one planted violation, to test the reporting path
+__global__ void check_selftest_kernel() { (void)ZCHECK(threadIdx.x > 0, kSiteSelftest, 42); }
+#else
+#define ZCHECK(cond, site, where) true
+#endif
 
 // ------------------------------------------------------------ primitives --
 
@@ -486,6 +524,7 @@ __device__ __forceinline__ void do_vector(const Args& a, const StepScalars& s, i
                                           bool& bad) {
   const int64_t w = j - a.wbase;                    // window index
   const int64_t k = j - static_cast<int64_t>(rank) * a.shard;  // shard index
+  if (!ZCHECK(w >= 0 && w + 8 <= a.wend && k >= 0 && k + 8 <= a.shard, kSiteVector, j)) return;
   float g[8];
   float th[8], m[8], v[8];
   if constexpr (MODE == kFused || MODE == kUpdate) {
@@ -568,6 +607,7 @@ __device__ __forceinline__ void do_scalar(const Args& a, const StepScalars& s, i
                                           bool& bad) {
   const int64_t w = j - a.wbase;
   const int64_t k = j - static_cast<int64_t>(rank) * a.shard;
+  if (!ZCHECK(w >= 0 && w < a.wend && k >= 0 && k < a.shard, kSiteScalar, j)) return;
   float g = 0.f, th = 0.f, m = 0.f, v = 0.f;
   if constexpr (MODE == kFused || MODE == kUpdate) {
     th = a.master[s.src][rank][k];
@@ -669,7 +709,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
         __syncthreads();
         if (warp == static_cast<int>(tile_no % kWarps)) {
           const float4 rec = tile_norm_record(sh_norm, par, kWarps, lane);
-          if (lane == 0) a.partials[sg.tile_global0 + (g - sg.tile_local0)] = rec;
+          const int64_t r = sg.tile_global0 + (g - sg.tile_local0);
+          if (lane == 0 && ZCHECK(r >= 0 && r < a.n_records, kSiteRecord, r)) a.partials[r] = rec;
         }
       }
     }
@@ -1063,14 +1104,20 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             if (c < n_rep) {
               int rr = t.first_rep + r_lo + c;
               if (rr >= N) rr -= N;
-              bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
-                       &full_bar[slot], pol);
+              if (ZCHECK(w >= 0 && w + len <= a.wend, kSiteRepCopy, w) &&
+                  ZCHECK((c + 1) * (2 * E) <= static_cast<int>(slot_bytes), kSiteStageBytes, c))
+                bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
+                         &full_bar[slot], pol);
             } else if (kAcc && c < n_rep_chunks) {
               int rr = t.first_rep + r_lo + (c - n_rep);
               if (rr >= N) rr -= N;
-              bulk_g2s(buf + static_cast<size_t>(n_rep) * (2 * E) +
-                           static_cast<size_t>(c - n_rep) * (4 * E),
-                       a.acc[rr] + w, len * 4, &full_bar[slot], pol);
+              if (ZCHECK(w >= 0 && w + len <= a.wend, kSiteAccCopy, w) &&
+                  ZCHECK(n_rep * (2 * E) + (c - n_rep + 1) * (4 * E) <=
+                             static_cast<int>(slot_bytes),
+                         kSiteStageBytes, c))
+                bulk_g2s(buf + static_cast<size_t>(n_rep) * (2 * E) +
+                             static_cast<size_t>(c - n_rep) * (4 * E),
+                         a.acc[rr] + w, len * 4, &full_bar[slot], pol);
             } else {
               const int q = c - n_rep_chunks;
               const float* src;
@@ -1082,9 +1129,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                 src = q == 0 ? a.master[s.src][t.rank]
                              : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
               }
-              bulk_g2s(buf + static_cast<size_t>(n_rep) * (kRepBytes * E) +
-                           static_cast<size_t>(q) * (4 * E),
-                       src + kk, len * 4, &full_bar[slot], pol);
+              if (ZCHECK(kk >= 0 && kk + len <= a.shard, kSiteStateCopy, kk) &&
+                  ZCHECK(n_rep * (kRepBytes * E) + (q + 1) * (4 * E) <=
+                             static_cast<int>(slot_bytes),
+                         kSiteStageBytes, c))
+                bulk_g2s(buf + static_cast<size_t>(n_rep) * (kRepBytes * E) +
+                             static_cast<size_t>(q) * (4 * E),
+                         src + kk, len * 4, &full_bar[slot], pol);
             }
           }
           __syncwarp();
@@ -1182,7 +1233,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 #pragma unroll
                 for (int e = 0; e < EPT; ++e) bad |= nonfinite(gv[e]);
               }
-              if constexpr (MODE == kReduce) stg_fv<EPT>(a.ghat[t.rank] + k, gv);
+              if constexpr (MODE == kReduce) {
+                if (ZCHECK(k >= 0 && k + EPT <= a.shard, kSiteStore, k))
+                  stg_fv<EPT>(a.ghat[t.rank] + k, gv);
+              }
             }
           }
           if (partials && completes) {
@@ -1222,10 +1276,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
               lds_fv<EPT>(sb + 8 * E + t_off * 4, v);
 #pragma unroll
               for (int e = 0; e < EPT; ++e) adamw(th[e], m[e], v[e], gv[e], a, s);
-              stg_fv<EPT>(a.master[s.dst][t.rank] + k, th);
-              stg_fv<EPT>(a.mom[s.dst][t.rank] + k, m);
-              stg_fv<EPT>(a.var[s.dst][t.rank] + k, v);
-              stg_hv<kBf16, EPT>(a.flat + w, th);
+              if (ZCHECK(k >= 0 && k + EPT <= a.shard && w >= 0 && w + EPT <= a.wend,
+                         kSiteStore, k)) {
+                stg_fv<EPT>(a.master[s.dst][t.rank] + k, th);
+                stg_fv<EPT>(a.mom[s.dst][t.rank] + k, m);
+                stg_fv<EPT>(a.var[s.dst][t.rank] + k, v);
+                stg_hv<kBf16, EPT>(a.flat + w, th);
+              }
             }
           }
         }
@@ -1269,7 +1326,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if (warp == static_cast<int>(tile_no % kConsumerWarps)) {
           const float4 rec =
               tile_norm_record_lanes(sh_sums[par], sh_norm, par, kConsumerWarps, lane);
-          if (lane == 0) a.partials[t.partial] = rec;
+          if (lane == 0 &&
+              ZCHECK(t.partial >= 0 && t.partial < a.n_records, kSiteRecord, t.partial))
+            a.partials[t.partial] = rec;
         }
       }
     }
@@ -1527,6 +1586,10 @@ int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
     }
     a.n_segs = s1 - s0;
     a.n_tiles = tiles;
+    // extents for the checked build: the window indices this launch may
+    // touch and the records the workspace holds
+    a.wend = p->segs[s1 - 1].hi - a.wbase;
+    a.n_records = p->info.n_tiles;
     if (tiles == 0) continue;
     if constexpr (kBulk) {
       const int rc = launch_bulk<MODE, kBf16>(a, tiles, stream);
@@ -1847,6 +1910,40 @@ ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns,
   wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       d_scaler, static_cast<uint64_t>(limit_ns));
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+}
+
+ZERO_API int zero_checked_status(int64_t* violations, int64_t* first, void* stream) {
+  if (!violations || !first) return ZERO_EINVAL;
+  *violations = 0;
+  *first = 0;
+#ifdef ZERO_CHECKED
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ZERO_ECUDA;
+  unsigned int count = 0;
+  unsigned long long code = 0;
+  const unsigned int zero_count = 0;
+  const unsigned long long zero_code = 0;
+  if (cudaMemcpyFromSymbol(&count, zk::g_check_count, sizeof(count)) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&code, zk::g_check_first, sizeof(code)) != cudaSuccess ||
+      cudaMemcpyToSymbol(zk::g_check_count, &zero_count, sizeof(zero_count)) != cudaSuccess ||
+      cudaMemcpyToSymbol(zk::g_check_first, &zero_code, sizeof(zero_code)) != cudaSuccess)
+    return ZERO_ECUDA;
+  *violations = count;
+  *first = static_cast<int64_t>(code);
+  return ZERO_OK;
+#else
+  (void)stream;
+  return ZERO_ESTATE;
+#endif
+}
+
+ZERO_API int zero_selftest_check(void* stream) {
+#ifdef ZERO_CHECKED
+  zk::check_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+#else
+  (void)stream;
+  return ZERO_ESTATE;
+#endif
 }
 
 ZERO_API int zero_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,

@@ -200,6 +200,31 @@ class Group:
         zero_step(self.plan, self.lo, self.hi, m, v, w, self.n_sets, gp, None, self.wbase,
                   self.flat.data_ptr(), self.hp, sc, fl, st)
 
+    # ----------------------------------------------------------- checkpoint
+    def state_dict(self):
+        """Everything a later step depends on, as CPU tensors: the owned
+        master/exp_avg/exp_avg_sq shards of the current state set, the
+        16-bit working parameters and the 80-byte device scaler. The other
+        ping-pong set and the replicas are scratch between steps."""
+        self.stream.synchronize()
+        idx = self.read_scaler().state_index if self.n_sets == 2 else 0
+        return {"state": self.state[idx].cpu().clone(), "flat": self.flat.cpu().clone(),
+                "scaler": self.scaler.cpu().clone(), "workload": self.wl.name,
+                "layout": (self.N, self.lo, self.hi, self.S, self.srow, self.row)}
+
+    def load_state_dict(self, sd):
+        """Restore a state_dict() of the same workload and layout; the state
+        goes back into the set the saved scaler names as current."""
+        if sd["workload"] != self.wl.name or tuple(sd["layout"]) != (
+                self.N, self.lo, self.hi, self.S, self.srow, self.row):
+            raise ValueError("state_dict of another workload or layout")
+        self.stream.synchronize()
+        self.scaler.copy_(sd["scaler"])
+        idx = self.read_scaler().state_index if self.n_sets == 2 else 0
+        self.state[idx].copy_(sd["state"])
+        self.flat.copy_(sd["flat"])
+        torch.cuda.synchronize()
+
     # ------------------------------------------------------------- readback
     def current_state(self):
         """(master, exp_avg, exp_avg_sq) of the owned window as fp32 CPU

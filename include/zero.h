@@ -363,6 +363,21 @@ ZERO_API int zero_cast_params(const zero_plan* plan, int32_t rank_lo, int32_t ra
  * outside the range. */
 ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns, void* stream);
 
+/* Checked builds (libzero_checked.so, compiled with -DZERO_CHECKED) test
+ * every global and shared-memory range a kernel is about to touch against
+ * the extents the plan gives (the call's window, the shard length, the
+ * workspace's records, the stage slot); a failing test skips that access,
+ * counts a violation and keeps the first one, and nothing traps.
+ * zero_checked_status synchronizes `stream`, returns the count and the
+ * first violation (site << 48 | low 48 bits of the offending index; sites:
+ * 1 self-test, 2 scalar element, 3 vector element, 4 replica copy,
+ * 5 accumulator copy, 6 state copy, 7 stage slot, 8 store, 9 norm record)
+ * and clears both. zero_selftest_check plants one violation (site 1,
+ * index 42). In the release build both return ZERO_ESTATE (and
+ * zero_checked_status zeroes its outputs). */
+ZERO_API int zero_checked_status(int64_t* violations, int64_t* first, void* stream);
+ZERO_API int zero_selftest_check(void* stream);
+
 /* Kernels launched per call, for accounting (L = ceil(segments processed /
  * 128), empty launches skipped): fused zero_step L + L (update; overflow
  * re-cast check merged with the bookkeeping in the last), two-pass zero_step

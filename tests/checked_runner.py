@@ -1,0 +1,56 @@
+"""Runs GPU parity cases through libzero_checked.so in its own process (the
+library variant is fixed per process) and prints one JSON line per case
+with the violations the kernels recorded. Used by tests/test_gpu_checked.py."""
+import json
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+import fsdp_sharded_mixed_shard_gb300 as Z  # noqa: E402
+
+Z.use_checked_library()
+
+from fsdp_sharded_mixed_shard_gb300 import workloads as W  # noqa: E402
+from parity_util import run_small  # noqa: E402
+
+
+def tiny_transformer_numels(d=64, vocab=503, ctx=128, layers=3):
+    out = [vocab * d, ctx * d]
+    for _ in range(layers):
+        out += [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
+    return out + [d, d]
+
+
+def cases():
+    t = tiny_transformer_numels()
+    yield "fused_bf16_n8", dict(wl=W.GPT2_SMALL.scaled(numels=t, bucket_elems=50_000, steps=2))
+    yield "two_pass_clip_fp16_n8", dict(wl=W.GPT2_SMALL.scaled(
+        numels=t, bucket_elems=50_000, steps=2, is_bf16=False, max_grad_norm=0.5,
+        init_scale=1024.0))
+    yield "two_pass_clip_n16", dict(wl=W.GPT2_SMALL.scaled(
+        numels=t, n_ranks=16, bucket_elems=0, steps=2, max_grad_norm=0.5))
+    yield "fused_n64_ragged", dict(wl=W.Workload("n64", [300_007], 64, 0, True, 5, 1e-3,
+                                                 steps=2))
+    yield "rank_subset_window", dict(wl=W.Workload("subset", [200_003], 8, 0, True, 7, 1e-3,
+                                                   steps=2, rank_lo=3, rank_hi=6))
+    yield "micro_batches_two_pass", dict(wl=W.GPT2_SMALL.scaled(
+        numels=t, bucket_elems=0, steps=2, max_grad_norm=0.5, n_micro=3))
+    yield "odd_shard_scalar_paths", dict(wl=W.TINY_FLAT.scaled(numels=[100_003], steps=2))
+
+
+def main():
+    Z.zero_selftest_check()
+    n, first = Z.zero_checked_status()
+    print(json.dumps({"case": "selftest", "violations": n, "first": first}), flush=True)
+    for name, kw in cases():
+        run_small(kw["wl"])
+        n, first = Z.zero_checked_status()
+        print(json.dumps({"case": name, "violations": n, "first": first}), flush=True)
+    print(json.dumps({"case": "library", "path": Z._build.ZERO_CHECKED_LIB,
+                      "loaded": Z.lib()._name}), flush=True)
+
+
+if __name__ == "__main__":
+    main()

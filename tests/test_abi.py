@@ -36,6 +36,18 @@ def test_every_declared_symbol_is_exported():
     exported = set(re.findall(r" T (zero_\w+)", out))
     assert names <= exported
     assert exported <= names, "exported but undeclared: %s" % (exported - names)
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.ZERO_CHECKED_LIB],
+                         capture_output=True, text=True).stdout
+    assert set(re.findall(r" T (zero_\w+)", out)) == exported
+
+
+def test_release_build_has_no_checks():
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_checked_status()
+    assert e.value.status == -6
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_selftest_check()
+    assert e.value.status == -6
 
 
 def test_struct_sizes():

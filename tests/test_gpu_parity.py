@@ -283,3 +283,45 @@ def test_clip_with_big_squares_in_some_warps(n):
     assert_state(got_v[:psi], v[:psi], "exp_avg_sq")
     assert_params(g.params_u16()[:psi], params[:psi])
     g.close()
+
+
+@pytest.mark.parametrize("clip,n_micro", [(0.0, 1), (0.5, 1), (0.0, 2)])
+def test_checkpoint_resume_is_bit_exact(tmp_path, clip, n_micro):
+    """Run 2 steps, save through torch, keep going 2 more steps; a fresh group
+    that loads the checkpoint and runs the same 2 steps ends bit-identical
+    (state, parameters and every scaler field), on both ping-pong parities."""
+    wl = W.GPT2_SMALL.scaled(name="resume", numels=tiny_transformer_numels(), bucket_elems=60_000,
+                             max_grad_norm=clip, n_micro=n_micro, steps=4, dynamic_scale=True,
+                             init_scale=1024.0)
+
+    def run(g, steps):
+        for step in steps:
+            if n_micro > 1:
+                g.step_micro(step)
+            else:
+                g.gen_grads(step)
+                g.step()
+        torch.cuda.synchronize()
+
+    a = harness.Group(wl)
+    a.init_state()
+    run(a, (1, 2))
+    path = tmp_path / "ckpt.pt"
+    torch.save(a.state_dict(), path)
+    run(a, (3, 4))
+    b = harness.Group(wl)
+    b.init_state()
+    run(b, (1,))            # leave b on the other ping-pong set and other values first
+    b.load_state_dict(torch.load(path))
+    run(b, (3, 4))
+    for x, y in zip(a.current_state(), b.current_state()):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert np.array_equal(a.params_u16(), b.params_u16())
+    assert bytes(a.read_scaler()) == bytes(b.read_scaler())
+    assert a.read_scaler().t == 4
+    other = harness.Group(wl.scaled(name="other"))
+    with pytest.raises(ValueError):
+        other.load_state_dict(torch.load(path))
+    other.close()
+    a.close()
+    b.close()
