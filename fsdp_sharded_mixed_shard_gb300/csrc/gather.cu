@@ -32,6 +32,7 @@
 #include <cstring>
 #include <new>
 
+#include "checked.cuh"
 #include "zero_internal.h"
 #include "zero_units_internal.h"
 
@@ -96,7 +97,9 @@ __device__ __forceinline__ void copy_tile(const uint8_t* src, int64_t bytes, uin
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) {
       const uintptr_t a = a0 + (static_cast<uintptr_t>(k) * kThreads + threadIdx.x) * 16;
-      if (a >= d0 && a + 16 <= end) v[k] = __ldcs(reinterpret_cast<const uint4*>(src + (a - d0)));
+      if (a >= d0 && a + 16 <= end &&
+          ZCHECK(s_lo + (a - d0) + 16 <= s_hi, kSiteGather, static_cast<int64_t>(a - d0)))
+        v[k] = __ldcs(reinterpret_cast<const uint4*>(src + (a - d0)));
     }
   } else {
     uint4 blk[kVecs], nxt[kVecs];
@@ -106,10 +109,15 @@ __device__ __forceinline__ void copy_tile(const uint8_t* src, int64_t bytes, uin
       const intptr_t rel = static_cast<intptr_t>(a - d0);  // negative before the piece
       const uintptr_t b = s_lo + static_cast<uintptr_t>(rel) - static_cast<uintptr_t>(d);
       const bool holds = rel + 16 - d > 0 && b < s_hi;
-      blk[k] = holds ? __ldcs(reinterpret_cast<const uint4*>(b)) : make_uint4(0, 0, 0, 0);
+      // a block read must hold a byte of the source (the rest of its 16 bytes
+      // lie in the same allocation granule)
+      blk[k] = holds && ZCHECK(b + 16 > s_lo && b < s_hi, kSiteGather, rel)
+                   ? __ldcs(reinterpret_cast<const uint4*>(b))
+                   : make_uint4(0, 0, 0, 0);
       const bool full = a >= d0 && a + 16 <= end;
-      nxt[k] = (lane == 31 && full) ? __ldcs(reinterpret_cast<const uint4*>(b + 16))
-                                    : make_uint4(0, 0, 0, 0);
+      nxt[k] = (lane == 31 && full && ZCHECK(b + 16 < s_hi, kSiteGather, rel))
+                   ? __ldcs(reinterpret_cast<const uint4*>(b + 16))
+                   : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int k = 0; k < kVecs; ++k) {
@@ -221,6 +229,13 @@ int copy_units(const zero_unit_plan* plan, int32_t unit_lo, int32_t unit_hi,
 }
 
 }  // namespace zg
+
+#ifdef ZERO_CHECKED
+// this unit's counters, for zero_checked_status
+extern "C" int zg_collect_checks(unsigned long long* count, unsigned long long* first) {
+  return collect_checks(count, first);
+}
+#endif
 
 extern "C" {
 

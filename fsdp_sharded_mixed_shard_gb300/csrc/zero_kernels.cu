@@ -46,6 +46,7 @@
 #include <mutex>
 #include <vector>
 
+#include "checked.cuh"
 #include "zero_internal.h"
 
 namespace zk {
@@ -127,40 +128,10 @@ struct StepScalars {
   int skip;        // 1: nothing to do in this launch
 };
 
-// ----------------------------------------------------- checked builds --
-//
-// Built with -DZERO_CHECKED (libzero_checked.so), every kernel tests the
-// global and shared-memory ranges it is about to touch against the extents
-// the plan gives (window, shard, records, stage slot). A failing test skips
-// the access, counts the violation and keeps the first one (site << 48 |
-// low 48 bits of the index) for zero_checked_status; nothing traps. The
-// release build compiles every test away.
-enum CheckSite : int {
-  kSiteSelftest = 1,
-  kSiteScalar = 2,
-  kSiteVector = 3,
-  kSiteRepCopy = 4,
-  kSiteAccCopy = 5,
-  kSiteStateCopy = 6,
-  kSiteStageBytes = 7,
-  kSiteStore = 8,
-  kSiteRecord = 9,
-};
-#ifdef ZERO_CHECKED
-__device__ unsigned long long g_check_first;
-__device__ unsigned int g_check_count;
-__device__ __noinline__ bool check_failed(int site, int64_t where) {
-  atomicAdd(&g_check_count, 1u);
-  atomicCAS(&g_check_first, 0ull,
-            (static_cast<unsigned long long>(site) << 48) |
-                (static_cast<unsigned long long>(where) & 0xFFFFFFFFFFFFull));
-  return false;
-}
-#define ZCHECK(cond, site, where) ((cond) ? true : check_failed((site), (where)))
+// Checked builds: see checked.cuh.
 // one planted violation, to test the reporting path
+#ifdef ZERO_CHECKED
 __global__ void check_selftest_kernel() { (void)ZCHECK(threadIdx.x > 0, kSiteSelftest, 42); }
-#else
-#define ZCHECK(cond, site, where) true
 #endif
 
 // ------------------------------------------------------------ primitives --
@@ -1912,22 +1883,20 @@ ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns,
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
+#ifdef ZERO_CHECKED
+int zg_collect_checks(unsigned long long* count, unsigned long long* first);  // gather.cu (C linkage)
+#endif
+
 ZERO_API int zero_checked_status(int64_t* violations, int64_t* first, void* stream) {
   if (!violations || !first) return ZERO_EINVAL;
   *violations = 0;
   *first = 0;
 #ifdef ZERO_CHECKED
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ZERO_ECUDA;
-  unsigned int count = 0;
-  unsigned long long code = 0;
-  const unsigned int zero_count = 0;
-  const unsigned long long zero_code = 0;
-  if (cudaMemcpyFromSymbol(&count, zk::g_check_count, sizeof(count)) != cudaSuccess ||
-      cudaMemcpyFromSymbol(&code, zk::g_check_first, sizeof(code)) != cudaSuccess ||
-      cudaMemcpyToSymbol(zk::g_check_count, &zero_count, sizeof(zero_count)) != cudaSuccess ||
-      cudaMemcpyToSymbol(zk::g_check_first, &zero_code, sizeof(zero_code)) != cudaSuccess)
+  unsigned long long count = 0, code = 0;
+  if (collect_checks(&count, &code) != 0 || zg_collect_checks(&count, &code) != 0)
     return ZERO_ECUDA;
-  *violations = count;
+  *violations = static_cast<int64_t>(count);
   *first = static_cast<int64_t>(code);
   return ZERO_OK;
 #else
@@ -2047,7 +2016,8 @@ __global__ void __launch_bounds__(kAccThreads)
 #pragma unroll
     for (int u = 0; u < kAccQuads; ++u) {
       const int64_t q = q0 + u * stride;
-      if (q < nq) w[u] = __ldcs(src4 + q);
+      if (q < nq && ZCHECK(a.off + 4 * q + 4 <= a.off + a.len, kSiteAccumulate, q))
+        w[u] = __ldcs(src4 + q);
     }
     if (!a.first) {
 #pragma unroll

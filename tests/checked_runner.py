@@ -40,6 +40,32 @@ def cases():
     yield "odd_shard_scalar_paths", dict(wl=W.TINY_FLAT.scaled(numels=[100_003], steps=2))
 
 
+def gather_case():
+    """All-gather and shard every unit of a pad-to-N layout whose slices sit
+    at every 16-byte phase; compare with the checker byte for byte."""
+    import numpy as np
+    import torch
+    import oracle
+    from fsdp_sharded_mixed_shard_gb300 import harness
+    uw = W.UnitWorkload("ragged_units", [1, 3, 5, 7, 1001, 40_097, 3, 11, 77_777],
+                        [0, 1, 1, 2, 3, 2, 4, 0, 4], 5, 7, 1, seed=3)
+    g = harness.UnitGroup(uw, window=1)
+    g.fill_shards()
+    torch.cuda.synchronize()
+    shards = [np.ascontiguousarray(g.shards[r].cpu().numpy().view(np.uint16)) for r in range(7)]
+    _, units, _, _ = oracle.make_unit_plan(uw.numels, uw.unit_of_tensor, uw.n_units, 7, 1)
+    for u, ou in enumerate(units):
+        g.gather(u, u + 1)
+        torch.cuda.synchronize()
+        got = g.buffers[0, :ou.psi_pad].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, oracle.gather_unit(ou, shards)), u
+        g.shard(u, u + 1)
+    torch.cuda.synchronize()
+    assert all(np.array_equal(g.shards[r].cpu().numpy().view(np.uint16), shards[r])
+               for r in range(7))
+    g.close()
+
+
 def main():
     Z.zero_selftest_check()
     n, first = Z.zero_checked_status()
@@ -48,6 +74,9 @@ def main():
         run_small(kw["wl"])
         n, first = Z.zero_checked_status()
         print(json.dumps({"case": name, "violations": n, "first": first}), flush=True)
+    gather_case()
+    n, first = Z.zero_checked_status()
+    print(json.dumps({"case": "unit_gather", "violations": n, "first": first}), flush=True)
     print(json.dumps({"case": "library", "path": Z._build.ZERO_CHECKED_LIB,
                       "loaded": Z.lib()._name}), flush=True)
 
