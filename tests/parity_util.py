@@ -1,5 +1,8 @@
 """Shared helpers of the GPU parity tests: run a workload through libzero and
 through the CPU checker on the same seeded inputs and compare."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -79,6 +82,31 @@ def compare_scaler(dev, orc, n_elems, clip):
                 2.0 ** -23 * abs(float(orc.clip_coef))
 
 
+def report(wl, step, mode, n_compared, dev, orc, got, want, flags_equal):
+    """One JSON line of parity statistics per workload and step, appended to
+    the file named by PARITY_REPORT (no-op when unset)."""
+    path = os.environ.get("PARITY_REPORT")
+    if not path:
+        return
+    gm, gmm, gv, gp = got
+    m, mm, v, p = want
+    gp = np.asarray(gp, np.uint16)
+    p = np.asarray(p, np.uint16)
+    rec = {"workload": wl.name, "step": step, "mode": mode, "elements": int(n_compared),
+           "master_max_rel": rel_err(gm, m), "exp_avg_max_rel": rel_err(gmm, mm),
+           "exp_avg_sq_max_rel": rel_err(gv, v),
+           "master_bit_exact": bool(np.array_equal(np.asarray(gm, np.float32).view(np.uint32),
+                                                   np.asarray(m, np.float32).view(np.uint32))),
+           "params_exact_frac": float((gp == p).mean()) if gp.size else 1.0,
+           "params_max_ulp": int(ulp_diff16(gp, p).max()) if gp.size else 0,
+           "flags_equal": bool(flags_equal), "t": dev.t, "t_checker": orc.t,
+           "scale": dev.scale, "scale_checker": orc.scale, "overflow": dev.overflow,
+           "norm_rel_diff": (abs(dev.norm_sq - orc.norm_sq) / orc.norm_sq
+                             if orc.norm_sq > 0 else 0.0)}
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
 def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True):
     """Full element-wise comparison over every step of `wl`. Returns the
     per-step max relative errors for reporting."""
@@ -131,9 +159,11 @@ def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True):
             if check_replicas and wlen:
                 assert np.array_equal(g.replicas_u16(), np.stack(reps)), "generator parity"
             dev = g.read_scaler()
+            gm, gmm, gv = (t.numpy() for t in g.current_state())
+            report(wl, step, "full", wlen, dev, sc, (gm, gmm, gv, g.params_u16()),
+                   (master, m, v, params), np.array_equal(g.flags_u32(), flags[:p.n_buckets]))
             compare_scaler(dev, sc, wlen, wl.max_grad_norm > 0)
             assert np.array_equal(g.flags_u32(), flags[:p.n_buckets])
-            gm, gmm, gv = (t.numpy() for t in g.current_state())
             assert_state(gm, master, "master")
             assert_state(gmm, m, "exp_avg")
             assert_state(gv, v, "exp_avg_sq")
@@ -213,9 +243,11 @@ def run_sampled(wl, steps=None, n_random=2048, n_threads=None):
             oracle.gen_step(p, lo, hi, gen, step, elems, master, m, v, params, hp, sc, flags,
                             n_threads=n_threads)
             dev = g.read_scaler()
+            gm, gmm, gv, gp = gather_state(g, elems)
+            report(wl, step, "sampled", len(elems), dev, sc, (gm, gmm, gv, gp),
+                   (master, m, v, params), np.array_equal(g.flags_u32(), flags[:p.n_buckets]))
             compare_scaler(dev, sc, (hi - lo) * p.shard, wl.max_grad_norm > 0)
             assert np.array_equal(g.flags_u32(), flags[:p.n_buckets])
-            gm, gmm, gv, gp = gather_state(g, elems)
             assert_state(gm, master, "master")
             assert_state(gmm, m, "exp_avg")
             assert_state(gv, v, "exp_avg_sq")
