@@ -33,6 +33,7 @@
 #include <new>
 
 #include "checked.cuh"
+#include "pdl.cuh"
 #include "zero_internal.h"
 #include "zero_units_internal.h"
 
@@ -146,6 +147,7 @@ __device__ __forceinline__ void copy_tile(const uint8_t* src, int64_t bytes, uin
 }
 
 __global__ void __launch_bounds__(kThreads) copy_kernel(const __grid_constant__ Args a) {
+  pdl_begin();
   for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     // the piece holding tile t: the last one whose first tile is <= t
     int lo = 0, hi = a.n_pieces - 1;
@@ -167,10 +169,10 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const __grid_constant__ 
 int flush(Args& a, cudaStream_t stream) {
   if (a.n_pieces == 0) return ZERO_OK;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(a.n_tiles, kMaxGrid));
-  copy_kernel<<<grid, kThreads, 0, stream>>>(a);
+  const cudaError_t e = launch_pdl(copy_kernel, dim3(grid), dim3(kThreads), 0, stream, a);
   a.n_pieces = 0;
   a.n_tiles = 0;  // stream_stores is kept for the next batch
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  return e == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
 // gather: shards -> unit buffers; otherwise unit buffers -> shards

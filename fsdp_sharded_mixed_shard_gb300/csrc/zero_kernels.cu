@@ -47,6 +47,7 @@
 #include <vector>
 
 #include "checked.cuh"
+#include "pdl.cuh"
 #include "zero_internal.h"
 
 namespace zk {
@@ -622,6 +623,7 @@ template <int MODE, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ Args a) {
   __shared__ StepScalars sh_s;
   __shared__ NormSlots sh_norm;
+  pdl_begin();
   if (threadIdx.x == 0) compute_step_scalars<MODE>(a, &sh_s);
   __syncthreads();
   const StepScalars s = sh_s;
@@ -1015,6 +1017,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   __shared__ int sh_abort;
   extern __shared__ __align__(128) unsigned char stage_mem[];
 
+  pdl_begin();
   if (threadIdx.x == 0) {
     compute_step_scalars<MODE>(a, &sh_s);
     for (int i = 0; i < n_slots; ++i) {
@@ -1357,6 +1360,7 @@ __device__ NormAcc cta_merge(NormAcc t, float4* sh) {
 __global__ void __launch_bounds__(kFinishThreads) norm_blocks_kernel(
     const float4* __restrict__ records, int64_t t0, int64_t t1, float4* __restrict__ out) {
   __shared__ float4 sh[kFinishThreads / 32];
+  pdl_begin();
   const int64_t n = t1 - t0;
   const int64_t chunk = (n + kFinishBlocks - 1) / kFinishBlocks;
   const int64_t b0 = t0 + blockIdx.x * chunk;
@@ -1373,6 +1377,7 @@ __global__ void __launch_bounds__(kFinishThreads) norm_blocks_kernel(
 __global__ void __launch_bounds__(kFinishThreads) norm_final_kernel(
     const float4* __restrict__ blocks, double max_norm, zero_scaler* sc) {
   __shared__ float4 sh[kFinishThreads / 32];
+  pdl_begin();
   NormAcc t;
   for (int i = threadIdx.x; i < kFinishBlocks; i += kFinishThreads) {
     const float4 q = blocks[i];
@@ -1397,14 +1402,18 @@ __global__ void __launch_bounds__(kFinishThreads) norm_final_kernel(
 
 int launch_norm_finish(const float4* records, int64_t t0, int64_t t1, float4* blocks,
                        double max_norm, zero_scaler* sc, cudaStream_t st) {
-  norm_blocks_kernel<<<kFinishBlocks, kFinishThreads, 0, st>>>(records, t0, t1, blocks);
-  norm_final_kernel<<<1, kFinishThreads, 0, st>>>(blocks, max_norm, sc);
+  if (launch_pdl(norm_blocks_kernel, dim3(kFinishBlocks), dim3(kFinishThreads), 0, st, records, t0,
+                 t1, blocks) != cudaSuccess ||
+      launch_pdl(norm_final_kernel, dim3(1), dim3(kFinishThreads), 0, st,
+                 static_cast<const float4*>(blocks), max_norm, sc) != cudaSuccess)
+    return ZERO_ECUDA;
   return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
 }
 
 // Bookkeeping alone (two-pass path, and plans without elements).
 __global__ void scaler_finish_kernel(zero_scaler* sc, double beta1, double beta2, int dynamic,
                                      int growth_interval, int flip_sets) {
+  pdl_begin();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   step_bookkeeping(sc, beta1, beta2, dynamic, growth_interval, flip_sets);
 }
@@ -1503,8 +1512,10 @@ int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
     return ZERO_ECUDA;
   const int64_t cap = static_cast<int64_t>(sms) * std::max(per_sm, 1);
   const int grid = static_cast<int>(std::min<int64_t>(tiles, cap));
-  kern<<<grid, kBulkThreads, smem, stream>>>(a, slots, slot_bytes);
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  return launch_pdl(kern, dim3(grid), dim3(kBulkThreads), smem, stream, a, slots, slot_bytes) ==
+                 cudaSuccess
+             ? ZERO_OK
+             : ZERO_ECUDA;
 }
 
 // The reduce pass moves few bytes per element at small N, so its fixed
@@ -1567,8 +1578,9 @@ int launch_mode(const zero_plan* p, Args& a, int32_t seg_begin, int32_t seg_end,
       if (rc) return rc;
     } else {
       const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
-      step_kernel<MODE, kBf16><<<grid, kThreads, 0, stream>>>(a);
-      if (cudaGetLastError() != cudaSuccess) return ZERO_ECUDA;
+      if (launch_pdl(step_kernel<MODE, kBf16>, dim3(grid), dim3(kThreads), 0, stream, a) !=
+          cudaSuccess)
+        return ZERO_ECUDA;
     }
   }
   return ZERO_OK;
@@ -1870,9 +1882,10 @@ ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t ra
     return rc;
   }
   delete a;
-  scaler_finish_kernel<<<1, 32, 0, st>>>(d_scaler, hp->beta1, hp->beta2, hp->dynamic_scale,
-                                         hp->growth_interval, fused ? 1 : 0);
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  if (launch_pdl(scaler_finish_kernel, dim3(1), dim3(32), 0, st, d_scaler, hp->beta1, hp->beta2,
+                 hp->dynamic_scale, hp->growth_interval, fused ? 1 : 0) != cudaSuccess)
+    return ZERO_ECUDA;
+  return ZERO_OK;
 }
 
 ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns, void* stream) {
@@ -2002,6 +2015,7 @@ __device__ __forceinline__ float4 widen4(const uint2& w) {
 template <bool kBf16>
 __global__ void __launch_bounds__(kAccThreads)
     accumulate_kernel(const __grid_constant__ AccArgs a) {
+  pdl_begin();
   const int r = blockIdx.y;
   const uint16_t* src = a.micro[r] + a.off;
   float* dst = a.acc[r] + a.off;
@@ -2086,9 +2100,14 @@ extern "C" ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, 
     // about 8 CTAs per SM in all, split evenly over the replicas
     const dim3 grid(static_cast<unsigned>(std::max(1, sms * 8 / N)), static_cast<unsigned>(N));
     if (plan->info.grad_dtype == ZERO_BF16)
-      accumulate_kernel<true><<<grid, kAccThreads, 0, st>>>(*a);
+      rc = launch_pdl(accumulate_kernel<true>, grid, dim3(kAccThreads), 0, st, *a) == cudaSuccess
+               ? ZERO_OK
+               : ZERO_ECUDA;
     else
-      accumulate_kernel<false><<<grid, kAccThreads, 0, st>>>(*a);
+      rc = launch_pdl(accumulate_kernel<false>, grid, dim3(kAccThreads), 0, st, *a) ==
+                   cudaSuccess
+               ? ZERO_OK
+               : ZERO_ECUDA;
     if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
   }
   delete a;
@@ -2180,7 +2199,9 @@ extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t ra
     const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
     // the kNorm body only reads fp32 gradients, so one instantiation serves
     // both 16-bit formats
-    step_kernel<kNorm, true><<<grid, kThreads, 0, st>>>(*a);
+    if (launch_pdl(step_kernel<kNorm, true>, dim3(grid), dim3(kThreads), 0, st, *a) !=
+        cudaSuccess)
+      rc = ZERO_ECUDA;
     if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
   }
   delete a;
