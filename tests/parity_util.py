@@ -194,6 +194,9 @@ def sample_elems(wl, p, n_random=2048, seed=0):
         pts.add(p.psi + d)
     if wl.inject is not None:
         pts.add(wl.inject[2])
+    for edge in (2 ** 31, 2 ** 32):  # where 32-bit index arithmetic would wrap
+        for d in (-2, -1, 0, 1, 2):
+            pts.add(edge + d)
     rng = np.random.default_rng(seed)
     if b > a:
         pts.update(rng.integers(a, b, n_random).tolist())
