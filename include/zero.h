@@ -57,6 +57,12 @@
  *     buffers are safe. Calls that share a scaler or buffers must be ordered
  *     by the caller.
  *   - Element indices are int64 (N * psi may exceed 2^31).
+ *   - Kernels are launched with programmatic stream serialization: each
+ *     waits for the previous grid in the stream before touching memory and
+ *     lets the next one be scheduled early. A caller kernel launched after a
+ *     library call behaves as with any launch, unless the caller gives it
+ *     that launch attribute too; then it must wait (griddepcontrol.wait)
+ *     before reading the library's results.
  */
 #ifndef ZERO_H
 #define ZERO_H
