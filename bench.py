@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--micro", type=int, default=1,
                     help="micro-batches per optimizer step, accumulated in fp32 (>= 1)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one whole step into a CUDA graph and replay it in the timed loop")
     ap.add_argument("--gather", action="store_true",
                     help="time the stage-3 unit all-gather (forward and backward gathers of "
                          "every unit) on the 8.81B-parameter layout at 64 ranks instead")
@@ -228,7 +230,8 @@ def run_libzero(args, rank, world, dist):
         wl = truncated(wl, args.numel_cap)
     if args.micro > 1:
         wl = wl.scaled(name="%s_micro%d" % (wl.name, args.micro), n_micro=args.micro)
-    g = harness.Group(wl, device=dev)
+    # a graph is captured on a stream of its own (the legacy default stream cannot be captured)
+    g = harness.Group(wl, device=dev, stream=torch.cuda.Stream(device=dev) if args.graph else None)
     path = "two_pass" if g.two_pass else "fused"
     g.init_state()
     g.gen_grads(1)
@@ -288,6 +291,16 @@ def run_libzero(args, rank, world, dist):
         for _, f in ph:
             f()
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # one whole step as a CUDA graph: the device-resident scaler carries
+        # the step count, loss scale and ping-pong set, so replays need no
+        # host logic
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=g.stream):
+            for _, f in ph:
+                f()
+        torch.cuda.synchronize()
 
     K = args.steps
     # Phase events on every PHASE_SAMPLE-th timed step only: an event between
@@ -308,8 +321,12 @@ def run_libzero(args, rank, world, dist):
     t0.record(g.stream)
     for k in range(K):
         if k % PHASE_SAMPLE:
-            for _, f in ph:
-                f()
+            if graph is not None:
+                with torch.cuda.stream(g.stream):  # replay() launches on the current stream
+                    graph.replay()
+            else:
+                for _, f in ph:
+                    f()
             continue
         for name, f in ph:
             a, b = evs[name][ev_i[name]]
@@ -466,6 +483,8 @@ def run_libzero(args, rank, world, dist):
             "clocks": clk, "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
             "phase_events": "per-kernel CUDA events on every %d-th timed step (%d of %d)"
                             % (PHASE_SAMPLE, len(sampled), K),
+            "launch": "CUDA graph replay of one captured step (eager on event steps)"
+                      if graph is not None else "eager C-ABI calls",
             "wall_s_timed": round(wall, 3), "scaler_t": sk.t, "device_error": sk.error}
     return line
 
