@@ -376,7 +376,7 @@ def run_libzero(args, rank, world, dist):
                 "step_bytes_per_param": step_bytes / pstep,
                 "step_achieved_gbs": round(step_bytes / (ms_per_step / 1e3) / 1e9, 1),
                 "step_frac": round(step_bytes / (ms_per_step / 1e3) / 1e9 / peak, 4),
-                "north_star_frac_2n26": round((2 * N + 26) * pstep / (ms_per_step / 1e3) / 1e9
+                "frac_of_2n26_bytes": round((2 * N + 26) * pstep / (ms_per_step / 1e3) / 1e9
                                               / peak, 4),
                 "kernel_gbs": kernel_gbs}
 
