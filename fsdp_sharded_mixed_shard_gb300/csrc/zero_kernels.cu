@@ -619,6 +619,58 @@ __device__ __forceinline__ void do_scalar(const Args& a, const StepScalars& s, i
   }
 }
 
+// One edge element of a tile by a whole warp (kFused / kReduce): lane p
+// loads the replica values at ring positions p and p + 32, so all N loads
+// are in flight together, and every lane adds them in ring order through
+// shuffles (the same operations in the same order as do_scalar); lane 0
+// then finishes the element. Used when a tile has only a few elements
+// outside its aligned body: the per-thread path would chain N dependent
+// global loads on one thread and hold up the whole tile.
+template <int MODE, bool kBf16>
+__device__ __forceinline__ void do_scalar_warp(const Args& a, const StepScalars& s, int64_t j,
+                                               int32_t rank, int first_rep, NormAcc& nacc,
+                                               bool& bad, int lane) {
+  static_assert(MODE == kFused || MODE == kReduce, "replica modes only");
+  const int64_t w = j - a.wbase;
+  const int64_t k = j - static_cast<int64_t>(rank) * a.shard;
+  if (!ZCHECK(w >= 0 && w < a.wend && k >= 0 && k < a.shard, kSiteScalar, j)) return;
+  const int N = a.n_ranks;
+  float x0 = 0.f, x1 = 0.f;
+  if (lane < N) {
+    int rr = first_rep + lane;
+    if (rr >= N) rr -= N;
+    x0 = widen<kBf16>(a.rep[rr][w]);
+    if (a.has_acc) x0 = __fadd_rn(a.acc[rr][w], x0);
+  }
+  if (lane + 32 < N) {
+    int rr = first_rep + lane + 32;
+    if (rr >= N) rr -= N;
+    x1 = widen<kBf16>(a.rep[rr][w]);
+    if (a.has_acc) x1 = __fadd_rn(a.acc[rr][w], x1);
+  }
+  float acc = 0.f;
+  for (int p = 0; p < N; ++p) {
+    const float x = __shfl_sync(0xFFFFFFFFu, p < 32 ? x0 : x1, p & 31);
+    acc = p == 0 ? x : __fadd_rn(acc, x);
+  }
+  if (lane != 0) return;
+  const float g = __fmul_rn(acc, s.inv);
+  bad |= nonfinite(g);
+  if constexpr (MODE == kReduce) {
+    a.ghat[rank][k] = g;
+    if (a.mode_flags & kFlagPartials) nacc.add(g);
+  } else {
+    float th = a.master[s.src][rank][k];
+    float m = a.mom[s.src][rank][k];
+    float v = a.var[s.src][rank][k];
+    adamw(th, m, v, g, a, s);
+    a.master[s.dst][rank][k] = th;
+    a.mom[s.dst][rank][k] = m;
+    a.var[s.dst][rank][k] = v;
+    a.flat[w] = narrow<kBf16>(th);
+  }
+}
+
 template <int MODE, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ Args a) {
   __shared__ StepScalars sh_s;
@@ -1145,12 +1197,25 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     NormAcc nacc;
     uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
-    // unaligned head [lo, va) and tail [vb, hi) with plain loads
+    // unaligned head [lo, va) and tail [vb, hi) with plain loads: a few
+    // edge elements (at most 7 on each side of an aligned body) one warp
+    // each, a whole unaligned tile one thread per element (coalesced)
     const int nhead = static_cast<int>(t.va - t.lo);
     const int ntail = static_cast<int>(t.hi - t.vb);
-    for (int q = tid; q < nhead + ntail; q += kConsumers) {
-      const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
-      do_scalar<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad);
+    bool by_warp = false;
+    if constexpr (MODE == kFused || MODE == kReduce) by_warp = nhead + ntail <= 2 * kConsumerWarps;
+    if (by_warp) {
+      if constexpr (MODE == kFused || MODE == kReduce) {
+        for (int q = warp; q < nhead + ntail; q += kConsumerWarps) {
+          const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
+          do_scalar_warp<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad, lane);
+        }
+      }
+    } else {
+      for (int q = tid; q < nhead + ntail; q += kConsumers) {
+        const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
+        do_scalar<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad);
+      }
     }
     const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
     for (int64_t j0 = t.va; j0 < t.vb; j0 += E) {
