@@ -91,16 +91,23 @@ class Group:
         return [base + r * rb for r in range(self.N)]
 
     def _state_ptrs(self, which):
+        """Per-set, per-rank shard addresses of one optimizer array (computed
+        arithmetically: indexing the tensor per rank costs microseconds each)."""
         out = [None] * (self.n_sets * self.N)
+        base = self.state.data_ptr()
+        sset = self.state.stride(0) * 4
+        sarr = self.state.stride(1) * 4
+        srank = self.state.stride(2) * 4
         for s in range(self.n_sets):
             for i in range(self.lo, self.hi):
-                out[s * self.N + i] = self.state[s, which, i - self.lo].data_ptr()
+                out[s * self.N + i] = base + s * sset + which * sarr + (i - self.lo) * srank
         return out
 
     def ghat_ptrs(self):
         out = [None] * self.N
+        base, srank = self.ghat.data_ptr(), self.ghat.stride(0) * 4
         for i in range(self.lo, self.hi):
-            out[i] = self.ghat[i - self.lo].data_ptr()
+            out[i] = base + (i - self.lo) * srank
         return out
 
     # ----------------------------------------------------------------- init
