@@ -1197,26 +1197,6 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     NormAcc nacc;
     uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
-    // unaligned head [lo, va) and tail [vb, hi) with plain loads: a few
-    // edge elements (at most 7 on each side of an aligned body) one warp
-    // each, a whole unaligned tile one thread per element (coalesced)
-    const int nhead = static_cast<int>(t.va - t.lo);
-    const int ntail = static_cast<int>(t.hi - t.vb);
-    bool by_warp = false;
-    if constexpr (MODE == kFused || MODE == kReduce) by_warp = nhead + ntail <= 2 * kConsumerWarps;
-    if (by_warp) {
-      if constexpr (MODE == kFused || MODE == kReduce) {
-        for (int q = warp; q < nhead + ntail; q += kConsumerWarps) {
-          const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
-          do_scalar_warp<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad, lane);
-        }
-      }
-    } else {
-      for (int q = tid; q < nhead + ntail; q += kConsumers) {
-        const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
-        do_scalar<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad);
-      }
-    }
     const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
     for (int64_t j0 = t.va; j0 < t.vb; j0 += E) {
       const int len = static_cast<int>(min(static_cast<int64_t>(E), t.vb - j0));
@@ -1327,6 +1307,27 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[cur]);
+      }
+    }
+    // unaligned head [lo, va) and tail [vb, hi) with plain loads, after the
+    // aligned body so that the producer streams the next tile meanwhile: a few
+    // edge elements (at most 7 on each side of an aligned body) one warp
+    // each, a whole unaligned tile one thread per element (coalesced)
+    const int nhead = static_cast<int>(t.va - t.lo);
+    const int ntail = static_cast<int>(t.hi - t.vb);
+    bool by_warp = false;
+    if constexpr (MODE == kFused || MODE == kReduce) by_warp = nhead + ntail <= 2 * kConsumerWarps;
+    if (by_warp) {
+      if constexpr (MODE == kFused || MODE == kReduce) {
+        for (int q = warp; q < nhead + ntail; q += kConsumerWarps) {
+          const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
+          do_scalar_warp<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad, lane);
+        }
+      }
+    } else {
+      for (int q = tid; q < nhead + ntail; q += kConsumers) {
+        const int64_t j = q < nhead ? t.lo + q : t.vb + (q - nhead);
+        do_scalar<MODE, kBf16>(a, s, j, t.rank, t.first_rep, nacc, bad);
       }
     }
     if constexpr (MODE == kFused || MODE == kReduce) {
