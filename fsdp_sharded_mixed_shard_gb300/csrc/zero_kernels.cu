@@ -870,6 +870,7 @@ __device__ __forceinline__ void consumer_sync() {
 struct TileGeom {
   int64_t lo, hi, va, vb, partial;
   int32_t rank, bucket, first_rep;
+  int32_t shift;  // 16-bit elements between a replica copy's aligned start and va (shifted bodies)
 };
 
 // a0 += low half of w, a1 += high half of w, each 16-bit value widened
@@ -1030,11 +1031,71 @@ __device__ __forceinline__ void stg_hv(uint16_t* p, const float (&x)[EPT]) {
   }
 }
 
-// Tile g of this launch: element range, owner, and the 16-byte aligned body
-// [va, vb) (empty when the owner's shard and the windows are misaligned).
+// The four 16-bit values that start `shift` elements (0 < shift < 8) past p
+// in shared memory (p 8-byte aligned, 24 bytes readable): three aligned
+// 8-byte loads, a word select (two steps) and, for an odd shift, a funnel
+// shift.
+__device__ __forceinline__ uint2 halves_at(const unsigned char* p, int shift) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p);
+  const uint2 b = *reinterpret_cast<const uint2*>(p + 8);
+  const uint2 c = *reinterpret_cast<const uint2*>(p + 16);
+  const uint32_t wd[6] = {a.x, a.y, b.x, b.y, c.x, c.y};
+  const int q = shift >> 1;  // whole 32-bit words to skip
+  uint32_t t[4], u[3];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) t[j] = (q & 2) ? wd[j + 2] : wd[j];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) u[j] = (q & 1) ? t[j + 1] : t[j];  // u[j] = wd[q + j]
+  if (shift & 1)
+    return make_uint2(__funnelshift_r(u[0], u[1], 16), __funnelshift_r(u[1], u[2], 16));
+  return make_uint2(u[0], u[1]);
+}
+
+// acc[e] += replica chunks 0..n-1 of this thread's 4 elements, in ring
+// order, for a shifted body: the thread's first element sits `shift`
+// elements past rp in each chunk. The same additions in the same order as
+// acc_stage.
+template <bool kBf16>
+__device__ __forceinline__ void acc_stage_shifted(const unsigned char* rp, int stride, int n,
+                                                  int shift, float (&acc)[4]) {
+#pragma unroll 4
+  for (int p = 0; p < n; ++p) {
+    const uint2 w = halves_at(rp + static_cast<size_t>(p) * stride, shift);
+    add_halves<kBf16>(acc[0], acc[1], w.x);
+    add_halves<kBf16>(acc[2], acc[3], w.y);
+  }
+}
+
+// 16-bit parameter stores at a window index that is not a multiple of 4:
+// two 4-byte stores when it is even, four 2-byte stores otherwise.
+template <bool kBf16>
+__device__ __forceinline__ void stg_hv_unaligned(uint16_t* p, const float (&x)[4]) {
+  const unsigned int h0 = narrow<kBf16>(x[0]), h1 = narrow<kBf16>(x[1]);
+  const unsigned int h2 = narrow<kBf16>(x[2]), h3 = narrow<kBf16>(x[3]);
+  if ((reinterpret_cast<uintptr_t>(p) & 3) == 0) {
+    unsigned int* q = reinterpret_cast<unsigned int*>(p);
+    __stcs(q, h0 | (h1 << 16));
+    __stcs(q + 1, h2 | (h3 << 16));
+  } else {
+    unsigned short* q = reinterpret_cast<unsigned short*>(p);
+    __stcs(q, static_cast<unsigned short>(h0));
+    __stcs(q + 1, static_cast<unsigned short>(h1));
+    __stcs(q + 2, static_cast<unsigned short>(h2));
+    __stcs(q + 3, static_cast<unsigned short>(h3));
+  }
+}
+
+// Tile g of this launch: element range, owner, and the aligned body
+// [va, vb). When the owner's shard and the windows share a 4-element phase
+// the body starts where the window index is a multiple of 8 (16-byte
+// replica chunks, 16-byte state chunks). Otherwise, if `shifted` is
+// allowed, the body starts where the shard index is a multiple of 4
+// (16-byte state chunks) and each replica chunk is copied from the 16-byte
+// block below its first element: `shift` elements earlier. Without either,
+// the body is empty and the tile goes element by element.
 // (A forward scan from the previous tile's segment measured slower than this
 // binary search.)
-__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
+__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shifted) {
   const Seg& sg = a.segs[find_seg(a, g)];
   TileGeom t;
   t.lo = sg.lo + (g - sg.tile_local0) * kTile;
@@ -1043,12 +1104,17 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g) {
   t.bucket = sg.bucket;
   t.partial = sg.tile_global0 + (g - sg.tile_local0);
   t.first_rep = sg.rank + 1 == a.n_ranks ? 0 : sg.rank + 1;
+  t.shift = 0;
   const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
   t.va = t.hi;
   t.vb = t.hi;
   if (((rank0 - a.wbase) & 3) == 0) {
     t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
     t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
+  } else if (shifted) {
+    t.va = min(t.lo + ((rank0 - t.lo) & 3), t.hi);
+    t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
+    t.shift = static_cast<int32_t>((t.va - a.wbase) & 7);
   }
   return t;
 }
@@ -1059,6 +1125,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
   constexpr int kRepBytes = kAcc ? 6 : 2;  // per replica and element: 16-bit value (+ fp32 accumulator)
+  // shifted bodies (owner shard and windows out of phase): 4 elements per
+  // thread, no accumulators; each replica chunk then holds up to 7 extra
+  // elements, so chunks are 16 bytes longer
+  constexpr bool kShift = EPT == 4 && !kAcc && (MODE == kFused || MODE == kReduce);
+  constexpr int kRepChunk = 2 * E + (kShift ? 16 : 0);         // bytes per replica chunk
+  constexpr int kRepBlock = kAcc ? kRepBytes * E : kRepChunk;  // per replica in a stage
   __shared__ StepScalars sh_s;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -1097,12 +1169,15 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     uint32_t phase = 0;  // == (it / n_slots) & 1
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
-      const TileGeom t = tile_geom(a, g);
+      const TileGeom t = tile_geom(a, g, kShift);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
       for (int64_t j0 = t.va; j0 < t.vb && !stop; j0 += E) {
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
         const int64_t w = j0 - a.wbase;
         const int64_t kk = j0 - rank0;
+        // replica copies start at the 16-byte block holding element w
+        const int64_t rw = w - t.shift;
+        const uint32_t rlen = t.shift ? ((len + t.shift + 7) & ~7u) : len;
         for (int st = 0; st < n_plan; ++st, ++it) {
           int go = 1;
           if (lane == 0) {
@@ -1113,8 +1188,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
               *abort_flag = 1;
               go = 0;
             } else {
+              const uint32_t nr = static_cast<uint32_t>(a.plan.r_hi[st] - a.plan.r_lo[st]);
+              const uint32_t ns = a.plan.states[st] ? (MODE == kUpdate ? 4u : 3u) : 0u;
               mbar_expect_tx(&full_bar[slot],
-                             len * static_cast<uint32_t>(a.plan.bytes_per_elem[st]));
+                             nr * (2 * rlen + (kAcc ? 4 * len : 0)) + ns * 4 * len);
             }
           }
           if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
@@ -1130,9 +1207,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             if (c < n_rep) {
               int rr = t.first_rep + r_lo + c;
               if (rr >= N) rr -= N;
-              if (ZCHECK(w >= 0 && w + len <= a.wend, kSiteRepCopy, w) &&
-                  ZCHECK((c + 1) * (2 * E) <= static_cast<int>(slot_bytes), kSiteStageBytes, c))
-                bulk_g2s(buf + static_cast<size_t>(c) * (2 * E), a.rep[rr] + w, len * 2,
+              // a shifted copy may read the rest of the 16-byte block that
+              // holds the window's last element
+              if (ZCHECK(rw >= 0 && rw + rlen <= ((a.wend + 7) & ~static_cast<int64_t>(7)),
+                         kSiteRepCopy, w) &&
+                  ZCHECK(c * kRepChunk + 2 * rlen <= slot_bytes, kSiteStageBytes, c))
+                bulk_g2s(buf + static_cast<size_t>(c) * kRepChunk, a.rep[rr] + rw, rlen * 2,
                          &full_bar[slot], pol);
             } else if (kAcc && c < n_rep_chunks) {
               int rr = t.first_rep + r_lo + (c - n_rep);
@@ -1156,10 +1236,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                              : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
               }
               if (ZCHECK(kk >= 0 && kk + len <= a.shard, kSiteStateCopy, kk) &&
-                  ZCHECK(n_rep * (kRepBytes * E) + (q + 1) * (4 * E) <=
-                             static_cast<int>(slot_bytes),
+                  ZCHECK(n_rep * kRepBlock + (q + 1) * (4 * E) <= static_cast<int>(slot_bytes),
                          kSiteStageBytes, c))
-                bulk_g2s(buf + static_cast<size_t>(n_rep) * (kRepBytes * E) +
+                bulk_g2s(buf + static_cast<size_t>(n_rep) * kRepBlock +
                              static_cast<size_t>(q) * (4 * E),
                          src + kk, len * 4, &full_bar[slot], pol);
             }
@@ -1193,7 +1272,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   bool dead = false;
   const bool partials = MODE == kReduce && (a.mode_flags & kFlagPartials);
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
-    const TileGeom t = tile_geom(a, g);
+    const TileGeom t = tile_geom(a, g, kShift);
     NormAcc nacc;
     uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
@@ -1240,8 +1319,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                           buf + static_cast<size_t>(r_hi - r_lo) * (2 * E) +
                                               t_off * 4,
                                           E, r_hi - r_lo, acc);
-            else
-              acc_stage<kBf16, EPT>(buf + t_off * 2, 2 * E, r_hi - r_lo, acc);
+            else if constexpr (kShift) {
+              if (t.shift)
+                acc_stage_shifted<kBf16>(buf + t_off * 2, kRepChunk, r_hi - r_lo, t.shift, acc);
+              else
+                acc_stage<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, acc);
+            } else {
+              acc_stage<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, acc);
+            }
             if (completes) {
               const uint64_t inv2 = f2_pack(s.inv, s.inv);
 #pragma unroll
@@ -1280,7 +1365,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if (mine) {
           if constexpr (MODE == kFused || MODE == kUpdate) {
             if (a.plan.states[st]) {
-              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * (kRepBytes * E);
+              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * kRepBlock;
               if constexpr (MODE == kUpdate) {
                 lds_fv<EPT>(sb + t_off * 4, gv);
                 sb += 4 * E;
@@ -1300,7 +1385,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                 stg_fv<EPT>(a.master[s.dst][t.rank] + k, th);
                 stg_fv<EPT>(a.mom[s.dst][t.rank] + k, m);
                 stg_fv<EPT>(a.var[s.dst][t.rank] + k, v);
-                stg_hv<kBf16, EPT>(a.flat + w, th);
+                if constexpr (kShift) {
+                  if (t.shift)
+                    stg_hv_unaligned<kBf16>(a.flat + w, th);
+                  else
+                    stg_hv<kBf16, EPT>(a.flat + w, th);
+                } else {
+                  stg_hv<kBf16, EPT>(a.flat + w, th);
+                }
               }
             }
           }
@@ -1512,15 +1604,17 @@ int grid_size() {
 // stages of at most kStageBudget bytes: replica chunks (2 bytes per element
 // each, 6 with the fp32 accumulator beside it) in ring order, then the indivisible state block (kFused 12, kUpdate
 // 16 bytes per element) in the last stage if it fits, else in a stage of
-// its own.
-inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
+// its own. rep_extra bytes follow every replica chunk (the 16-byte block a
+// shifted body's chunk copies ahead of its first element); the slot holds
+// the largest stage.
+inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes, int rep_extra,
                                  uint32_t* slot_bytes) {
   StagePlan pl{};
   const int budget = kStageBudget / E;  // bytes per element
   const int n_rep = mode == kUpdate ? 0 : n_ranks;
   const int state_bpe = mode == kFused ? 12 : (mode == kUpdate ? 16 : 0);
   int lo = 0, cur = 0;
-  int max_bpe = 0;
+  int64_t max_bytes = 0;
   bool overflow = false;
   auto close = [&](int hi, int with_states) {
     const int bpe = rep_bytes * (hi - lo) + (with_states ? state_bpe : 0);
@@ -1532,7 +1626,8 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
     pl.r_hi[pl.n] = static_cast<int16_t>(hi);
     pl.states[pl.n] = with_states;
     pl.bytes_per_elem[pl.n] = bpe;
-    max_bpe = std::max(max_bpe, bpe);
+    max_bytes = std::max(max_bytes, static_cast<int64_t>(bpe) * E +
+                                        static_cast<int64_t>(rep_extra) * (hi - lo));
     ++pl.n;
     lo = hi;
     cur = 0;
@@ -1552,7 +1647,7 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes,
     close(n_rep, 0);
   }
   if (overflow) pl.n = 0;
-  *slot_bytes = static_cast<uint32_t>((max_bpe * E + 127) & ~127);
+  *slot_bytes = static_cast<uint32_t>((max_bytes + 127) & ~static_cast<int64_t>(127));
   return pl;
 }
 
@@ -1560,7 +1655,8 @@ template <int MODE, bool kBf16, int EPT, bool kAcc>
 int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
   constexpr int E = kConsumers * EPT;
   uint32_t slot_bytes = 0;
-  a.plan = make_stage_plan(MODE, a.n_ranks, E, kAcc ? 6 : 2, &slot_bytes);
+  constexpr int kRepExtra = EPT == 4 && !kAcc && (MODE == kFused || MODE == kReduce) ? 16 : 0;
+  a.plan = make_stage_plan(MODE, a.n_ranks, E, kAcc ? 6 : 2, kRepExtra, &slot_bytes);
   if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
   const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));
   if (slots < 2) return ZERO_ERANGE;
@@ -1594,8 +1690,15 @@ int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
   if constexpr (MODE == kFused || MODE == kReduce) {
     if (a.has_acc) return launch_bulk_ept<MODE, kBf16, 4, true>(a, tiles, stream);
   }
-  if (MODE == kReduce && 2 * a.n_ranks * kConsumers * 8 <= kStageBudget)
-    return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
+  if (MODE == kReduce && 2 * a.n_ranks * kConsumers * 8 <= kStageBudget) {
+    // 8 elements per thread only when every owner's slice shares the
+    // window's 4-element phase: the 4-element kernel keeps a bulk body
+    // (shifted replica copies) for owners out of phase
+    bool in_phase = true;
+    for (int i = 0; i < a.n_segs; ++i)
+      in_phase = in_phase && ((static_cast<int64_t>(a.segs[i].rank) * a.shard - a.wbase) & 3) == 0;
+    if (in_phase) return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
+  }
   return launch_bulk_ept<MODE, kBf16, 4, false>(a, tiles, stream);
 }
 

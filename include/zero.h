@@ -216,7 +216,11 @@ ZERO_API int zero_scaler_init(const zero_hparams* hp, zero_scaler* out);
  *   replicas:     host array of N device pointers; replicas[r] points at
  *                 flat element `window_base` of rank r's 16-bit gradient, and
  *                 must cover every element of the processed ranks' slices.
- *                 Padding elements (j >= psi) must hold zeros.
+ *                 Padding elements (j >= psi) must hold zeros. The step
+ *                 may read the rest of the 16-byte block that holds the
+ *                 window's last element (at most 14 bytes past it; the
+ *                 values are not used), so that block must be allocated:
+ *                 any buffer from cudaMalloc that holds the element is.
  *   window_base:  flat index that replicas[r] and flat_params point at
  *                 (0 for full buffers; i*S when only rank i's slice is held).
  *   flat_params:  device pointer at flat element window_base of the 16-bit

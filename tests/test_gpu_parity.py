@@ -372,3 +372,26 @@ def test_slices_off_the_8_element_grid(n, psi, two_pass, micro):
     p, _, _ = oracle.make_plan(wl.numels, n, 0)
     assert p.shard % 8 == 4
     run_small(wl, two_pass=two_pass)
+
+
+@pytest.mark.parametrize("n,psi,mod4,bf16,two_pass,micro", [
+    (8, 8 * 25_001 - 5, 1, True, False, 1),     # S odd
+    (8, 8 * 25_001 - 5, 1, False, True, 1),     # S odd, fp16, clipped in two passes
+    (8, 8 * 25_002, 2, True, False, 1),         # S = 2 (mod 4)
+    (8, 8 * 25_002, 2, True, True, 1),
+    (8, 8 * 25_003, 3, False, False, 1),        # S = 3 (mod 4)
+    (64, 64 * 3_001 - 7, 1, True, False, 1),
+    (64, 64 * 3_001 - 7, 1, True, True, 1),
+    (64, 64 * 3_002, 2, True, False, 2),        # micro-batches keep the element path
+])
+def test_slices_out_of_phase_with_the_window(n, psi, mod4, bf16, two_pass, micro):
+    """Shards whose size is not a multiple of 4: the owners' slices start at
+    every 16-bit phase of the 16-byte grid, so their tiles take the shifted
+    body (replica chunks copied from the 16-byte block below the first
+    element, unaligned parameter stores), against the checker element by
+    element."""
+    wl = W.Workload("phase", [psi], n, 0, bf16, 53 + mod4, 1e-3, steps=2, n_micro=micro,
+                    max_grad_norm=0.5 if two_pass else 0.0)
+    p, _, _ = oracle.make_plan(wl.numels, n, 0)
+    assert p.shard % 4 == mod4
+    run_small(wl, two_pass=two_pass)
