@@ -185,11 +185,31 @@ def _check(fn, rc):
         raise ZeroError(fn, rc)
 
 
-def _ptrs(seq):
-    """Python list of device addresses (int or None) -> C array of void*."""
+def _ptrs(seq, need=0, what="pointer array"):
+    """Python list of device addresses (int or None) -> C array of void*.
+    The library reads `need` entries of the array (it cannot see its
+    length), so a shorter list is refused here."""
     if seq is None:
         return None
+    if len(seq) < need:
+        raise ValueError(f"{what}: {len(seq)} entries, the call reads {need}")
     return (_VP * len(seq))(*[None if q is None else int(q) for q in seq])
+
+
+def _ranks(plan):
+    """N of a plan (the pointer arrays hold N or n_sets * N entries); 0 for
+    an invalid plan, which the call itself then reports."""
+    info = ZeroPlanInfo()
+    if not plan or lib().zero_plan_get_info(plan, C.byref(info)) != 0:
+        return 0
+    return info.n_ranks
+
+
+def _unit_ranks(plan):
+    info = ZeroUnitPlanInfo()
+    if not plan or lib().zero_unit_plan_get_info(plan, C.byref(info)) != 0:
+        return 0
+    return info.n_ranks
 
 
 def _vp(x):
@@ -249,85 +269,108 @@ def zero_scaler_init(hp):
 
 # ------------------------------------------------------------------ step ----
 
+def _rank_arrays(plan, n_sets=1, **lists):
+    """C arrays of the per-rank pointer lists of one call: replicas, accum,
+    micro and grad_shards hold N entries, optimizer arrays n_sets * N."""
+    n = _ranks(plan)
+    per_set = {"master", "exp_avg", "exp_avg_sq"}
+    return {k: _ptrs(v, (n_sets * n) if k in per_set else n, k) for k, v in lists.items()}
+
+
 def zero_reduce_scatter(plan, bucket, rank_lo, rank_hi, replicas, window_base, grad_shards,
                         d_scaler, d_bucket_flags=0, d_workspace=0, stream=0):
+    q = _rank_arrays(plan, replicas=replicas, grad_shards=grad_shards)
     _check("zero_reduce_scatter", lib().zero_reduce_scatter(
-        plan, bucket, rank_lo, rank_hi, _ptrs(replicas), window_base, _ptrs(grad_shards),
+        plan, bucket, rank_lo, rank_hi, q["replicas"], window_base, q["grad_shards"],
         _vp(d_scaler), _vp(d_bucket_flags), _vp(d_workspace), _vp(stream)))
 
 
 def zero_grad_norm(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, d_workspace, stream=0):
+    q = _rank_arrays(plan, grad_shards=grad_shards)
     _check("zero_grad_norm", lib().zero_grad_norm(
-        plan, rank_lo, rank_hi, _ptrs(grad_shards), C.byref(hp), _vp(d_scaler),
+        plan, rank_lo, rank_hi, q["grad_shards"], C.byref(hp), _vp(d_scaler),
         _vp(d_workspace), _vp(stream)))
 
 
 def zero_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
               replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags=0, stream=0):
+    q = _rank_arrays(plan, n_sets, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq,
+                     grad_shards=grad_shards, replicas=replicas)
     _check("zero_step", lib().zero_step(
-        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
-        _ptrs(grad_shards), _ptrs(replicas), window_base, _vp(flat_params), C.byref(hp),
+        plan, rank_lo, rank_hi, q["master"], q["exp_avg"], q["exp_avg_sq"], n_sets,
+        q["grad_shards"], q["replicas"], window_base, _vp(flat_params), C.byref(hp),
         _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
 
 
 def zero_step_update(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
                      replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags=0,
                      stream=0):
+    q = _rank_arrays(plan, n_sets, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq,
+                     grad_shards=grad_shards, replicas=replicas)
     _check("zero_step_update", lib().zero_step_update(
-        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
-        _ptrs(grad_shards), _ptrs(replicas), window_base, _vp(flat_params), C.byref(hp),
+        plan, rank_lo, rank_hi, q["master"], q["exp_avg"], q["exp_avg_sq"], n_sets,
+        q["grad_shards"], q["replicas"], window_base, _vp(flat_params), C.byref(hp),
         _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
 
 
 def zero_step_finish(plan, rank_lo, rank_hi, master, n_sets, grad_shards, window_base,
                      flat_params, hp, d_scaler, stream=0):
+    q = _rank_arrays(plan, n_sets, master=master, grad_shards=grad_shards)
     _check("zero_step_finish", lib().zero_step_finish(
-        plan, rank_lo, rank_hi, _ptrs(master), n_sets, _ptrs(grad_shards), window_base,
+        plan, rank_lo, rank_hi, q["master"], n_sets, q["grad_shards"], window_base,
         _vp(flat_params), C.byref(hp), _vp(d_scaler), _vp(stream)))
 
 
 def zero_cast_params(plan, rank_lo, rank_hi, master, flat_params, window_base, stream=0):
+    q = _rank_arrays(plan, 1, master=master)
     _check("zero_cast_params", lib().zero_cast_params(
-        plan, rank_lo, rank_hi, _ptrs(master), _vp(flat_params), window_base, _vp(stream)))
+        plan, rank_lo, rank_hi, q["master"], _vp(flat_params), window_base, _vp(stream)))
 
 
 def zero_accumulate(plan, rank_lo, rank_hi, micro, accum, window_base, first, stream=0):
+    q = _rank_arrays(plan, micro=micro, accum=accum)
     _check("zero_accumulate", lib().zero_accumulate(
-        plan, rank_lo, rank_hi, _ptrs(micro), _ptrs(accum), window_base, int(bool(first)),
+        plan, rank_lo, rank_hi, q["micro"], q["accum"], window_base, int(bool(first)),
         _vp(stream)))
 
 
 def zero_reduce_scatter_accum(plan, bucket, rank_lo, rank_hi, replicas, accum, n_micro,
                               window_base, grad_shards, d_scaler, d_bucket_flags=0,
                               d_workspace=0, stream=0):
+    q = _rank_arrays(plan, replicas=replicas, accum=accum, grad_shards=grad_shards)
     _check("zero_reduce_scatter_accum", lib().zero_reduce_scatter_accum(
-        plan, bucket, rank_lo, rank_hi, _ptrs(replicas), _ptrs(accum), n_micro, window_base,
-        _ptrs(grad_shards), _vp(d_scaler), _vp(d_bucket_flags), _vp(d_workspace), _vp(stream)))
+        plan, bucket, rank_lo, rank_hi, q["replicas"], q["accum"], n_micro, window_base,
+        q["grad_shards"], _vp(d_scaler), _vp(d_bucket_flags), _vp(d_workspace), _vp(stream)))
 
 
 def zero_step_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,
                     replicas, accum, n_micro, window_base, flat_params, hp, d_scaler,
                     d_bucket_flags=0, stream=0):
+    q = _rank_arrays(plan, n_sets, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq,
+                     grad_shards=grad_shards, replicas=replicas, accum=accum)
     _check("zero_step_accum", lib().zero_step_accum(
-        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
-        _ptrs(grad_shards), _ptrs(replicas), _ptrs(accum), n_micro, window_base,
-        _vp(flat_params), C.byref(hp), _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
+        plan, rank_lo, rank_hi, q["master"], q["exp_avg"], q["exp_avg_sq"], n_sets,
+        q["grad_shards"], q["replicas"], q["accum"], n_micro, window_base, _vp(flat_params),
+        C.byref(hp), _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
 
 
 def zero_step_update_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
                            grad_shards, replicas, accum, n_micro, window_base, flat_params, hp,
                            d_scaler, d_bucket_flags=0, stream=0):
+    q = _rank_arrays(plan, n_sets, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq,
+                     grad_shards=grad_shards, replicas=replicas, accum=accum)
     _check("zero_step_update_accum", lib().zero_step_update_accum(
-        plan, rank_lo, rank_hi, _ptrs(master), _ptrs(exp_avg), _ptrs(exp_avg_sq), n_sets,
-        _ptrs(grad_shards), _ptrs(replicas), _ptrs(accum), n_micro, window_base,
-        _vp(flat_params), C.byref(hp), _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
+        plan, rank_lo, rank_hi, q["master"], q["exp_avg"], q["exp_avg_sq"], n_sets,
+        q["grad_shards"], q["replicas"], q["accum"], n_micro, window_base, _vp(flat_params),
+        C.byref(hp), _vp(d_scaler), _vp(d_bucket_flags), _vp(stream)))
 
 
 def zero_grad_norm_noalloc(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, stream=0):
     """zero_grad_norm without a workspace: for callers that cannot allocate
     device memory (see include/zero.h)."""
+    q = _rank_arrays(plan, grad_shards=grad_shards)
     _check("zero_grad_norm_noalloc", lib().zero_grad_norm_noalloc(
-        plan, rank_lo, rank_hi, _ptrs(grad_shards), C.byref(hp), _vp(d_scaler), _vp(stream)))
+        plan, rank_lo, rank_hi, q["grad_shards"], C.byref(hp), _vp(d_scaler), _vp(stream)))
 
 
 def zero_selftest_wait_timeout(d_scaler, limit_ns, stream=0):
@@ -384,13 +427,17 @@ def zero_unit_plan_tensors(plan):
 
 
 def zero_gather_units(plan, unit_lo, unit_hi, shards, unit_buffers, stream=0):
+    N = _unit_ranks(plan)
     _check("zero_gather_units", lib().zero_gather_units(
-        plan, unit_lo, unit_hi, _ptrs(shards), _ptrs(unit_buffers), _vp(stream)))
+        plan, unit_lo, unit_hi, _ptrs(shards, N, "shards"), _ptrs(unit_buffers, unit_hi - unit_lo,
+        "unit_buffers"), _vp(stream)))
 
 
 def zero_shard_units(plan, unit_lo, unit_hi, unit_buffers, shards, stream=0):
+    N = _unit_ranks(plan)
     _check("zero_shard_units", lib().zero_shard_units(
-        plan, unit_lo, unit_hi, _ptrs(unit_buffers), _ptrs(shards), _vp(stream)))
+        plan, unit_lo, unit_hi, _ptrs(unit_buffers, unit_hi - unit_lo, "unit_buffers"),
+        _ptrs(shards, N, "shards"), _vp(stream)))
 
 
 def zero_unit_plan_strategy_cost(plan, strategy, n_replicas=1):

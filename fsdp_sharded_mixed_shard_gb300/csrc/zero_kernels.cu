@@ -1066,13 +1066,16 @@ __device__ __forceinline__ void acc_stage_shifted(const unsigned char* rp, int s
   }
 }
 
-// 16-bit parameter stores at a window index that is not a multiple of 4:
-// two 4-byte stores when it is even, four 2-byte stores otherwise.
+// 16-bit parameter stores of a shifted body: one 8-byte store when p is
+// 8-byte aligned, two 4-byte stores when it is 4-byte aligned, four 2-byte
+// stores otherwise.
 template <bool kBf16>
 __device__ __forceinline__ void stg_hv_unaligned(uint16_t* p, const float (&x)[4]) {
   const unsigned int h0 = narrow<kBf16>(x[0]), h1 = narrow<kBf16>(x[1]);
   const unsigned int h2 = narrow<kBf16>(x[2]), h3 = narrow<kBf16>(x[3]);
-  if ((reinterpret_cast<uintptr_t>(p) & 3) == 0) {
+  if ((reinterpret_cast<uintptr_t>(p) & 7) == 0) {
+    __stcs(reinterpret_cast<uint2*>(p), make_uint2(h0 | (h1 << 16), h2 | (h3 << 16)));
+  } else if ((reinterpret_cast<uintptr_t>(p) & 3) == 0) {
     unsigned int* q = reinterpret_cast<unsigned int*>(p);
     __stcs(q, h0 | (h1 << 16));
     __stcs(q + 1, h2 | (h3 << 16));
@@ -1086,13 +1089,15 @@ __device__ __forceinline__ void stg_hv_unaligned(uint16_t* p, const float (&x)[4
 }
 
 // Tile g of this launch: element range, owner, and the aligned body
-// [va, vb). When the owner's shard and the windows share a 4-element phase
+// [va, vb). When the owner's shard starts on the windows' 8-element grid
 // the body starts where the window index is a multiple of 8 (16-byte
 // replica chunks, 16-byte state chunks). Otherwise, if `shifted` is
 // allowed, the body starts where the shard index is a multiple of 4
 // (16-byte state chunks) and each replica chunk is copied from the 16-byte
-// block below its first element: `shift` elements earlier. Without either,
-// the body is empty and the tile goes element by element.
+// block below its first element: `shift` elements earlier. Whole tiles then
+// have no edge elements. Without `shifted`, an owner 4 elements off the
+// grid keeps the window-aligned body and a few edge elements per tile; any
+// other owner's tiles go element by element.
 // (A forward scan from the previous tile's segment measured slower than this
 // binary search.)
 __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shifted) {
@@ -1108,7 +1113,8 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shi
   const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
   t.va = t.hi;
   t.vb = t.hi;
-  if (((rank0 - a.wbase) & 3) == 0) {
+  const int64_t off_grid = (rank0 - a.wbase) & 7;
+  if (off_grid == 0 || (!shifted && (off_grid & 3) == 0)) {
     t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
     t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
   } else if (shifted) {
@@ -1125,8 +1131,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
   constexpr int kRepBytes = kAcc ? 6 : 2;  // per replica and element: 16-bit value (+ fp32 accumulator)
-  // shifted bodies (owner shard and windows out of phase): 4 elements per
-  // thread, no accumulators; each replica chunk then holds up to 7 extra
+  // shifted bodies (owner shard off the windows' 8-element grid): 4 elements
+  // per thread, no accumulators; each replica chunk then holds up to 7 extra
   // elements, so chunks are 16 bytes longer
   constexpr bool kShift = EPT == 4 && !kAcc && (MODE == kFused || MODE == kReduce);
   constexpr int kRepChunk = 2 * E + (kShift ? 16 : 0);         // bytes per replica chunk
@@ -1691,12 +1697,12 @@ int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
     if (a.has_acc) return launch_bulk_ept<MODE, kBf16, 4, true>(a, tiles, stream);
   }
   if (MODE == kReduce && 2 * a.n_ranks * kConsumers * 8 <= kStageBudget) {
-    // 8 elements per thread only when every owner's slice shares the
-    // window's 4-element phase: the 4-element kernel keeps a bulk body
-    // (shifted replica copies) for owners out of phase
+    // 8 elements per thread only when every owner's slice starts on the
+    // window's 8-element grid: the 4-element kernel gives the other owners
+    // a shifted bulk body without edge elements
     bool in_phase = true;
     for (int i = 0; i < a.n_segs; ++i)
-      in_phase = in_phase && ((static_cast<int64_t>(a.segs[i].rank) * a.shard - a.wbase) & 3) == 0;
+      in_phase = in_phase && ((static_cast<int64_t>(a.segs[i].rank) * a.shard - a.wbase) & 7) == 0;
     if (in_phase) return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
   }
   return launch_bulk_ept<MODE, kBf16, 4, false>(a, tiles, stream);

@@ -214,3 +214,31 @@ def test_unit_planner_and_gather_reject_bad_arguments():
         assert e.value.status == -2
     finally:
         Z.zero_unit_plan_destroy(p)
+
+
+def test_binding_refuses_short_pointer_lists():
+    """The C calls read N (or n_sets * N) entries of every per-rank pointer
+    array and cannot see a list's length, so the binding checks it before
+    the call. Nothing reaches a device: the check fails first."""
+    plan = Z.zero_plan_create([1000], 4, 0, Z.ZERO_BF16)
+    try:
+        four, eight = [16] * 4, [16] * 8
+        hp = Z.ZeroHParams(1e-3, 0.9, 0.999, 1e-8, 0.0, 0.0, 0, 2000, 1.0)
+        with pytest.raises(ValueError, match="master"):
+            Z.zero_step(plan, 0, 4, four, eight, eight, 2, None, four, 0, 16, hp, 16)
+        with pytest.raises(ValueError, match="replicas"):
+            Z.zero_step(plan, 0, 4, eight, eight, eight, 2, None, [16] * 3, 0, 16, hp, 16)
+        with pytest.raises(ValueError, match="grad_shards"):
+            Z.zero_reduce_scatter(plan, -1, 0, 4, four, 0, [16] * 2, 16)
+        with pytest.raises(ValueError, match="accum"):
+            Z.zero_accumulate(plan, 0, 4, four, [16], 0, True)
+    finally:
+        Z.zero_plan_destroy(plan)
+    uplan = Z.zero_unit_plan_create([10, 20], [0, 1], 2, 4, 1)
+    try:
+        with pytest.raises(ValueError, match="shards"):
+            Z.zero_gather_units(uplan, 0, 2, [16] * 3, [16, 16])
+        with pytest.raises(ValueError, match="unit_buffers"):
+            Z.zero_gather_units(uplan, 0, 2, four, [16])
+    finally:
+        Z.zero_unit_plan_destroy(uplan)

@@ -364,9 +364,11 @@ def test_cuda_graph_replay_equals_eager_steps(clip):
 @pytest.mark.parametrize("n,psi,two_pass,micro", [(8, 99_997, False, 1), (8, 99_997, True, 1),
                                                   (64, 64_250, False, 1), (64, 64_250, False, 2)])
 def test_slices_off_the_8_element_grid(n, psi, two_pass, micro):
-    """Shards of S = 4 (mod 8) elements: every tile of an odd owner has a few
-    edge elements outside its aligned body (the warp-cooperative path),
-    against the checker element by element."""
+    """Shards of S = 4 (mod 8) elements: odd owners start 4 elements off the
+    windows' 8-element grid. The fused step and the reduce pass give their
+    tiles a shifted body (copies from 4 elements early); with micro-batch
+    accumulators every tile has a few edge elements outside its aligned body
+    (the warp-cooperative path). Against the checker element by element."""
     wl = W.Workload("offgrid", [psi], n, 0, True, 51, 1e-3, steps=2, n_micro=micro,
                     max_grad_norm=0.5 if two_pass else 0.0)
     p, _, _ = oracle.make_plan(wl.numels, n, 0)
