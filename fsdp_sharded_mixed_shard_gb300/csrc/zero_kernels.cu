@@ -870,7 +870,7 @@ __device__ __forceinline__ void consumer_sync() {
 struct TileGeom {
   int64_t lo, hi, va, vb, partial;
   int32_t rank, bucket, first_rep;
-  int32_t shift;  // 16-bit elements between a replica copy's aligned start and va (shifted bodies)
+  int32_t shift;  // window elements from the 16-byte block below va to va (shard-indexed bodies)
 };
 
 // a0 += low half of w, a1 += high half of w, each 16-bit value widened
@@ -1031,38 +1031,88 @@ __device__ __forceinline__ void stg_hv(uint16_t* p, const float (&x)[EPT]) {
   }
 }
 
-// The four 16-bit values that start `shift` elements (0 < shift < 8) past p
-// in shared memory (p 8-byte aligned, 24 bytes readable): three aligned
-// 8-byte loads, a word select (two steps) and, for an odd shift, a funnel
-// shift.
-__device__ __forceinline__ uint2 halves_at(const unsigned char* p, int shift) {
-  const uint2 a = *reinterpret_cast<const uint2*>(p);
-  const uint2 b = *reinterpret_cast<const uint2*>(p + 8);
-  const uint2 c = *reinterpret_cast<const uint2*>(p + 16);
-  const uint32_t wd[6] = {a.x, a.y, b.x, b.y, c.x, c.y};
-  const int q = shift >> 1;  // whole 32-bit words to skip
-  uint32_t t[4], u[3];
+// Shifted replica values. A thread's EPT values start `shift` elements
+// (0 < shift < 8) past its position p in a replica chunk. For EPT = 4 (p
+// 8-byte aligned) they lie in the 16 bytes from the 8-byte block that holds
+// the first of them: two aligned 8-byte loads, then a word select and, for
+// an odd shift, a funnel shift. For EPT = 8 (p 16-byte aligned) they lie in
+// the 32 bytes from p: two 16-byte loads, a two-step word select and the
+// funnel shift. The chunk holds 16 bytes past its last thread's position.
+template <int EPT>
+struct ShiftedVec;
+template <>
+struct ShiftedVec<4> {
+  uint2 a, c;
+  __device__ __forceinline__ void load(const unsigned char* p, int shift) {
+    const unsigned char* b = p + ((shift >> 2) << 3);
+    a = *reinterpret_cast<const uint2*>(b);
+    c = *reinterpret_cast<const uint2*>(b + 8);
+  }
+  // the EPT / 2 words of values, low element in the low half
+  __device__ __forceinline__ void words(int shift, uint32_t (&x)[2]) const {
+    const int s = shift & 3;  // elements past the first loaded block
+    const uint32_t w0 = (s & 2) ? a.y : a.x;
+    const uint32_t w1 = (s & 2) ? c.x : a.y;
+    const uint32_t w2 = (s & 2) ? c.y : c.x;
+    x[0] = (s & 1) ? __funnelshift_r(w0, w1, 16) : w0;
+    x[1] = (s & 1) ? __funnelshift_r(w1, w2, 16) : w1;
+  }
+};
+template <>
+struct ShiftedVec<8> {
+  uint4 a, b;
+  __device__ __forceinline__ void load(const unsigned char* p, int) {
+    a = *reinterpret_cast<const uint4*>(p);
+    b = *reinterpret_cast<const uint4*>(p + 16);
+  }
+  __device__ __forceinline__ void words(int shift, uint32_t (&x)[4]) const {
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const int q = shift >> 1;
+    uint32_t t[6], u[5];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) t[j] = (q & 2) ? wd[j + 2] : wd[j];
+    for (int j = 0; j < 6; ++j) t[j] = (q & 2) ? wd[j + 2] : wd[j];
 #pragma unroll
-  for (int j = 0; j < 3; ++j) u[j] = (q & 1) ? t[j + 1] : t[j];  // u[j] = wd[q + j]
-  if (shift & 1)
-    return make_uint2(__funnelshift_r(u[0], u[1], 16), __funnelshift_r(u[1], u[2], 16));
-  return make_uint2(u[0], u[1]);
+    for (int j = 0; j < 5; ++j) u[j] = (q & 1) ? t[j + 1] : t[j];  // u[j] = wd[q + j]
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = (shift & 1) ? __funnelshift_r(u[j], u[j + 1], 16) : u[j];
+  }
+};
+
+// acc[e] += replica chunks 0..R-1 of a shifted body, loads first.
+template <bool kBf16, int R, int EPT>
+__device__ __forceinline__ void acc_reps_shifted(const unsigned char* rp, int stride, int shift,
+                                                 float (&acc)[EPT]) {
+  ShiftedVec<EPT> w[R];
+#pragma unroll
+  for (int p = 0; p < R; ++p) w[p].load(rp + static_cast<size_t>(p) * stride, shift);
+#pragma unroll
+  for (int p = 0; p < R; ++p) {
+    uint32_t x[EPT / 2];
+    w[p].words(shift, x);
+#pragma unroll
+    for (int i = 0; i < EPT / 2; ++i) add_halves<kBf16>(acc[2 * i], acc[2 * i + 1], x[i]);
+  }
 }
 
-// acc[e] += replica chunks 0..n-1 of this thread's 4 elements, in ring
-// order, for a shifted body: the thread's first element sits `shift`
-// elements past rp in each chunk. The same additions in the same order as
-// acc_stage.
-template <bool kBf16>
+// acc[e] += replica chunks 0..n-1 of this thread's EPT elements, in ring
+// order, for a shifted body (groups of at most 8 chunks, each loaded
+// before it is added). The same additions in the same order as acc_stage.
+template <bool kBf16, int EPT>
 __device__ __forceinline__ void acc_stage_shifted(const unsigned char* rp, int stride, int n,
-                                                  int shift, float (&acc)[4]) {
-#pragma unroll 4
-  for (int p = 0; p < n; ++p) {
-    const uint2 w = halves_at(rp + static_cast<size_t>(p) * stride, shift);
-    add_halves<kBf16>(acc[0], acc[1], w.x);
-    add_halves<kBf16>(acc[2], acc[3], w.y);
+                                                  int shift, float (&acc)[EPT]) {
+  int p = 0;
+  for (; p + 8 <= n; p += 8)
+    acc_reps_shifted<kBf16, 8, EPT>(rp + static_cast<size_t>(p) * stride, stride, shift, acc);
+  rp += static_cast<size_t>(p) * stride;
+  switch (n - p) {
+    case 1: acc_reps_shifted<kBf16, 1, EPT>(rp, stride, shift, acc); break;
+    case 2: acc_reps_shifted<kBf16, 2, EPT>(rp, stride, shift, acc); break;
+    case 3: acc_reps_shifted<kBf16, 3, EPT>(rp, stride, shift, acc); break;
+    case 4: acc_reps_shifted<kBf16, 4, EPT>(rp, stride, shift, acc); break;
+    case 5: acc_reps_shifted<kBf16, 5, EPT>(rp, stride, shift, acc); break;
+    case 6: acc_reps_shifted<kBf16, 6, EPT>(rp, stride, shift, acc); break;
+    case 7: acc_reps_shifted<kBf16, 7, EPT>(rp, stride, shift, acc); break;
+    default: break;
   }
 }
 
@@ -1091,16 +1141,16 @@ __device__ __forceinline__ void stg_hv_unaligned(uint16_t* p, const float (&x)[4
 // Tile g of this launch: element range, owner, and the aligned body
 // [va, vb). When the owner's shard starts on the windows' 8-element grid
 // the body starts where the window index is a multiple of 8 (16-byte
-// replica chunks, 16-byte state chunks). Otherwise, if `shifted` is
-// allowed, the body starts where the shard index is a multiple of 4
-// (16-byte state chunks) and each replica chunk is copied from the 16-byte
-// block below its first element: `shift` elements earlier. Whole tiles then
-// have no edge elements. Without `shifted`, an owner 4 elements off the
-// grid keeps the window-aligned body and a few edge elements per tile; any
-// other owner's tiles go element by element.
+// replica chunks, 16-byte state chunks). Otherwise, with `shard_body`, it
+// starts where the shard index is a multiple of 4 (16-byte state chunks),
+// `shift` elements past a 16-byte block of the windows: replica chunks are
+// copied from that block and parameter stores are unaligned. Whole tiles
+// then have no edge elements. Without `shard_body`, an owner 4 elements
+// off the grid keeps the window-aligned body and a few edge elements per
+// tile; any other owner's tiles go element by element.
 // (A forward scan from the previous tile's segment measured slower than this
 // binary search.)
-__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shifted) {
+__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shard_body) {
   const Seg& sg = a.segs[find_seg(a, g)];
   TileGeom t;
   t.lo = sg.lo + (g - sg.tile_local0) * kTile;
@@ -1114,10 +1164,10 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shi
   t.va = t.hi;
   t.vb = t.hi;
   const int64_t off_grid = (rank0 - a.wbase) & 7;
-  if (off_grid == 0 || (!shifted && (off_grid & 3) == 0)) {
+  if (off_grid == 0 || (!shard_body && (off_grid & 3) == 0)) {
     t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
     t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
-  } else if (shifted) {
+  } else if (shard_body) {
     t.va = min(t.lo + ((rank0 - t.lo) & 3), t.hi);
     t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
     t.shift = static_cast<int32_t>((t.va - a.wbase) & 7);
@@ -1131,10 +1181,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
   constexpr int kRepBytes = kAcc ? 6 : 2;  // per replica and element: 16-bit value (+ fp32 accumulator)
-  // shifted bodies (owner shard off the windows' 8-element grid): 4 elements
-  // per thread, no accumulators; each replica chunk then holds up to 7 extra
-  // elements, so chunks are 16 bytes longer
-  constexpr bool kShift = EPT == 4 && !kAcc && (MODE == kFused || MODE == kReduce);
+  // shifted bodies (owner shard off the windows' 8-element grid), without
+  // accumulators: each replica chunk then holds up to 7 extra elements, so
+  // chunks are 16 bytes longer
+  constexpr bool kShift = !kAcc && (MODE == kFused || MODE == kReduce);
+  // the update pass bulk-copies only shard-indexed arrays (g, master, m, v):
+  // its body follows the shard index for every owner, and only its 16-bit
+  // parameter stores see the window's phase
+  constexpr bool kShardBody = kShift || (MODE == kUpdate && EPT == 4);
   constexpr int kRepChunk = 2 * E + (kShift ? 16 : 0);         // bytes per replica chunk
   constexpr int kRepBlock = kAcc ? kRepBytes * E : kRepChunk;  // per replica in a stage
   __shared__ StepScalars sh_s;
@@ -1175,7 +1229,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     uint32_t phase = 0;  // == (it / n_slots) & 1
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
-      const TileGeom t = tile_geom(a, g, kShift);
+      const TileGeom t = tile_geom(a, g, kShardBody);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
       for (int64_t j0 = t.va; j0 < t.vb && !stop; j0 += E) {
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
@@ -1278,7 +1332,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   bool dead = false;
   const bool partials = MODE == kReduce && (a.mode_flags & kFlagPartials);
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
-    const TileGeom t = tile_geom(a, g, kShift);
+    const TileGeom t = tile_geom(a, g, kShardBody);
     NormAcc nacc;
     uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
@@ -1327,7 +1381,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                           E, r_hi - r_lo, acc);
             else if constexpr (kShift) {
               if (t.shift)
-                acc_stage_shifted<kBf16>(buf + t_off * 2, kRepChunk, r_hi - r_lo, t.shift, acc);
+                acc_stage_shifted<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, t.shift,
+                                              acc);
               else
                 acc_stage<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, acc);
             } else {
@@ -1391,7 +1446,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                 stg_fv<EPT>(a.master[s.dst][t.rank] + k, th);
                 stg_fv<EPT>(a.mom[s.dst][t.rank] + k, m);
                 stg_fv<EPT>(a.var[s.dst][t.rank] + k, v);
-                if constexpr (kShift) {
+                if constexpr (kShardBody) {
                   if (t.shift)
                     stg_hv_unaligned<kBf16>(a.flat + w, th);
                   else
@@ -1661,7 +1716,7 @@ template <int MODE, bool kBf16, int EPT, bool kAcc>
 int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
   constexpr int E = kConsumers * EPT;
   uint32_t slot_bytes = 0;
-  constexpr int kRepExtra = EPT == 4 && !kAcc && (MODE == kFused || MODE == kReduce) ? 16 : 0;
+  constexpr int kRepExtra = !kAcc && (MODE == kFused || MODE == kReduce) ? 16 : 0;
   a.plan = make_stage_plan(MODE, a.n_ranks, E, kAcc ? 6 : 2, kRepExtra, &slot_bytes);
   if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
   const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));
@@ -1696,14 +1751,9 @@ int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
   if constexpr (MODE == kFused || MODE == kReduce) {
     if (a.has_acc) return launch_bulk_ept<MODE, kBf16, 4, true>(a, tiles, stream);
   }
-  if (MODE == kReduce && 2 * a.n_ranks * kConsumers * 8 <= kStageBudget) {
-    // 8 elements per thread only when every owner's slice starts on the
-    // window's 8-element grid: the 4-element kernel gives the other owners
-    // a shifted bulk body without edge elements
-    bool in_phase = true;
-    for (int i = 0; i < a.n_segs; ++i)
-      in_phase = in_phase && ((static_cast<int64_t>(a.segs[i].rank) * a.shard - a.wbase) & 7) == 0;
-    if (in_phase) return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
+  if constexpr (MODE == kReduce) {
+    if (2 * a.n_ranks * kConsumers * 8 <= kStageBudget)
+      return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
   }
   return launch_bulk_ept<MODE, kBf16, 4, false>(a, tiles, stream);
 }

@@ -382,6 +382,7 @@ def test_slices_off_the_8_element_grid(n, psi, two_pass, micro):
     (8, 8 * 25_002, 2, True, False, 1),         # S = 2 (mod 4)
     (8, 8 * 25_002, 2, True, True, 1),
     (8, 8 * 25_003, 3, False, False, 1),        # S = 3 (mod 4)
+    (8, 8 * 25_003, 3, True, True, 1),
     (64, 64 * 3_001 - 7, 1, True, False, 1),
     (64, 64 * 3_001 - 7, 1, True, True, 1),
     (64, 64 * 3_002, 2, True, False, 2),        # micro-batches keep the element path
@@ -397,3 +398,22 @@ def test_slices_out_of_phase_with_the_window(n, psi, mod4, bf16, two_pass, micro
     p, _, _ = oracle.make_plan(wl.numels, n, 0)
     assert p.shard % 4 == mod4
     run_small(wl, two_pass=two_pass)
+
+
+@pytest.mark.parametrize("rank_lo,rank_hi,bucket,per_bucket", [
+    (3, 6, 0, False),          # a window that starts at an odd owner
+    (0, 8, 30_001, True),      # odd bucket size: segments start off every grid
+    (5, 6, 0, False),          # one odd owner alone (window base = 5 S)
+])
+def test_out_of_phase_windows_and_buckets(rank_lo, rank_hi, bucket, per_bucket):
+    """S odd with rank windows and odd bucket boundaries: the owners' phase
+    against the 16-byte grid is taken relative to the window base, and a
+    segment that starts at a bucket boundary starts its body at the next
+    shard index that is a multiple of 4. Fused and two-pass clipped steps,
+    against the checker element by element."""
+    for clip in (0.0, 0.5):
+        wl = W.Workload("window", [8 * 25_001 - 3], 8, bucket, True, 61, 1e-3, steps=2,
+                        rank_lo=rank_lo, rank_hi=rank_hi, max_grad_norm=clip)
+        p, _, _ = oracle.make_plan(wl.numels, 8, bucket)
+        assert p.shard % 2 == 1
+        run_small(wl, per_bucket=per_bucket and clip > 0, two_pass=clip > 0)
