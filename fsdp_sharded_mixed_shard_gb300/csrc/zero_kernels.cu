@@ -929,18 +929,19 @@ __device__ __forceinline__ void add_halves_to(float& d0, float& d1, uint32_t w, 
 
 // With fp32 accumulators of earlier micro-batches: replica value
 // A = acc + widen(micro) (one rounding), then the ring sum sum += A.
-// micro chunks are 2E bytes apart, accumulator chunks 4E bytes apart.
+// micro chunks are mstride bytes apart, accumulator chunks astride.
 template <bool kBf16, int EPT>
 __device__ __forceinline__ void acc_stage_accum(const unsigned char* mp, const unsigned char* ap,
-                                                int E, int n, float (&sum)[EPT]) {
+                                                int mstride, int astride, int n,
+                                                float (&sum)[EPT]) {
 #pragma unroll 2
   for (int p = 0; p < n; ++p) {
     HalfVec<EPT> w;
-    w.load(mp + static_cast<size_t>(p) * (2 * E));
+    w.load(mp + static_cast<size_t>(p) * mstride);
     float av[EPT];
 #pragma unroll
     for (int i = 0; i < EPT / 4; ++i) {
-      const float4 q = reinterpret_cast<const float4*>(ap + static_cast<size_t>(p) * (4 * E))[i];
+      const float4 q = reinterpret_cast<const float4*>(ap + static_cast<size_t>(p) * astride)[i];
       av[4 * i] = q.x;
       av[4 * i + 1] = q.y;
       av[4 * i + 2] = q.z;
@@ -1116,6 +1117,41 @@ __device__ __forceinline__ void acc_stage_shifted(const unsigned char* rp, int s
   }
 }
 
+// acc_stage_accum for a shifted body (4 elements per thread): the micro
+// values start `shift` elements past mp in each micro chunk, the
+// accumulator values (shift & 3) floats past ap (16-byte aligned; 32 bytes
+// readable) in each accumulator chunk. The same operations in the same
+// order as acc_stage_accum.
+template <bool kBf16>
+__device__ __forceinline__ void acc_stage_accum_shifted(const unsigned char* mp,
+                                                        const unsigned char* ap, int mstride,
+                                                        int astride, int n, int shift,
+                                                        float (&sum)[4]) {
+  const int sa = shift & 3;
+#pragma unroll 2
+  for (int p = 0; p < n; ++p) {
+    ShiftedVec<4> w;
+    w.load(mp + static_cast<size_t>(p) * mstride, shift);
+    uint32_t x[2];
+    w.words(shift, x);
+    const float4* q = reinterpret_cast<const float4*>(ap + static_cast<size_t>(p) * astride);
+    const float4 f0 = q[0], f1 = q[1];
+    const float fd[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    float t[6], av[4];
+#pragma unroll
+    for (int j = 0; j < 6; ++j) t[j] = (sa & 2) ? fd[j + 2] : fd[j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) av[j] = (sa & 1) ? t[j + 1] : t[j];  // av[j] = fd[sa + j]
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float v0, v1;
+      add_halves_to<kBf16>(v0, v1, x[i], av[2 * i], av[2 * i + 1]);
+      sum[2 * i] = __fadd_rn(sum[2 * i], v0);
+      sum[2 * i + 1] = __fadd_rn(sum[2 * i + 1], v1);
+    }
+  }
+}
+
 // 16-bit parameter stores of a shifted body: one 8-byte store when p is
 // 8-byte aligned, two 4-byte stores when it is 4-byte aligned, four 2-byte
 // stores otherwise.
@@ -1181,16 +1217,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
   constexpr int kRepBytes = kAcc ? 6 : 2;  // per replica and element: 16-bit value (+ fp32 accumulator)
-  // shifted bodies (owner shard off the windows' 8-element grid), without
-  // accumulators: each replica chunk then holds up to 7 extra elements, so
-  // chunks are 16 bytes longer
-  constexpr bool kShift = !kAcc && (MODE == kFused || MODE == kReduce);
+  // shifted bodies (owner shard off the windows' 8-element grid): each
+  // replica chunk then holds up to 7 extra elements and each accumulator
+  // chunk up to 3, so chunks are 16 bytes longer
+  constexpr bool kShift = MODE == kFused || MODE == kReduce;
   // the update pass bulk-copies only shard-indexed arrays (g, master, m, v):
   // its body follows the shard index for every owner, and only its 16-bit
   // parameter stores see the window's phase
   constexpr bool kShardBody = kShift || (MODE == kUpdate && EPT == 4);
-  constexpr int kRepChunk = 2 * E + (kShift ? 16 : 0);         // bytes per replica chunk
-  constexpr int kRepBlock = kAcc ? kRepBytes * E : kRepChunk;  // per replica in a stage
+  constexpr int kRepChunk = 2 * E + (kShift ? 16 : 0);  // bytes per replica chunk
+  constexpr int kAccChunk = 4 * E + (kShift ? 16 : 0);  // bytes per accumulator chunk
+  constexpr int kRepBlock = kAcc ? kRepChunk + kAccChunk : kRepChunk;  // per replica in a stage
   __shared__ StepScalars sh_s;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -1238,6 +1275,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         // replica copies start at the 16-byte block holding element w
         const int64_t rw = w - t.shift;
         const uint32_t rlen = t.shift ? ((len + t.shift + 7) & ~7u) : len;
+        // accumulator copies start at the 16-byte block holding element w
+        const int32_t ashift = t.shift & 3;
+        const int64_t aw = w - ashift;
+        const uint32_t alen = (len + ashift + 3) & ~3u;
         for (int st = 0; st < n_plan; ++st, ++it) {
           int go = 1;
           if (lane == 0) {
@@ -1251,7 +1292,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
               const uint32_t nr = static_cast<uint32_t>(a.plan.r_hi[st] - a.plan.r_lo[st]);
               const uint32_t ns = a.plan.states[st] ? (MODE == kUpdate ? 4u : 3u) : 0u;
               mbar_expect_tx(&full_bar[slot],
-                             nr * (2 * rlen + (kAcc ? 4 * len : 0)) + ns * 4 * len);
+                             nr * (2 * rlen + (kAcc ? 4 * alen : 0)) + ns * 4 * len);
             }
           }
           if (!__shfl_sync(0xFFFFFFFFu, go, 0)) {
@@ -1277,13 +1318,13 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             } else if (kAcc && c < n_rep_chunks) {
               int rr = t.first_rep + r_lo + (c - n_rep);
               if (rr >= N) rr -= N;
-              if (ZCHECK(w >= 0 && w + len <= a.wend, kSiteAccCopy, w) &&
-                  ZCHECK(n_rep * (2 * E) + (c - n_rep + 1) * (4 * E) <=
-                             static_cast<int>(slot_bytes),
+              if (ZCHECK(aw >= 0 && aw + alen <= ((a.wend + 3) & ~static_cast<int64_t>(3)),
+                         kSiteAccCopy, w) &&
+                  ZCHECK(n_rep * kRepChunk + (c - n_rep) * kAccChunk + 4 * alen <= slot_bytes,
                          kSiteStageBytes, c))
-                bulk_g2s(buf + static_cast<size_t>(n_rep) * (2 * E) +
-                             static_cast<size_t>(c - n_rep) * (4 * E),
-                         a.acc[rr] + w, len * 4, &full_bar[slot], pol);
+                bulk_g2s(buf + static_cast<size_t>(n_rep) * kRepChunk +
+                             static_cast<size_t>(c - n_rep) * kAccChunk,
+                         a.acc[rr] + aw, alen * 4, &full_bar[slot], pol);
             } else {
               const int q = c - n_rep_chunks;
               const float* src;
@@ -1374,12 +1415,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if constexpr (MODE == kFused || MODE == kReduce) {
           const bool completes = r_hi == N && r_lo < r_hi;  // stage ends the range's sum
           if (mine) {
-            if constexpr (kAcc)
-              acc_stage_accum<kBf16, EPT>(buf + t_off * 2,
-                                          buf + static_cast<size_t>(r_hi - r_lo) * (2 * E) +
-                                              t_off * 4,
-                                          E, r_hi - r_lo, acc);
-            else if constexpr (kShift) {
+            if constexpr (kAcc) {
+              const unsigned char* mp = buf + t_off * 2;
+              const unsigned char* ap =
+                  buf + static_cast<size_t>(r_hi - r_lo) * kRepChunk + t_off * 4;
+              if (t.shift)
+                acc_stage_accum_shifted<kBf16>(mp, ap, kRepChunk, kAccChunk, r_hi - r_lo,
+                                               t.shift, acc);
+              else
+                acc_stage_accum<kBf16, EPT>(mp, ap, kRepChunk, kAccChunk, r_hi - r_lo, acc);
+            } else if constexpr (kShift) {
               if (t.shift)
                 acc_stage_shifted<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, t.shift,
                                               acc);
@@ -1716,7 +1761,7 @@ template <int MODE, bool kBf16, int EPT, bool kAcc>
 int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
   constexpr int E = kConsumers * EPT;
   uint32_t slot_bytes = 0;
-  constexpr int kRepExtra = !kAcc && (MODE == kFused || MODE == kReduce) ? 16 : 0;
+  constexpr int kRepExtra = MODE == kFused || MODE == kReduce ? (kAcc ? 32 : 16) : 0;
   a.plan = make_stage_plan(MODE, a.n_ranks, E, kAcc ? 6 : 2, kRepExtra, &slot_bytes);
   if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
   const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));

@@ -331,6 +331,9 @@ ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t ra
  *   rounding, added in ring order; the unscale becomes fp32(1/(S_l*N*n_micro))
  *   (the average over every micro-batch of every rank). The accumulators are
  *   read, never written: the fused step reads 6N + 26 bytes per element.
+ *   As with the replicas, the step may read the rest of the 16-byte block
+ *   that holds an accumulator window's last element (at most 12 bytes past
+ *   it), so that block must be allocated.
  *   With n_micro == 1 they equal the calls without the suffix (accum may be
  *   NULL). zero_step_accum's accumulators only matter on the fused path. */
 ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,

@@ -40,6 +40,8 @@ def cases():
     yield "odd_shard_scalar_paths", dict(wl=W.TINY_FLAT.scaled(numels=[100_003], steps=2))
     yield "odd_shard_two_pass_n8", dict(wl=W.Workload("odd2", [8 * 25_001 - 3], 8, 0, True, 9,
                                                       1e-3, steps=2, max_grad_norm=0.5))
+    yield "odd_shard_micro_fused_n8", dict(wl=W.Workload("oddm", [8 * 25_001 - 5], 8, 0, True,
+                                                         13, 1e-3, steps=2, n_micro=3))
     yield "shard_4_mod_8_fused_n64", dict(wl=W.Workload("s4", [64 * 3_004], 64, 0, True, 11,
                                                         1e-3, steps=2))
 

@@ -385,14 +385,16 @@ def test_slices_off_the_8_element_grid(n, psi, two_pass, micro):
     (8, 8 * 25_003, 3, True, True, 1),
     (64, 64 * 3_001 - 7, 1, True, False, 1),
     (64, 64 * 3_001 - 7, 1, True, True, 1),
-    (64, 64 * 3_002, 2, True, False, 2),        # micro-batches keep the element path
+    (64, 64 * 3_002, 2, True, False, 2),        # micro-batches: shifted accumulator copies
+    (8, 8 * 25_001 - 5, 1, True, False, 3),
+    (8, 8 * 25_003, 3, False, True, 2),
 ])
 def test_slices_out_of_phase_with_the_window(n, psi, mod4, bf16, two_pass, micro):
     """Shards whose size is not a multiple of 4: the owners' slices start at
     every 16-bit phase of the 16-byte grid, so their tiles take the shifted
-    body (replica chunks copied from the 16-byte block below the first
-    element, unaligned parameter stores), against the checker element by
-    element."""
+    body (replica and accumulator chunks copied from the 16-byte block below
+    the first element, unaligned parameter stores), against the checker
+    element by element."""
     wl = W.Workload("phase", [psi], n, 0, bf16, 53 + mod4, 1e-3, steps=2, n_micro=micro,
                     max_grad_norm=0.5 if two_pass else 0.0)
     p, _, _ = oracle.make_plan(wl.numels, n, 0)
