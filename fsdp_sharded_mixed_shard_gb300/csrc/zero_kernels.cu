@@ -1096,23 +1096,25 @@ __device__ __forceinline__ void acc_reps_shifted(const unsigned char* rp, int st
 }
 
 // acc[e] += replica chunks 0..n-1 of this thread's EPT elements, in ring
-// order, for a shifted body (groups of at most 8 chunks, each loaded
-// before it is added). The same additions in the same order as acc_stage.
+// order, for a shifted body: groups of G chunks (32 loaded words), each
+// group loaded before it is added. The same additions in the same order as
+// acc_stage.
 template <bool kBf16, int EPT>
 __device__ __forceinline__ void acc_stage_shifted(const unsigned char* rp, int stride, int n,
                                                   int shift, float (&acc)[EPT]) {
+  constexpr int G = EPT == 4 ? 8 : 4;
   int p = 0;
-  for (; p + 8 <= n; p += 8)
-    acc_reps_shifted<kBf16, 8, EPT>(rp + static_cast<size_t>(p) * stride, stride, shift, acc);
+  for (; p + G <= n; p += G)
+    acc_reps_shifted<kBf16, G, EPT>(rp + static_cast<size_t>(p) * stride, stride, shift, acc);
   rp += static_cast<size_t>(p) * stride;
   switch (n - p) {
     case 1: acc_reps_shifted<kBf16, 1, EPT>(rp, stride, shift, acc); break;
     case 2: acc_reps_shifted<kBf16, 2, EPT>(rp, stride, shift, acc); break;
     case 3: acc_reps_shifted<kBf16, 3, EPT>(rp, stride, shift, acc); break;
-    case 4: acc_reps_shifted<kBf16, 4, EPT>(rp, stride, shift, acc); break;
-    case 5: acc_reps_shifted<kBf16, 5, EPT>(rp, stride, shift, acc); break;
-    case 6: acc_reps_shifted<kBf16, 6, EPT>(rp, stride, shift, acc); break;
-    case 7: acc_reps_shifted<kBf16, 7, EPT>(rp, stride, shift, acc); break;
+    case 4: if constexpr (G > 4) acc_reps_shifted<kBf16, 4, EPT>(rp, stride, shift, acc); break;
+    case 5: if constexpr (G > 5) acc_reps_shifted<kBf16, 5, EPT>(rp, stride, shift, acc); break;
+    case 6: if constexpr (G > 6) acc_reps_shifted<kBf16, 6, EPT>(rp, stride, shift, acc); break;
+    case 7: if constexpr (G > 7) acc_reps_shifted<kBf16, 7, EPT>(rp, stride, shift, acc); break;
     default: break;
   }
 }
@@ -1177,16 +1179,17 @@ __device__ __forceinline__ void stg_hv_unaligned(uint16_t* p, const float (&x)[4
 // Tile g of this launch: element range, owner, and the aligned body
 // [va, vb). When the owner's shard starts on the windows' 8-element grid
 // the body starts where the window index is a multiple of 8 (16-byte
-// replica chunks, 16-byte state chunks). Otherwise, with `shard_body`, it
-// starts where the shard index is a multiple of 4 (16-byte state chunks),
-// `shift` elements past a 16-byte block of the windows: replica chunks are
-// copied from that block and parameter stores are unaligned. Whole tiles
-// then have no edge elements. Without `shard_body`, an owner 4 elements
-// off the grid keeps the window-aligned body and a few edge elements per
-// tile; any other owner's tiles go element by element.
+// replica chunks, 16-byte state chunks). Otherwise it starts where the
+// shard index is a multiple of 4 (16-byte state chunks), `shift` elements
+// past a 16-byte block of the windows: replica and accumulator chunks are
+// copied from that block and parameter stores are unaligned. Either way a
+// whole tile has no elements outside its body; a tile that starts at a
+// bucket boundary or ends an owner's slice has a few. A kernel built
+// without off-grid support (`off` false; the host launches it only when
+// every owner is on the grid) would take such tiles element by element.
 // (A forward scan from the previous tile's segment measured slower than this
 // binary search.)
-__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool shard_body) {
+__device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool off) {
   const Seg& sg = a.segs[find_seg(a, g)];
   TileGeom t;
   t.lo = sg.lo + (g - sg.tile_local0) * kTile;
@@ -1195,39 +1198,35 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool sha
   t.bucket = sg.bucket;
   t.partial = sg.tile_global0 + (g - sg.tile_local0);
   t.first_rep = sg.rank + 1 == a.n_ranks ? 0 : sg.rank + 1;
-  t.shift = 0;
   const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
-  t.va = t.hi;
-  t.vb = t.hi;
-  const int64_t off_grid = (rank0 - a.wbase) & 7;
-  if (off_grid == 0 || (!shard_body && (off_grid & 3) == 0)) {
+  t.shift = 0;
+  if (((rank0 - a.wbase) & 7) == 0) {
     t.va = min(t.lo + ((a.wbase - t.lo) & 7), t.hi);
-    t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
-  } else if (shard_body) {
+  } else if (off) {
     t.va = min(t.lo + ((rank0 - t.lo) & 3), t.hi);
-    t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
     t.shift = static_cast<int32_t>((t.va - a.wbase) & 7);
+  } else {
+    t.va = t.hi;
   }
+  t.vb = t.va + ((t.hi - t.va) & ~static_cast<int64_t>(7));
   return t;
 }
 
-template <int MODE, bool kBf16, int EPT, bool kAcc>
+template <int MODE, bool kBf16, int EPT, bool kAcc, bool kOff>
 __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
                                                                int n_slots,
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
-  constexpr int kRepBytes = kAcc ? 6 : 2;  // per replica and element: 16-bit value (+ fp32 accumulator)
+  // 8 elements per thread only in the reduce pass (its 16-bit stores are
+  // the parameter stores of the other modes, done 4 at a time)
+  static_assert(MODE == kReduce || EPT == 4, "8 elements per thread: reduce pass only");
   // shifted bodies (owner shard off the windows' 8-element grid): each
-  // replica chunk then holds up to 7 extra elements and each accumulator
-  // chunk up to 3, so chunks are 16 bytes longer
-  constexpr bool kShift = MODE == kFused || MODE == kReduce;
-  // the update pass bulk-copies only shard-indexed arrays (g, master, m, v):
-  // its body follows the shard index for every owner, and only its 16-bit
-  // parameter stores see the window's phase
-  constexpr bool kShardBody = kShift || (MODE == kUpdate && EPT == 4);
-  constexpr int kRepChunk = 2 * E + (kShift ? 16 : 0);  // bytes per replica chunk
-  constexpr int kAccChunk = 4 * E + (kShift ? 16 : 0);  // bytes per accumulator chunk
-  constexpr int kRepBlock = kAcc ? kRepChunk + kAccChunk : kRepChunk;  // per replica in a stage
+  // replica chunk holds up to 7 extra elements and each accumulator chunk up
+  // to 3, so chunks are 16 bytes longer. The update pass bulk-copies only
+  // shard-indexed arrays (g, master, m, v); only its parameter stores see
+  // the window's phase.
+  constexpr bool kShift = kOff && (MODE == kFused || MODE == kReduce);
+  constexpr int kPad = kShift ? 16 : 0;  // extra bytes per chunk of a shifted tile
   __shared__ StepScalars sh_s;
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
@@ -1266,7 +1265,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
     uint32_t phase = 0;  // == (it / n_slots) & 1
     bool stop = false;
     for (int64_t g = blockIdx.x; g < a.n_tiles && !stop; g += gridDim.x) {
-      const TileGeom t = tile_geom(a, g, kShardBody);
+      const TileGeom t = tile_geom(a, g, kOff);
       const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
       for (int64_t j0 = t.va; j0 < t.vb && !stop; j0 += E) {
         const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(E), t.vb - j0));
@@ -1279,6 +1278,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         const int32_t ashift = t.shift & 3;
         const int64_t aw = w - ashift;
         const uint32_t alen = (len + ashift + 3) & ~3u;
+        // stage layout of this tile: replica chunks, accumulator chunks, states
+        const int rstride = 2 * E + (t.shift ? kPad : 0);
+        const int astride = 4 * E + (t.shift ? kPad : 0);
+        const int rblock = kAcc ? rstride + astride : rstride;
         for (int st = 0; st < n_plan; ++st, ++it) {
           int go = 1;
           if (lane == 0) {
@@ -1312,18 +1315,18 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
               // holds the window's last element
               if (ZCHECK(rw >= 0 && rw + rlen <= ((a.wend + 7) & ~static_cast<int64_t>(7)),
                          kSiteRepCopy, w) &&
-                  ZCHECK(c * kRepChunk + 2 * rlen <= slot_bytes, kSiteStageBytes, c))
-                bulk_g2s(buf + static_cast<size_t>(c) * kRepChunk, a.rep[rr] + rw, rlen * 2,
+                  ZCHECK(c * rstride + 2 * rlen <= slot_bytes, kSiteStageBytes, c))
+                bulk_g2s(buf + static_cast<size_t>(c) * rstride, a.rep[rr] + rw, rlen * 2,
                          &full_bar[slot], pol);
             } else if (kAcc && c < n_rep_chunks) {
               int rr = t.first_rep + r_lo + (c - n_rep);
               if (rr >= N) rr -= N;
               if (ZCHECK(aw >= 0 && aw + alen <= ((a.wend + 3) & ~static_cast<int64_t>(3)),
                          kSiteAccCopy, w) &&
-                  ZCHECK(n_rep * kRepChunk + (c - n_rep) * kAccChunk + 4 * alen <= slot_bytes,
+                  ZCHECK(n_rep * rstride + (c - n_rep) * astride + 4 * alen <= slot_bytes,
                          kSiteStageBytes, c))
-                bulk_g2s(buf + static_cast<size_t>(n_rep) * kRepChunk +
-                             static_cast<size_t>(c - n_rep) * kAccChunk,
+                bulk_g2s(buf + static_cast<size_t>(n_rep) * rstride +
+                             static_cast<size_t>(c - n_rep) * astride,
                          a.acc[rr] + aw, alen * 4, &full_bar[slot], pol);
             } else {
               const int q = c - n_rep_chunks;
@@ -1337,9 +1340,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                              : (q == 1 ? a.mom[s.src][t.rank] : a.var[s.src][t.rank]);
               }
               if (ZCHECK(kk >= 0 && kk + len <= a.shard, kSiteStateCopy, kk) &&
-                  ZCHECK(n_rep * kRepBlock + (q + 1) * (4 * E) <= static_cast<int>(slot_bytes),
+                  ZCHECK(n_rep * rblock + (q + 1) * (4 * E) <= static_cast<int>(slot_bytes),
                          kSiteStageBytes, c))
-                bulk_g2s(buf + static_cast<size_t>(n_rep) * kRepBlock +
+                bulk_g2s(buf + static_cast<size_t>(n_rep) * rblock +
                              static_cast<size_t>(q) * (4 * E),
                          src + kk, len * 4, &full_bar[slot], pol);
             }
@@ -1373,11 +1376,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   bool dead = false;
   const bool partials = MODE == kReduce && (a.mode_flags & kFlagPartials);
   for (int64_t g = blockIdx.x; g < a.n_tiles; g += gridDim.x, ++tile_no) {
-    const TileGeom t = tile_geom(a, g, kShardBody);
+    const TileGeom t = tile_geom(a, g, kOff);
     NormAcc nacc;
     uint64_t phi = 0, plo = 0;  // packed in-range accumulators (even | odd elements)
     bool bad = false;
     const int64_t rank0 = static_cast<int64_t>(t.rank) * a.shard;
+    const int rstride = 2 * E + (t.shift ? kPad : 0);  // stage layout, as the producer's
+    const int astride = 4 * E + (t.shift ? kPad : 0);
+    const int rblock = kAcc ? rstride + astride : rstride;
     for (int64_t j0 = t.va; j0 < t.vb; j0 += E) {
       const int len = static_cast<int>(min(static_cast<int64_t>(E), t.vb - j0));
       const bool mine = t_off < len;
@@ -1418,20 +1424,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             if constexpr (kAcc) {
               const unsigned char* mp = buf + t_off * 2;
               const unsigned char* ap =
-                  buf + static_cast<size_t>(r_hi - r_lo) * kRepChunk + t_off * 4;
-              if (t.shift)
-                acc_stage_accum_shifted<kBf16>(mp, ap, kRepChunk, kAccChunk, r_hi - r_lo,
+                  buf + static_cast<size_t>(r_hi - r_lo) * rstride + t_off * 4;
+              if (kShift && t.shift)
+                acc_stage_accum_shifted<kBf16>(mp, ap, rstride, astride, r_hi - r_lo,
                                                t.shift, acc);
               else
-                acc_stage_accum<kBf16, EPT>(mp, ap, kRepChunk, kAccChunk, r_hi - r_lo, acc);
-            } else if constexpr (kShift) {
-              if (t.shift)
-                acc_stage_shifted<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, t.shift,
-                                              acc);
-              else
-                acc_stage<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, acc);
+                acc_stage_accum<kBf16, EPT>(mp, ap, rstride, astride, r_hi - r_lo, acc);
+            } else if (kShift && t.shift) {
+              acc_stage_shifted<kBf16, EPT>(buf + t_off * 2, rstride, r_hi - r_lo, t.shift,
+                                            acc);
             } else {
-              acc_stage<kBf16, EPT>(buf + t_off * 2, kRepChunk, r_hi - r_lo, acc);
+              acc_stage<kBf16, EPT>(buf + t_off * 2, rstride, r_hi - r_lo, acc);
             }
             if (completes) {
               const uint64_t inv2 = f2_pack(s.inv, s.inv);
@@ -1471,7 +1474,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if (mine) {
           if constexpr (MODE == kFused || MODE == kUpdate) {
             if (a.plan.states[st]) {
-              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * kRepBlock;
+              const unsigned char* sb = buf + static_cast<size_t>(r_hi - r_lo) * rblock;
               if constexpr (MODE == kUpdate) {
                 lds_fv<EPT>(sb + t_off * 4, gv);
                 sb += 4 * E;
@@ -1491,14 +1494,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                 stg_fv<EPT>(a.master[s.dst][t.rank] + k, th);
                 stg_fv<EPT>(a.mom[s.dst][t.rank] + k, m);
                 stg_fv<EPT>(a.var[s.dst][t.rank] + k, v);
-                if constexpr (kShardBody) {
-                  if (t.shift)
-                    stg_hv_unaligned<kBf16>(a.flat + w, th);
-                  else
-                    stg_hv<kBf16, EPT>(a.flat + w, th);
-                } else {
+                if (kOff && t.shift)
+                  stg_hv_unaligned<kBf16>(a.flat + w, th);
+                else
                   stg_hv<kBf16, EPT>(a.flat + w, th);
-                }
               }
             }
           }
@@ -1757,17 +1756,17 @@ inline StagePlan make_stage_plan(int mode, int n_ranks, int E, int rep_bytes, in
   return pl;
 }
 
-template <int MODE, bool kBf16, int EPT, bool kAcc>
+template <int MODE, bool kBf16, int EPT, bool kAcc, bool kOff>
 int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
   constexpr int E = kConsumers * EPT;
   uint32_t slot_bytes = 0;
-  constexpr int kRepExtra = MODE == kFused || MODE == kReduce ? (kAcc ? 32 : 16) : 0;
+  constexpr int kRepExtra = kOff && (MODE == kFused || MODE == kReduce) ? (kAcc ? 32 : 16) : 0;
   a.plan = make_stage_plan(MODE, a.n_ranks, E, kAcc ? 6 : 2, kRepExtra, &slot_bytes);
   if (a.plan.n < 1 || a.plan.n > kMaxStagePlan || slot_bytes == 0) return ZERO_ERANGE;
   const int slots = std::min(kMaxStages, kSmemCap / static_cast<int>(slot_bytes));
   if (slots < 2) return ZERO_ERANGE;
   const size_t smem = static_cast<size_t>(slots) * slot_bytes;
-  auto kern = bulk_kernel<MODE, kBf16, EPT, kAcc>;
+  auto kern = bulk_kernel<MODE, kBf16, EPT, kAcc, kOff>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return ZERO_ECUDA;
@@ -1791,16 +1790,37 @@ int launch_bulk_ept(Args& a, int64_t tiles, cudaStream_t stream) {
 // consumer thread, one tile) whenever a range's replicas fit one stage
 // (N <= 8); the update and fused passes measured faster with 2048-element
 // ranges and more, smaller slots.
-template <int MODE, bool kBf16>
-int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+template <int MODE, bool kBf16, bool kOff>
+int launch_bulk_off(Args& a, int64_t tiles, cudaStream_t stream) {
   if constexpr (MODE == kFused || MODE == kReduce) {
-    if (a.has_acc) return launch_bulk_ept<MODE, kBf16, 4, true>(a, tiles, stream);
+    if (a.has_acc) return launch_bulk_ept<MODE, kBf16, 4, true, kOff>(a, tiles, stream);
   }
   if constexpr (MODE == kReduce) {
     if (2 * a.n_ranks * kConsumers * 8 <= kStageBudget)
-      return launch_bulk_ept<MODE, kBf16, 8, false>(a, tiles, stream);
+      return launch_bulk_ept<MODE, kBf16, 8, false, kOff>(a, tiles, stream);
   }
-  return launch_bulk_ept<MODE, kBf16, 4, false>(a, tiles, stream);
+  return launch_bulk_ept<MODE, kBf16, 4, false, kOff>(a, tiles, stream);
+}
+
+// The reduce and update passes are built twice: with support for owners
+// off the windows' 8-element grid (shifted bodies) and without it. The
+// leaner build runs whenever every owner of the launch is on the grid:
+// carrying the shifted paths measured 2-3 % slower in aligned reduce and
+// update passes on one box (no different on another). The fused pass
+// measured the other way round: 167.2 against 162.6 Gparams/s on the GPT-2
+// list at N = 8 with the shifted paths built in (same box, same data), so
+// it always runs that build.
+template <int MODE, bool kBf16>
+int launch_bulk(Args& a, int64_t tiles, cudaStream_t stream) {
+  if constexpr (MODE == kFused) {
+    return launch_bulk_off<MODE, kBf16, true>(a, tiles, stream);
+  } else {
+    bool off = false;
+    for (int i = 0; i < a.n_segs; ++i)
+      off = off || ((static_cast<int64_t>(a.segs[i].rank) * a.shard - a.wbase) & 7) != 0;
+    return off ? launch_bulk_off<MODE, kBf16, true>(a, tiles, stream)
+               : launch_bulk_off<MODE, kBf16, false>(a, tiles, stream);
+  }
 }
 
 template <int MODE, bool kBf16>
