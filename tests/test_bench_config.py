@@ -1,0 +1,22 @@
+"""bench.py's timing hygiene on CPU: which workloads are timed with an L2
+flush before every step (a step that moves less than twice the 129 MB L2)
+and what the JSON line's config says about it."""
+import bench
+from fsdp_sharded_mixed_shard_gb300 import workloads as W
+
+
+def test_small_workloads_are_timed_cold():
+    assert bench.needs_flush(W.TINY_FLAT, "fused")          # 34 MB per step
+    cfg = bench.config_of(W.TINY_FLAT, "fused")
+    assert cfg["l2"].startswith("L2 flushed before every timed step")
+    assert "256 MB" in cfg["l2"]
+    assert bench.FLUSH_BYTES > bench.L2_BYTES
+
+
+def test_large_workloads_exceed_l2():
+    for wl, path in ((W.GPT2_SMALL, "fused"), (W.STAGE3_SLICE, "fused"),
+                     (W.LLAMA_2B, "two_pass"), (W.FLAT_1P5B, "two_pass")):
+        assert not bench.needs_flush(wl, path), wl.name
+        assert bench.config_of(wl, path)["l2"].startswith("inputs larger than L2")
+    # GPT-2 list at N = 8: (2N + 26) bytes per parameter
+    assert bench.step_bytes(W.GPT2_SMALL, "fused") == 42 * 124_439_808
