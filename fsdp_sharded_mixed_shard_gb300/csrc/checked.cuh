@@ -26,6 +26,7 @@ enum CheckSite : int {
   kSiteRecord = 9,
   kSiteAccumulate = 10,
   kSiteGather = 11,
+  kSiteLoad = 12,
 };
 
 #ifdef ZERO_CHECKED

@@ -241,6 +241,8 @@ __device__ __forceinline__ void ff_merge(float& hi, float& lo, float h2, float l
 
 constexpr float kNormMainLimit = 0x1p56f;
 constexpr float kNormBigScale = 0x1p-96f;
+// a running sum of squares below this holds no square of a |g| >= 2^56
+constexpr float kNormSumLimit = 0x1p112f;
 
 // Packed form of ff_add_sq for two independent accumulators at once, with
 // sm_100+'s paired fp32 instructions (PTX add/sub/mul/fma .rn.f32x2: each
@@ -1453,22 +1455,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
             }
           }
           if (partials && completes) {
-            // squares of this thread's elements: one warp-wide range check,
-            // then the straight-line paired-fp32 path (non-finite values
-            // show up in the accumulators, checked once per tile)
+            // squares of this thread's elements on the straight-line
+            // paired-fp32 path, whatever their size: a square of 2^112 or
+            // more (|g| >= 2^56) or a non-finite one shows in the
+            // accumulators at the end of the tile, which then redoes this
+            // thread's body with the per-element split
             float q[EPT];
 #pragma unroll
             for (int e = 0; e < EPT; ++e) q[e] = mine ? gv[e] : 0.0f;
-            bool in_range = true;
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) in_range &= fabsf(q[e]) < kNormMainLimit;
-            if (__all_sync(0xFFFFFFFFu, in_range)) {
-#pragma unroll
-              for (int i = 0; i < EPT / 2; ++i) ff2_add_sq(phi, plo, f2_pack(q[2 * i], q[2 * i + 1]));
-            } else {
-#pragma unroll
-              for (int e = 0; e < EPT; ++e) nacc.add(q[e]);
-            }
+            for (int i = 0; i < EPT / 2; ++i) ff2_add_sq(phi, plo, f2_pack(q[2 * i], q[2 * i + 1]));
           }
         }
         if (mine) {
@@ -1532,8 +1528,23 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         float h0, h1, l0, l1;
         f2_unpack(phi, h0, h1);
         f2_unpack(plo, l0, l1);
-        nacc.merge(h0, l0, 0.f, 0.f);
-        nacc.merge(h1, l1, 0.f, 0.f);
+        if (h0 < kNormSumLimit && h1 < kNormSumLimit) {  // false for NaN as well
+          nacc.merge(h0, l0, 0.f, 0.f);
+          nacc.merge(h1, l1, 0.f, 0.f);
+        } else if constexpr (MODE == kReduce) {
+          // rare: redo this thread's body elements with the split into
+          // in-range and scaled big squares, from the reduced gradient this
+          // thread stored above (its own stores, so its loads see them)
+          for (int64_t j0 = t.va; j0 < t.vb && !dead; j0 += E) {
+            const int len = static_cast<int>(min(static_cast<int64_t>(E), t.vb - j0));
+            const int64_t k = j0 + t_off - rank0;
+            if (t_off < len && ZCHECK(k >= 0 && k + EPT <= a.shard, kSiteLoad, k)) {
+              const float* gp = a.ghat[t.rank] + k;
+#pragma unroll
+              for (int e = 0; e < EPT; ++e) nacc.add(gp[e]);
+            }
+          }
+        }
         bad |= nacc.nonfinite_seen();
       }
       if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a, t.bucket);

@@ -385,7 +385,8 @@ ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns,
  * first violation (site << 48 | low 48 bits of the offending index; sites:
  * 1 self-test, 2 scalar element, 3 vector element, 4 replica copy,
  * 5 accumulator copy, 6 state copy, 7 stage slot, 8 store, 9 norm record,
- * 10 micro-batch accumulation, 11 unit gather / shard, zero_units.h)
+ * 10 micro-batch accumulation, 11 unit gather / shard, zero_units.h,
+ * 12 reload of a reduced gradient for the norm's big-square path)
  * and clears both. zero_selftest_check plants one violation (site 1,
  * index 42). In the release build both return ZERO_ESTATE (and
  * zero_checked_status zeroes its outputs). */
