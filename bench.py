@@ -64,7 +64,25 @@ def parse_args():
                     help="unit padding grain in elements for --gather (1: multiple of N)")
     ap.add_argument("--numel-cap", type=int, default=0,
                     help="run the workload's first N flat parameters only (small profiling case)")
+    ap.add_argument("--flat", type=int, default=0,
+                    help="instead of --workload: one flat bf16 tensor of this many parameters "
+                         "(shape studies, e.g. shards that start off the 16-byte grid)")
+    ap.add_argument("--ranks", type=int, default=8, help="simulated ranks N for --flat")
+    ap.add_argument("--clip", type=float, default=0.0,
+                    help="max grad norm for --flat (> 0: the two-pass clipped step)")
     return ap.parse_args()
+
+
+def selected_workload(args):
+    """The workload a run times: --flat PSI --ranks N [--clip C] (seeded
+    N(0, 1e-3) bf16 gradients, the GPT-2 workload's hyperparameters), else
+    the named --workload."""
+    if args.flat:
+        from fsdp_sharded_mixed_shard_gb300 import workloads as W
+        name = "flat_%d_n%d_bf16%s" % (args.flat, args.ranks, "_clip" if args.clip > 0 else "")
+        return W.Workload(name, [args.flat], args.ranks, 0, True, 3, 1e-3,
+                          max_grad_norm=args.clip)
+    return workload(args.workload)
 
 
 def workload(name):
@@ -244,7 +262,7 @@ def run_libzero(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = workload(args.workload)
+    wl = selected_workload(args)
     if args.numel_cap:
         wl = truncated(wl, args.numel_cap)
     if args.micro > 1:
@@ -732,7 +750,7 @@ def cpu_baseline(wl, seconds):
 def run_reference(args):
     """The CPU checker on the host cores: each of the warmup + steps steps is a
     bounded sample of the workload, sized so the run takes about two minutes."""
-    wl = workload(args.workload)
+    wl = selected_workload(args)
     total = args.steps + args.warmup
     n, _ = calibrate_oracle(wl, 100.0, total)
     s = oracle_sample(wl, n)
@@ -778,7 +796,7 @@ def main():
     line = run_libzero(args, rank, world, dist)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(workload(args.workload), args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(selected_workload(args), args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -20,3 +20,17 @@ def test_large_workloads_exceed_l2():
         assert bench.config_of(wl, path)["l2"].startswith("inputs larger than L2")
     # GPT-2 list at N = 8: (2N + 26) bytes per parameter
     assert bench.step_bytes(W.GPT2_SMALL, "fused") == 42 * 124_439_808
+
+
+def test_flat_shape_option():
+    import sys
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py", "--flat", "40000064", "--ranks", "64", "--clip", "1.0"]
+        a = bench.parse_args()
+    finally:
+        sys.argv = old
+    wl = bench.selected_workload(a)
+    assert wl.numels == [40_000_064] and wl.n_ranks == 64 and wl.max_grad_norm == 1.0
+    assert wl.name == "flat_40000064_n64_bf16_clip"
+    assert bench.config_of(wl, "two_pass")["shard_elems"] == 625_001

@@ -402,12 +402,14 @@ def test_slices_out_of_phase_with_the_window(n, psi, mod4, bf16, two_pass, micro
     run_small(wl, two_pass=two_pass)
 
 
-@pytest.mark.parametrize("rank_lo,rank_hi,bucket,per_bucket", [
-    (3, 6, 0, False),          # a window that starts at an odd owner
-    (0, 8, 30_001, True),      # odd bucket size: segments start off every grid
-    (5, 6, 0, False),          # one odd owner alone (window base = 5 S)
+@pytest.mark.parametrize("rank_lo,rank_hi,bucket,per_bucket,micro", [
+    (3, 6, 0, False, 1),          # a window that starts at an odd owner
+    (0, 8, 30_001, True, 1),      # odd bucket size: segments start off every grid
+    (5, 6, 0, False, 1),          # one odd owner alone (window base = 5 S)
+    (0, 8, 30_001, True, 2),      # the same with micro-batch accumulators
+    (2, 7, 0, False, 3),
 ])
-def test_out_of_phase_windows_and_buckets(rank_lo, rank_hi, bucket, per_bucket):
+def test_out_of_phase_windows_and_buckets(rank_lo, rank_hi, bucket, per_bucket, micro):
     """S odd with rank windows and odd bucket boundaries: the owners' phase
     against the 16-byte grid is taken relative to the window base, and a
     segment that starts at a bucket boundary starts its body at the next
@@ -415,7 +417,7 @@ def test_out_of_phase_windows_and_buckets(rank_lo, rank_hi, bucket, per_bucket):
     against the checker element by element."""
     for clip in (0.0, 0.5):
         wl = W.Workload("window", [8 * 25_001 - 3], 8, bucket, True, 61, 1e-3, steps=2,
-                        rank_lo=rank_lo, rank_hi=rank_hi, max_grad_norm=clip)
+                        rank_lo=rank_lo, rank_hi=rank_hi, max_grad_norm=clip, n_micro=micro)
         p, _, _ = oracle.make_plan(wl.numels, 8, bucket)
         assert p.shard % 2 == 1
         run_small(wl, per_bucket=per_bucket and clip > 0, two_pass=clip > 0)
