@@ -143,8 +143,17 @@ def peaks():
 
 
 def kernel_source_sha(source="zero_kernels.cu"):
+    """Hash of a kernel source's code, with comments and whitespace removed:
+    a comment edit keeps the committed traffic figures valid, any code edit
+    voids them."""
     p = os.path.join(ROOT, "fsdp_sharded_mixed_shard_gb300", "csrc", source)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    return code_sha(open(p, encoding="utf-8").read())
+
+
+def code_sha(txt):
+    txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+    txt = re.sub(r"//[^\n]*", " ", txt)
+    return hashlib.sha256(" ".join(txt.split()).encode()).hexdigest()[:16]
 
 
 def profiled_traffic(kernel, wl_name, source="zero_kernels.cu"):

@@ -777,8 +777,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
 // global memory with streaming stores and release the slot on its "empty"
 // mbarrier. With S slots, S - 1 stages (~100-170 KB per SM) are in flight
 // while one is computed, independent of the register budget.
-// Tile heads/tails that are not 16-byte aligned are done by the consumers
-// with plain loads (do_scalar).
+// An owner whose slice starts off the windows' 8-element grid gets a
+// shard-indexed body: its chunks are copied from the 16-byte block below
+// their first element (16 bytes longer) and the values picked out in shared
+// memory (tile_geom). The few elements of a tile outside its body (at a
+// bucket boundary or an owner's last tile) are done by the consumers with
+// plain loads, one warp per element (do_scalar_warp) or one thread each.
 // Every mbarrier wait is bounded by kWaitLimitNs of %globaltimer; on expiry
 // the thread records ZERO_DEVERR_TIMEOUT, the CTA stops issuing, the
 // producer waits (again bounded) for the copies it issued, and all return.

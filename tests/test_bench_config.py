@@ -34,3 +34,11 @@ def test_flat_shape_option():
     assert wl.numels == [40_000_064] and wl.n_ranks == 64 and wl.max_grad_norm == 1.0
     assert wl.name == "flat_40000064_n64_bf16_clip"
     assert bench.config_of(wl, "two_pass")["shard_elems"] == 625_001
+
+
+def test_traffic_figures_survive_comment_edits_only():
+    a = "int f(int x) {\n  return x + 1;  // one more\n}\n"
+    b = "/* f: successor */\nint f(int x) {\n    return x + 1;\n}\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench.code_sha(a) == bench.code_sha(b)
+    assert bench.code_sha(a) != bench.code_sha(c)
