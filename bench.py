@@ -733,8 +733,11 @@ def calibrate_oracle(wl, seconds_total, steps):
 
 
 def cpu_baseline(wl, seconds):
-    steps = 3
-    n, _ = calibrate_oracle(wl, seconds, steps)
+    """The checker timed on a bounded sample: the first n parameters (at
+    most 2^25, so the materialised replicas stay within host memory) for as
+    many steps (at least 3) as fill about `seconds` of single-core time."""
+    n, rate = calibrate_oracle(wl, seconds, 3)
+    steps = max(3, int(round(seconds * rate / n)))
     s = oracle_sample(wl, n)
     t = time_oracle_steps(s, steps)
     out = {"value": round(s.psi * steps / t / 1e9, 6), "unit": UNIT, "cores": 1,
