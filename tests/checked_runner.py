@@ -13,7 +13,7 @@ import fsdp_sharded_mixed_shard_gb300 as Z  # noqa: E402
 Z.use_checked_library()
 
 from fsdp_sharded_mixed_shard_gb300 import workloads as W  # noqa: E402
-from parity_util import run_small  # noqa: E402
+from parity_util import random_workload, run_small  # noqa: E402
 
 
 def tiny_transformer_numels(d=64, vocab=503, ctx=128, layers=3):
@@ -80,6 +80,12 @@ def main():
         run_small(kw["wl"])
         n, first = Z.zero_checked_status()
         print(json.dumps({"case": name, "violations": n, "first": first}), flush=True)
+    # the first 24 random shapes of the random-shape parity test
+    for i in range(24):
+        wl, per_bucket, two_pass = random_workload(i)
+        run_small(wl, per_bucket=per_bucket, two_pass=two_pass)
+    n, first = Z.zero_checked_status()
+    print(json.dumps({"case": "random_shapes_24", "violations": n, "first": first}), flush=True)
     gather_case()
     n, first = Z.zero_checked_status()
     print(json.dumps({"case": "unit_gather", "violations": n, "first": first}), flush=True)

@@ -260,3 +260,33 @@ def run_sampled(wl, steps=None, n_random=2048, n_threads=None):
         g.close()
         del g
         torch.cuda.empty_cache()
+
+
+def random_case(i):
+    """Random-shape case i (seeded): N, tensor list, bucket, rank window,
+    micro-batches, gradient format, clip and per-bucket calls."""
+    rng = np.random.default_rng(20_261_202 + i)
+    n = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 13, 16, 31, 64]))
+    n_tensors = int(rng.integers(1, 5))
+    numels = [int(x) for x in rng.integers(0, 60_000, size=n_tensors)]
+    if sum(numels) == 0:
+        numels[0] = 1
+    bucket = int(rng.choice([0, 0, 7, 4096, 10_001, 32_768]))
+    lo = int(rng.integers(0, n))
+    hi = int(rng.integers(lo + 1, n + 1))
+    micro = int(rng.choice([1, 1, 2, 3]))
+    bf16 = bool(rng.integers(0, 2))
+    clip = float(rng.choice([0.0, 0.0, 0.3]))
+    per_bucket = clip > 0 and bucket > 0 and bool(rng.integers(0, 2))
+    return dict(n=n, numels=numels, bucket=bucket, lo=lo, hi=hi, micro=micro, bf16=bf16,
+                clip=clip, per_bucket=per_bucket)
+
+
+def random_workload(i):
+    """(workload, per_bucket, two_pass) of random-shape case i."""
+    from fsdp_sharded_mixed_shard_gb300 import workloads as W
+    c = random_case(i)
+    wl = W.Workload("random%d" % i, c["numels"], c["n"], c["bucket"], c["bf16"], 100 + i, 1e-3,
+                    init_scale=1.0 if c["bf16"] else 1024.0, steps=2, rank_lo=c["lo"],
+                    rank_hi=c["hi"], n_micro=c["micro"], max_grad_norm=c["clip"])
+    return wl, c["per_bucket"], c["clip"] > 0

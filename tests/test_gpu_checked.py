@@ -32,8 +32,8 @@ def test_checked_build_records_no_violation():
     assert got["selftest"]["first"] == (1 << 48) | 42
     assert got["library"]["loaded"].endswith("libzero_checked.so")
     cases = [x for x in lines if x["case"] not in ("selftest", "library")]
-    assert len(cases) == 11
-    assert {"odd_shard_two_pass_n8", "shard_4_mod_8_fused_n64",
-            "odd_shard_micro_fused_n8"} <= {x["case"] for x in cases}
+    assert len(cases) == 12
+    assert {"odd_shard_two_pass_n8", "shard_4_mod_8_fused_n64", "odd_shard_micro_fused_n8",
+            "random_shapes_24"} <= {x["case"] for x in cases}
     for x in cases:
         assert x["violations"] == 0, x
