@@ -8,6 +8,8 @@ the sm_103a kernels of _lib/libzero.so. Loading fails loudly when the library
 has not been built (run ``__graft_entry__.build()``); there is no fallback.
 """
 import ctypes as C
+
+import numpy as np
 import os
 
 from . import _build
@@ -186,14 +188,19 @@ def _check(fn, rc):
 
 
 def _ptrs(seq, need=0, what="pointer array"):
-    """Python list of device addresses (int or None) -> C array of void*.
-    The library reads `need` entries of the array (it cannot see its
-    length), so a shorter list is refused here."""
+    """Device addresses (a list of int or None, or a uint64 numpy array built
+    once by the caller) -> void** for the call. The library reads `need`
+    entries (it cannot see the length), so a shorter list is refused here.
+    The returned pointer keeps its array alive for the call."""
     if seq is None:
         return None
-    if len(seq) < need:
-        raise ValueError(f"{what}: {len(seq)} entries, the call reads {need}")
-    return (_VP * len(seq))(*[None if q is None else int(q) for q in seq])
+    if isinstance(seq, np.ndarray):
+        arr = np.ascontiguousarray(seq, dtype=np.uint64)
+    else:
+        arr = np.fromiter((0 if q is None else q for q in seq), dtype=np.uint64, count=len(seq))
+    if arr.size < need:
+        raise ValueError(f"{what}: {arr.size} entries, the call reads {need}")
+    return arr.ctypes.data_as(_P(_VP))
 
 
 def _ranks(plan):

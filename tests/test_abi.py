@@ -242,3 +242,15 @@ def test_binding_refuses_short_pointer_lists():
             Z.zero_gather_units(uplan, 0, 2, four, [16])
     finally:
         Z.zero_unit_plan_destroy(uplan)
+
+
+def test_binding_accepts_prebuilt_pointer_tables():
+    """A caller may build a per-rank pointer table once as a uint64 numpy
+    array; lists of int or None marshal to the same values."""
+    import numpy as np
+    p = Z._ptrs([16, None, 48])
+    assert [p[i] for i in range(3)] == [16, None, 48]
+    q = Z._ptrs(np.array([16, 0, 48], dtype=np.uint64))
+    assert [q[i] for i in range(3)] == [16, None, 48]
+    with pytest.raises(ValueError, match="master"):
+        Z._ptrs(np.zeros(3, dtype=np.uint64), 4, "master")
