@@ -1223,8 +1223,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
                                                                int n_slots,
                                                                uint32_t slot_bytes) {
   constexpr int E = kConsumers * EPT;  // elements per range
-  // 8 elements per thread only in the reduce pass (its 16-bit stores are
-  // the parameter stores of the other modes, done 4 at a time)
+  // 8 elements per thread only in the reduce pass: the fused and update
+  // passes store their 16-bit parameters 4 elements at a time
   static_assert(MODE == kReduce || EPT == 4, "8 elements per thread: reduce pass only");
   // shifted bodies (owner shard off the windows' 8-element grid): each
   // replica chunk holds up to 7 extra elements and each accumulator chunk up
@@ -1506,10 +1506,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&empty_bar[cur]);
       }
     }
-    // unaligned head [lo, va) and tail [vb, hi) with plain loads, after the
-    // aligned body so that the producer streams the next tile meanwhile: a few
-    // edge elements (at most 7 on each side of an aligned body) one warp
-    // each, a whole unaligned tile one thread per element (coalesced)
+    // head [lo, va) and tail [vb, hi) outside the body, with plain loads,
+    // after the body so that the producer streams the next tile meanwhile:
+    // in the fused and reduce passes up to 32 such elements one warp each
+    // (at most 7 on each side of a body), otherwise one thread per element
+    // (coalesced)
     const int nhead = static_cast<int>(t.va - t.lo);
     const int ntail = static_cast<int>(t.hi - t.vb);
     bool by_warp = false;
