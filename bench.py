@@ -6,8 +6,10 @@ reduce-scatter of N resident replicas in ring order with fp32 accumulation,
 unscale, non-finite vote, (clip for clip workloads), AdamW on the fp32
 master/m/v shard, cast to the 16-bit working copy, loss-scale bookkeeping.
 
-Default workload: GPT-2-small tensor list (124,439,808 parameters), N = 8
-simulated ranks, 25M-element buckets, bf16 gradients, fused single pass.
+Default workload: one flat tensor of 1.5e9 parameters, N = 8 simulated ranks,
+fp16 gradients with a dynamic loss scale, global-norm clip at 1.0: the
+largest parameter count of the five workloads on one GPU, on the two-pass
+path (reduce-scatter with norm records, norm finish, update, bookkeeping).
 
 Prints ONE JSON line (rank 0). `value` is Gparams/s of the whole job with
 inputs resident in HBM; `e2e` is the same metric through the C ABI with the
@@ -38,7 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sharded AdamW step Gparams/s; achieved HBM GB/s as % of GB300 peak"
 UNIT = "Gparams/s"
-PHASE_SAMPLE = 8   # timed steps per step with per-phase events
+PHASE_SAMPLE = 8   # short steps: one timed step in PHASE_SAMPLE carries per-phase events
+LONG_STEP_MS = 2.0  # steps at least this long carry per-phase events on every timed step
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -48,7 +51,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="libzero", choices=["libzero", "reference"])
-    ap.add_argument("--workload", default="gpt2_small",
+    ap.add_argument("--workload", default="flat_1p5b",
                     choices=["tiny_flat", "gpt2_small", "flat_1p5b", "stage3_slice", "llama_2b"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -333,10 +336,21 @@ def run_libzero(args, rank, world, dist):
     launches_per_step = ((2 * L) if not g.two_pass else (L + (2 if clip else 0) + L + 1)) + \
         (k_micro - 1)
 
-    for _ in range(args.warmup):
+    # the clock sampler starts before the warm-up, so that the timed region
+    # follows the warm-up steps directly (no idle gap before the first step)
+    clocks = ClockSampler(device_uuid(dev))
+    clocks.start()
+    time.sleep(0.3)
+    # the last warm-up step's time decides how the phases are sampled below
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        if i == args.warmup - 1:
+            w0.record(g.stream)
         for _, f in ph:
             f()
+    w1.record(g.stream)
     torch.cuda.synchronize()
+    warm_ms = w0.elapsed_time(w1)
     graph = None
     if args.graph:
         # one whole step as a CUDA graph: the device-resident scaler carries
@@ -354,23 +368,28 @@ def run_libzero(args, rank, world, dist):
     flush_buf = None
     if needs_flush(wl, "two_pass" if g.two_pass else "fused"):
         flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    # Phase events on every PHASE_SAMPLE-th timed step only: an event between
-    # two launches stops the next kernel from starting early (programmatic
-    # dependent launch), so the other steps run back to back as a user's do.
-    every = 1 if flush_buf is not None else PHASE_SAMPLE
-    sampled = [k for k in range(K) if k % every == 0]
+    # Per-phase events. An event between two launches stops the next kernel
+    # from starting early (programmatic dependent launch), which costs a few
+    # microseconds per launch: steps of LONG_STEP_MS or more carry events on
+    # every timed step (the cost is under 0.2 % of such a step, and the
+    # per-kernel means then come from exactly the timed steps); shorter steps
+    # carry them on one timed step in PHASE_SAMPLE, never the first, and run
+    # the others back to back as a user's do.
+    if flush_buf is not None or warm_ms >= LONG_STEP_MS:
+        every, first_sampled = 1, 0
+    else:
+        every, first_sampled = PHASE_SAMPLE, min(PHASE_SAMPLE - 1, K - 1)
+    sampled = [k for k in range(K) if k % every == first_sampled % every and k >= first_sampled]
     step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(K if flush_buf is not None else 0)]
     evs = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(len(sampled) * max(1, k_micro))] for name, _ in ph}
     ev_i = {name: 0 for name, _ in ph}
+    sampled_set = set(sampled)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(device_uuid(dev))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
     wall0 = time.time()
     t0.record(g.stream)
     for k in range(K):
@@ -378,7 +397,7 @@ def run_libzero(args, rank, world, dist):
             with torch.cuda.stream(g.stream):
                 flush_buf.fill_(k)
             step_evs[k][0].record(g.stream)
-        if k % every:
+        if k not in sampled_set:
             if graph is not None:
                 with torch.cuda.stream(g.stream):  # replay() launches on the current stream
                     graph.replay()
@@ -543,8 +562,9 @@ def run_libzero(args, rank, world, dist):
                            % (N, world)),
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * K,
             "clocks": clk, "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
-            "phase_events": "per-kernel CUDA events on every %d-th timed step (%d of %d)"
-                            % (PHASE_SAMPLE, len(sampled), K),
+            "phase_events": "per-kernel CUDA events on %d of %d timed steps (%s)"
+                            % (len(sampled), K, "every step" if every == 1 else
+                               "steps %d, %d, ... of the timed loop" % (sampled[0], sampled[0] + every)),
             "launch": "CUDA graph replay of one captured step (eager on event steps)"
                       if graph is not None else "eager C-ABI calls",
             "wall_s_timed": round(wall, 3), "scaler_t": sk.t, "device_error": sk.error}

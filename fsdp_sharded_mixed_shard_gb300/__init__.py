@@ -15,11 +15,14 @@ import os
 from . import _build
 
 __all__ = [
-    "ZeroError", "ZeroPlanInfo", "ZeroSegment", "ZeroHParams", "ZeroScaler",
-    "ZERO_BF16", "ZERO_FP16", "ZERO_MAX_RANKS", "ZERO_TILE_ELEMS",
-    "zero_plan_create", "zero_plan_destroy", "zero_plan_get_info", "zero_plan_tensor_offsets",
-    "zero_plan_segments", "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
-    "zero_reduce_scatter", "zero_grad_norm", "zero_step", "zero_step_update", "zero_step_finish",
+    "ZeroError", "ZeroPlanInfo", "ZeroSegment", "ZeroBucket", "ZeroHParams", "ZeroScaler",
+    "ZeroNormRecord", "ZeroExchange",
+    "ZERO_BF16", "ZERO_FP16", "ZERO_MAX_RANKS", "ZERO_TILE_ELEMS", "ZERO_NORM_OWNER_BLOCKS",
+    "zero_plan_create", "zero_plan_destroy", "zero_plan_get_info", "zero_plan_info_get",
+    "zero_plan_tensor_offsets", "zero_plan_segments", "zero_plan_buckets",
+    "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
+    "zero_reduce_scatter", "zero_grad_norm", "zero_grad_norm_local", "zero_grad_norm_apply",
+    "zero_step", "zero_step_update", "zero_step_finish",
     "zero_cast_params", "zero_accumulate", "zero_reduce_scatter_accum", "zero_step_accum",
     "zero_step_update_accum", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
     "zero_checked_status", "zero_selftest_check", "use_checked_library",
@@ -35,6 +38,7 @@ ZERO_BF16 = 0
 ZERO_FP16 = 1
 ZERO_MAX_RANKS = 64
 ZERO_TILE_ELEMS = 4096
+ZERO_NORM_OWNER_BLOCKS = 16
 ZERO_UNIT_MAX_ALIGN = 4096
 (ZERO_FULL_SHARD, ZERO_SHARD_GRAD_OP, ZERO_NO_SHARD, ZERO_HYBRID_SHARD,
  ZERO_NO_RESHARD_AFTER_FORWARD) = range(5)
@@ -61,6 +65,22 @@ class ZeroPlanInfo(C.Structure):
 
 class ZeroSegment(C.Structure):
     _fields_ = [("lo", C.c_int64), ("hi", C.c_int64), ("rank", C.c_int32), ("bucket", C.c_int32)]
+
+
+class ZeroBucket(C.Structure):
+    _fields_ = [("lo", C.c_int64), ("hi", C.c_int64), ("seg_first", C.c_int32),
+                ("seg_count", C.c_int32)]
+
+
+class ZeroNormRecord(C.Structure):
+    _fields_ = [("hi", C.c_float), ("lo", C.c_float), ("big_hi", C.c_float),
+                ("big_lo", C.c_float)]
+
+
+class ZeroExchange(C.Structure):
+    """zero.h zero_exchange: one process's share of a step's global scalars."""
+    _fields_ = [("overflow", C.c_uint32), ("reserved", C.c_uint32 * 3),
+                ("owner", ZeroNormRecord * ZERO_MAX_RANKS)]
 
 
 class ZeroHParams(C.Structure):
@@ -134,16 +154,21 @@ def lib():
         L.zero_plan_destroy.argtypes = [_VP]
         L.zero_plan_destroy.restype = None
         L.zero_plan_get_info.argtypes = [_VP, _P(ZeroPlanInfo)]
+        L.zero_plan_info_get.argtypes = [_VP, _P(ZeroPlanInfo)]
+        L.zero_plan_buckets.argtypes = [_VP, _P(ZeroBucket), _P(ZeroSegment)]
         L.zero_plan_tensor_offsets.argtypes = [_VP, _P(C.c_int64)]
         L.zero_plan_segments.argtypes = [_VP, _P(ZeroSegment), C.c_int32]
         L.zero_plan_bucket_range.argtypes = [_VP, C.c_int32, _P(C.c_int64), _P(C.c_int64)]
-        L.zero_workspace_bytes.argtypes = [_VP]
+        L.zero_workspace_bytes.argtypes = [_VP, C.c_int32]
         L.zero_workspace_bytes.restype = C.c_size_t
         L.zero_scaler_init.argtypes = [_P(ZeroHParams), _P(ZeroScaler)]
         L.zero_reduce_scatter.argtypes = [_VP, C.c_int32, C.c_int32, C.c_int32, _P(_VP),
                                           C.c_int64, _P(_VP), _VP, _VP, _VP, _VP]
         L.zero_grad_norm.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(ZeroHParams), _VP,
                                      _VP, _VP]
+        L.zero_grad_norm_local.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP),
+                                           _P(ZeroHParams), _VP, _VP, _VP, _VP]
+        L.zero_grad_norm_apply.argtypes = [_VP, _VP, _P(ZeroHParams), _VP, _VP]
         L.zero_step.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _P(_VP), C.c_int32,
                                 _P(_VP), _P(_VP), C.c_int64, _VP, _P(ZeroHParams), _VP, _VP, _VP]
         L.zero_step_update.argtypes = L.zero_step.argtypes
@@ -243,6 +268,12 @@ def zero_plan_get_info(plan):
     return info
 
 
+def zero_plan_info_get(plan):
+    info = ZeroPlanInfo()
+    _check("zero_plan_info_get", lib().zero_plan_info_get(plan, C.byref(info)))
+    return info
+
+
 def zero_plan_tensor_offsets(plan):
     n = zero_plan_get_info(plan).n_tensors
     out = (C.c_int64 * max(n, 1))()
@@ -257,6 +288,17 @@ def zero_plan_segments(plan):
     return [(s.lo, s.hi, s.rank, s.bucket) for s in out[:n]]
 
 
+def zero_plan_buckets(plan):
+    """(buckets, segments): lists of (lo, hi, seg_first, seg_count) and of
+    (lo, hi, rank, bucket)."""
+    info = zero_plan_get_info(plan)
+    bk = (ZeroBucket * max(info.n_buckets, 1))()
+    sg = (ZeroSegment * max(info.n_segments, 1))()
+    _check("zero_plan_buckets", lib().zero_plan_buckets(plan, bk, sg))
+    return ([(b.lo, b.hi, b.seg_first, b.seg_count) for b in bk[:info.n_buckets]],
+            [(s.lo, s.hi, s.rank, s.bucket) for s in sg[:info.n_segments]])
+
+
 def zero_plan_bucket_range(plan, bucket):
     lo, hi = C.c_int64(), C.c_int64()
     _check("zero_plan_bucket_range", lib().zero_plan_bucket_range(plan, bucket, C.byref(lo),
@@ -264,8 +306,8 @@ def zero_plan_bucket_range(plan, bucket):
     return lo.value, hi.value
 
 
-def zero_workspace_bytes(plan):
-    return int(lib().zero_workspace_bytes(plan))
+def zero_workspace_bytes(plan, two_pass=1):
+    return int(lib().zero_workspace_bytes(plan, int(bool(two_pass))))
 
 
 def zero_scaler_init(hp):
@@ -297,6 +339,19 @@ def zero_grad_norm(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, d_workspac
     _check("zero_grad_norm", lib().zero_grad_norm(
         plan, rank_lo, rank_hi, q["grad_shards"], C.byref(hp), _vp(d_scaler),
         _vp(d_workspace), _vp(stream)))
+
+
+def zero_grad_norm_local(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, d_workspace,
+                         d_exchange, stream=0):
+    q = _rank_arrays(plan, grad_shards=grad_shards)
+    _check("zero_grad_norm_local", lib().zero_grad_norm_local(
+        plan, rank_lo, rank_hi, q["grad_shards"], C.byref(hp), _vp(d_scaler), _vp(d_workspace),
+        _vp(d_exchange), _vp(stream)))
+
+
+def zero_grad_norm_apply(plan, d_exchange, hp, d_scaler, stream=0):
+    _check("zero_grad_norm_apply", lib().zero_grad_norm_apply(
+        plan, _vp(d_exchange), C.byref(hp), _vp(d_scaler), _vp(stream)))
 
 
 def zero_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,

@@ -39,4 +39,18 @@ cudaError_t launch_pdl(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Actual>(args)...);
 }
 
+// An ordinary stream-ordered launch (no programmatic dependency) that
+// returns the launch's own status, so a caller's earlier sticky error is
+// neither consumed nor reported as this launch's.
+template <typename... KernelArgs, typename... Actual>
+cudaError_t launch_plain(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Actual&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Actual>(args)...);
+}
+
 #endif

@@ -129,6 +129,10 @@ ZERO_API int zero_plan_get_info(const zero_plan* plan, zero_plan_info* out) {
   return ZERO_OK;
 }
 
+ZERO_API int zero_plan_info_get(const zero_plan* plan, zero_plan_info* out) {
+  return zero_plan_get_info(plan, out);
+}
+
 ZERO_API int zero_plan_tensor_offsets(const zero_plan* plan, int64_t* out) {
   if (!plan || (!out && !plan->offsets.empty())) return ZERO_EINVAL;
   std::copy(plan->offsets.begin(), plan->offsets.end(), out);
@@ -141,6 +145,28 @@ ZERO_API int zero_plan_segments(const zero_plan* plan, zero_segment* out, int32_
   const int32_t c = std::min(n, cap);
   std::copy(plan->segs.begin(), plan->segs.begin() + c, out);
   return cap < n ? ZERO_ERANGE : ZERO_OK;
+}
+
+ZERO_API int zero_plan_buckets(const zero_plan* plan, zero_bucket* out, zero_segment* segs) {
+  if (!plan) return ZERO_EINVAL;
+  if (segs) std::copy(plan->segs.begin(), plan->segs.end(), segs);
+  if (!out) return ZERO_OK;
+  const int32_t nb = plan->info.n_buckets;
+  for (int32_t b = 0; b < nb; ++b) {
+    int64_t lo = 0, hi = 0;
+    zero_plan_bucket_range(plan, b, &lo, &hi);
+    out[b].lo = lo;
+    out[b].hi = hi;
+    out[b].seg_first = 0;
+    out[b].seg_count = 0;
+  }
+  // segments are ordered by lo, so each bucket's segments are one run
+  for (int32_t s = plan->info.n_segments - 1; s >= 0; --s) {
+    zero_bucket& b = out[plan->segs[s].bucket];
+    b.seg_first = s;
+    b.seg_count += 1;
+  }
+  return ZERO_OK;
 }
 
 ZERO_API int zero_plan_bucket_range(const zero_plan* plan, int32_t bucket, int64_t* lo,
@@ -157,11 +183,12 @@ ZERO_API int zero_plan_bucket_range(const zero_plan* plan, int32_t bucket, int64
   return ZERO_OK;
 }
 
-ZERO_API size_t zero_workspace_bytes(const zero_plan* plan) {
-  if (!plan) return 0;
-  // one 16-byte norm record per tile, then 256 records for the finish kernels
-  size_t b = (static_cast<size_t>(plan->info.n_tiles) + 256) * 16;
-  return (b + 255) & ~static_cast<size_t>(255);
+ZERO_API size_t zero_workspace_bytes(const zero_plan* plan, int32_t two_pass) {
+  if (!plan || !two_pass) return 0;
+  // one 16-byte norm record per tile, then the norm finish's share records
+  const size_t records = static_cast<size_t>(plan->info.n_tiles) +
+                         static_cast<size_t>(plan->info.n_ranks) * zero_detail::kNormOwnerBlocks;
+  return (records * 16 + 255) & ~static_cast<size_t>(255);
 }
 
 ZERO_API int zero_scaler_init(const zero_hparams* hp, zero_scaler* out) {

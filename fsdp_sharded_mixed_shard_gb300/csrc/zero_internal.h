@@ -21,6 +21,9 @@ struct zero_plan {
 
 namespace zero_detail {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// norm finish: share records per owner that the workspace holds after the
+// tile records (one 16-byte record each)
+constexpr int kNormOwnerBlocks = 16;
 }  // namespace zero_detail
 
 #endif

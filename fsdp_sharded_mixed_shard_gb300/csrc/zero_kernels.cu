@@ -3,30 +3,37 @@
  * and the launch layer behind the C ABI (zero.h).
  *
  * Kernels
- *   step_kernel<MODE, dtype>  one persistent, tile-scheduled kernel body with
- *                             four modes:
+ *   bulk_kernel<MODE, dtype, ...>  the three streaming passes, each a
+ *                             persistent cp.async.bulk + mbarrier pipeline
+ *                             (one producer warp, sixteen consumer warps):
  *     kFused  reduce-scatter + unscale + non-finite vote + AdamW + cast in one
  *             pass; reads the current optimizer set, writes the other one
  *             (2N + 26 bytes per element);
  *     kReduce reduce-scatter + unscale + vote, writes fp32 g and the per-tile
- *             squared-norm partials (2N + 4 bytes per element);
+ *             squared-norm records (2N + 4 bytes per element);
  *     kUpdate AdamW + cast from fp32 g, in place, after the overflow and clip
- *             decisions are known (30 bytes per element);
- *     kNorm   per-tile squared-norm partials from fp32 g (4 bytes per element);
+ *             decisions are known (30 bytes per element).
+ *   step_kernel<MODE, dtype>  a plain tile-scheduled kernel for the two light
+ *                             modes:
+ *     kNorm   per-tile squared-norm records from fp32 g (4 bytes per element);
  *     kCast   16-bit working copy from an fp32 master set (6 bytes per element),
- *             optionally only when the step's overflow word is set.
- *   norm_blocks_kernel,       fixed-partition float-float merge of the tile
- *   norm_final_kernel         records; fp64 norm and clip coefficient.
+ *             optionally only when the step's overflow word is set, and then
+ *             the step's bookkeeping in the last CTA.
+ *   norm_owner_kernel,        fixed-partition float-float merge of each
+ *   norm_final_kernel,        owner's tile records; owner records merged in
+ *   norm_import_kernel        ascending owner order; fp64 norm and clip
+ *                             coefficient (or the owner records exported for
+ *                             a cross-process exchange, and their import).
  *   scaler_finish_kernel      loss-scale / skip / step-count bookkeeping (one
  *                             thread).
  *
  * Work decomposition: the owned elements are cut into segments (one bucket of
  * one rank) and each segment into tiles of ZERO_TILE_ELEMS elements. A
- * persistent grid (a multiple of the SM count) walks the tiles round-robin;
- * inside a tile each thread handles 16-byte vectors of 8 elements, so a warp
- * reads 512 contiguous bytes of each replica per access. Segment starts that
- * are not 8-element aligned in the replicas, or whose optimizer shard is not
- * 4-element aligned at the same point, take a scalar path.
+ * persistent grid walks the tiles round-robin. In the bulk passes an owner
+ * whose slice starts off the windows' 8-element grid gets a shard-indexed
+ * body whose replica chunks are copied from the 16-byte block below their
+ * first element (see tile_geom); the few elements of a tile outside its
+ * body take per-element paths.
  *
  * Arithmetic: every fp32 operation of the step is an explicit round-to-
  * nearest-even intrinsic (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn) and
@@ -57,7 +64,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTile = ZERO_TILE_ELEMS;
 constexpr int kVec = 8;                       // 16-bit elements per 16-byte vector
 constexpr int kMaxSegs = 128;                 // segments per launch (kernel parameter space)
-constexpr int kChunk = 8;                     // replicas loaded together
 
 static_assert(kTile % (kVec * kThreads) == 0, "tile must be a whole number of vector passes");
 
@@ -490,87 +496,24 @@ __device__ void compute_step_scalars(const Args& a, StepScalars* out) {
 
 // ------------------------------------------------------------- the body --
 
-// Per-element work on a vector of 8 elements starting at flat index j
-// (aligned path) -- MODE-specific.
+// Per-element work of step_kernel on a vector of 8 elements starting at flat
+// index j: kNorm adds the squares of 8 reduced gradients to the tile's
+// record, kCast writes 8 parameters from the master set.
 template <int MODE, bool kBf16>
 __device__ __forceinline__ void do_vector(const Args& a, const StepScalars& s, int64_t j,
-                                          int32_t rank, int first_rep, NormAcc& nacc,
-                                          bool& bad) {
+                                          int32_t rank, NormAcc& nacc) {
+  static_assert(MODE == kNorm || MODE == kCast, "step_kernel modes only");
   const int64_t w = j - a.wbase;                    // window index
   const int64_t k = j - static_cast<int64_t>(rank) * a.shard;  // shard index
   if (!ZCHECK(w >= 0 && w + 8 <= a.wend && k >= 0 && k + 8 <= a.shard, kSiteVector, j)) return;
-  float g[8];
-  float th[8], m[8], v[8];
-  if constexpr (MODE == kFused || MODE == kUpdate) {
-    load8f(a.master[s.src][rank] + k, th);
-    load8f(a.mom[s.src][rank] + k, m);
-    load8f(a.var[s.src][rank] + k, v);
-  }
-  if constexpr (MODE == kFused || MODE == kReduce) {
-    const int N = a.n_ranks;
-    float acc[8];
-    for (int base = 0; base < N; base += kChunk) {
-      uint4 r[kChunk];
-#pragma unroll
-      for (int c = 0; c < kChunk; ++c) {
-        const int p = base + c;
-        if (p < N) {
-          int rr = first_rep + p;
-          if (rr >= N) rr -= N;
-          r[c] = __ldcs(reinterpret_cast<const uint4*>(a.rep[rr] + w));
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < kChunk; ++c) {
-        const int p = base + c;
-        if (p < N) {
-          float x[8];
-          widen8<kBf16>(r[c], x);
-          if (p == 0) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = x[e];
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      g[e] = __fmul_rn(acc[e], s.inv);
-      bad |= nonfinite(g[e]);
-    }
-  }
-  if constexpr (MODE == kUpdate || MODE == kNorm) {
-    load8f(a.ghat[rank] + k, g);
-  }
-  if constexpr (MODE == kReduce) {
-    store8f(a.ghat[rank] + k, g);
-    if (a.mode_flags & kFlagPartials) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) nacc.add(g[e]);
-    }
-  }
+  float x[8];
   if constexpr (MODE == kNorm) {
+    load8f(a.ghat[rank] + k, x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) nacc.add(g[e]);
-  }
-  if constexpr (MODE == kFused || MODE == kUpdate) {
-    if (MODE == kUpdate && s.clip != 1.0f) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) g[e] = __fmul_rn(g[e], s.clip);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) adamw(th[e], m[e], v[e], g[e], a, s);
-    store8f(a.master[s.dst][rank] + k, th);
-    store8f(a.mom[s.dst][rank] + k, m);
-    store8f(a.var[s.dst][rank] + k, v);
-    __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(th));
-  }
-  if constexpr (MODE == kCast) {
-    load8f(a.master[s.src][rank] + k, th);
-    __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(th));
+    for (int e = 0; e < 8; ++e) nacc.add(x[e]);
+  } else {
+    load8f(a.master[s.src][rank] + k, x);
+    __stcs(reinterpret_cast<uint4*>(a.flat + w), narrow8<kBf16>(x));
   }
 }
 
@@ -673,8 +616,13 @@ __device__ __forceinline__ void do_scalar_warp(const Args& a, const StepScalars&
   }
 }
 
+// The light modes (kNorm, kCast) as a plain tile-scheduled kernel: 16-byte
+// vectors of 8 elements where an owner's slice sits on the windows'
+// 8-element grid and its shard on the 4-element grid, single elements
+// elsewhere (coalesced over the CTA's threads).
 template <int MODE, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant__ Args a) {
+  static_assert(MODE == kNorm || MODE == kCast, "the streaming modes run in bulk_kernel");
   __shared__ StepScalars sh_s;
   __shared__ NormSlots sh_norm;
   pdl_begin();
@@ -696,13 +644,11 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
     const int64_t lo = sg.lo + (g - sg.tile_local0) * kTile;
     const int64_t hi = min(lo + kTile, sg.hi);
     const int32_t rank = sg.rank;
-    int first_rep = rank + 1;
-    if (first_rep >= a.n_ranks) first_rep -= a.n_ranks;
     NormAcc nacc;
-    bool bad = false;
+    bool unused = false;
 
     // vector body [va, vb): 8-element aligned in the windows and 4-element
-    // aligned in the shards; otherwise everything is scalar
+    // aligned in the shards; otherwise every element takes the single path
     const int64_t rank0 = static_cast<int64_t>(rank) * a.shard;
     const bool vec_ok = (((rank0 - a.wbase) & 3) == 0);
     int64_t va = hi, vb = hi;
@@ -713,32 +659,25 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const __grid_constant
     }
     const int nvec = static_cast<int>((vb - va) >> 3);
     for (int q = threadIdx.x; q < nvec; q += kThreads)
-      do_vector<MODE, kBf16>(a, s, va + static_cast<int64_t>(q) * kVec, rank, first_rep, nacc,
-                             bad);
-    // scalar head [lo, va) and tail [vb, hi)
+      do_vector<MODE, kBf16>(a, s, va + static_cast<int64_t>(q) * kVec, rank, nacc);
+    // head [lo, va) and tail [vb, hi)
     const int nhead = static_cast<int>(va - lo);
     const int ntail = static_cast<int>(hi - vb);
     for (int q = threadIdx.x; q < nhead + ntail; q += kThreads) {
       const int64_t j = q < nhead ? lo + q : vb + (q - nhead);
-      do_scalar<MODE, kBf16>(a, s, j, rank, first_rep, nacc, bad);
+      do_scalar<MODE, kBf16>(a, s, j, rank, 0, nacc, unused);
     }
 
-    if constexpr (MODE == kFused || MODE == kReduce) {
-      // non-finite vote: one atomic per warp that saw one
-      if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) raise_flag(a, sg.bucket);
-    }
-    if constexpr (MODE == kReduce || MODE == kNorm) {
-      if (MODE == kNorm || (a.mode_flags & kFlagPartials)) {
-        // publish, one barrier, and the tile's fp64 total formed by warp
-        // (tile_no mod 8) so the fp64 work rotates over the warps
-        const int par = tile_no & 1;
-        tile_norm_publish(nacc, sh_norm, par, warp, lane);
-        __syncthreads();
-        if (warp == static_cast<int>(tile_no % kWarps)) {
-          const float4 rec = tile_norm_record(sh_norm, par, kWarps, lane);
-          const int64_t r = sg.tile_global0 + (g - sg.tile_local0);
-          if (lane == 0 && ZCHECK(r >= 0 && r < a.n_records, kSiteRecord, r)) a.partials[r] = rec;
-        }
+    if constexpr (MODE == kNorm) {
+      // publish, one barrier, and the tile's record formed by warp
+      // (tile_no mod 8), so that the merge rotates over the warps
+      const int par = tile_no & 1;
+      tile_norm_publish(nacc, sh_norm, par, warp, lane);
+      __syncthreads();
+      if (warp == static_cast<int>(tile_no % kWarps)) {
+        const float4 rec = tile_norm_record(sh_norm, par, kWarps, lane);
+        const int64_t r = sg.tile_global0 + (g - sg.tile_local0);
+        if (lane == 0 && ZCHECK(r >= 0 && r < a.n_records, kSiteRecord, r)) a.partials[r] = rec;
       }
     }
   }
@@ -1588,18 +1527,31 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   }
 }
 
-// Norm finish, two small kernels with a fixed partition (independent of the
-// GPU), so the result is deterministic:
-//   norm_blocks_kernel: kFinishBlocks CTAs; CTA b merges the tile records of
-//     its contiguous share of [t0, t1) (thread k takes every
-//     kFinishThreads-th record, then fixed shuffle and shared-memory trees)
-//     into one record, in fp32 float-float;
-//   norm_final_kernel: one CTA merges the kFinishBlocks records the same way,
-//     forms norm^2 = hi + lo + 2^192 (bhi + blo) in fp64, the norm and the
-//     clip coefficient c = max_norm / (norm + 1e-6) (fp64; applied, rounded
-//     to fp32, only when c < 1).
-constexpr int kFinishBlocks = 256;
+// Norm finish. The global squared norm is defined so that it does not depend
+// on how the owners are split over calls or processes:
+//   owner record R_i: owner i's tile records merged in float-float over a
+//     fixed partition of its own tiles (kOwnerBlocks contiguous shares;
+//     inside a share thread k takes every kFinishThreads-th record, then a
+//     fixed CTA tree; the kOwnerBlocks share records then a fixed 16-lane
+//     shuffle tree);
+//   total = R_lo + ... + R_{hi-1}: float-float merges in ascending owner
+//     order (a zero record merges as the identity, so owners outside a
+//     window change nothing);
+//   norm^2 = hi + lo + 2^192 (bhi + blo) in fp64, the norm and the clip
+//     coefficient c = max_norm / (norm + 1e-6) in fp64 (applied, rounded to
+//     fp32, only when c < 1).
+// R_i depends only on owner i's gradients, so processes that own disjoint
+// windows can export their records (norm_final_kernel, export mode), add the
+// exports up and import the sum (norm_import_kernel): each then holds what
+// one call over all owners computes, bit for bit.
+constexpr int kOwnerBlocks = zero_detail::kNormOwnerBlocks;
 constexpr int kFinishThreads = 256;
+static_assert(kOwnerBlocks * ZERO_MAX_RANKS <= 1024, "one final CTA holds every share record");
+
+// first tile (plan numbering) of each owner of a window, plus the end
+struct OwnerTiles {
+  int64_t t[ZERO_MAX_RANKS + 1];
+};
 
 // Merge the kFinishThreads per-thread accumulators of a CTA; result in
 // thread 0.
@@ -1636,57 +1588,146 @@ __device__ NormAcc cta_merge(NormAcc t, float4* sh) {
   return r;
 }
 
-__global__ void __launch_bounds__(kFinishThreads) norm_blocks_kernel(
-    const float4* __restrict__ records, int64_t t0, int64_t t1, float4* __restrict__ out) {
+// CTA (b, i): share b of the tiles of owner rank_lo + i. Tile t's record is
+// records[t - rec_base]; the share's record goes to
+// blocks[owner * kOwnerBlocks + b].
+__global__ void __launch_bounds__(kFinishThreads) norm_owner_kernel(
+    const float4* __restrict__ records, int64_t rec_base, int64_t n_records,
+    const __grid_constant__ OwnerTiles ot, int32_t rank_lo, float4* __restrict__ blocks) {
   __shared__ float4 sh[kFinishThreads / 32];
   pdl_begin();
-  const int64_t n = t1 - t0;
-  const int64_t chunk = (n + kFinishBlocks - 1) / kFinishBlocks;
+  const int i = blockIdx.y;
+  const int64_t t0 = ot.t[i], t1 = ot.t[i + 1];
+  const int64_t chunk = (t1 - t0 + kOwnerBlocks - 1) / kOwnerBlocks;
   const int64_t b0 = t0 + blockIdx.x * chunk;
   const int64_t b1 = min(b0 + chunk, t1);
   NormAcc t;
-  for (int64_t i = b0 + threadIdx.x; i < b1; i += kFinishThreads) {
-    const float4 q = records[i];
+  for (int64_t k = b0 + threadIdx.x; k < b1; k += kFinishThreads) {
+    const int64_t r = k - rec_base;
+    if (!ZCHECK(r >= 0 && r < n_records, kSiteRecord, r)) continue;
+    const float4 q = records[r];
     t.merge(q.x, q.y, q.z, q.w);
   }
-  const NormAcc r = cta_merge(t, sh);
-  if (threadIdx.x == 0) out[blockIdx.x] = make_float4(r.hi, r.lo, r.bhi, r.blo);
+  const NormAcc m = cta_merge(t, sh);
+  if (threadIdx.x == 0)
+    blocks[(rank_lo + i) * kOwnerBlocks + blockIdx.x] = make_float4(m.hi, m.lo, m.bhi, m.blo);
 }
 
-__global__ void __launch_bounds__(kFinishThreads) norm_final_kernel(
-    const float4* __restrict__ blocks, double max_norm, zero_scaler* sc) {
-  __shared__ float4 sh[kFinishThreads / 32];
+// norm^2, the norm and the clip coefficient from a total record.
+__device__ void finish_norm(const NormAcc& r, double max_norm, zero_scaler* sc) {
+  double nsq = __dadd_rn(static_cast<double>(r.hi), static_cast<double>(r.lo));
+  if (r.bhi != 0.f || r.blo != 0.f)
+    nsq = __dadd_rn(nsq, __dmul_rn(__dadd_rn(static_cast<double>(r.bhi),
+                                             static_cast<double>(r.blo)),
+                                   0x1p192));
+  const double nrm = __dsqrt_rn(nsq);
+  const double c = __ddiv_rn(max_norm, __dadd_rn(nrm, 1e-6));
+  sc->norm_sq = nsq;
+  sc->norm = nrm;
+  sc->clip_apply = c < 1.0 ? 1 : 0;
+  sc->clip_coef = c < 1.0 ? __double2float_rn(c) : 1.0f;
+  sc->norm_step = sc->t + 1;
+}
+
+constexpr int kFinalThreads = kOwnerBlocks * ZERO_MAX_RANKS;
+
+// One CTA. Owner records R_o of [rank_lo, rank_hi) from the share records
+// (16 lanes per owner). Apply mode: total in ascending owner order, then
+// the scaler's norm fields. Export mode: the records of the window and
+// zeros elsewhere, and the scaler's overflow word, into *ex.
+__global__ void __launch_bounds__(kFinalThreads) norm_final_kernel(
+    const float4* __restrict__ blocks, int32_t rank_lo, int32_t rank_hi, int32_t export_mode,
+    double max_norm, zero_scaler* sc, zero_exchange* ex) {
+  __shared__ float4 sh_owner[ZERO_MAX_RANKS];
   pdl_begin();
+  const int tid = threadIdx.x;
+  const int o = rank_lo + tid / kOwnerBlocks;
+  const int part = tid % kOwnerBlocks;
   NormAcc t;
-  for (int i = threadIdx.x; i < kFinishBlocks; i += kFinishThreads) {
-    const float4 q = blocks[i];
-    t.merge(q.x, q.y, q.z, q.w);
+  if (o < rank_hi) {
+    const float4 q = blocks[o * kOwnerBlocks + part];
+    t.hi = q.x;
+    t.lo = q.y;
+    t.bhi = q.z;
+    t.blo = q.w;
   }
-  const NormAcc r = cta_merge(t, sh);
-  if (threadIdx.x == 0) {
-    double nsq = __dadd_rn(static_cast<double>(r.hi), static_cast<double>(r.lo));
-    if (r.bhi != 0.f || r.blo != 0.f)
-      nsq = __dadd_rn(nsq, __dmul_rn(__dadd_rn(static_cast<double>(r.bhi),
-                                               static_cast<double>(r.blo)),
-                                     0x1p192));
-    const double nrm = __dsqrt_rn(nsq);
-    const double c = __ddiv_rn(max_norm, __dadd_rn(nrm, 1e-6));
-    sc->norm_sq = nsq;
-    sc->norm = nrm;
-    sc->clip_apply = c < 1.0 ? 1 : 0;
-    sc->clip_coef = c < 1.0 ? __double2float_rn(c) : 1.0f;
-    sc->norm_step = sc->t + 1;
+#pragma unroll
+  for (int off = kOwnerBlocks / 2; off > 0; off >>= 1) {
+    float h2 = __shfl_down_sync(0xFFFFFFFFu, t.hi, off, kOwnerBlocks);
+    float l2 = __shfl_down_sync(0xFFFFFFFFu, t.lo, off, kOwnerBlocks);
+    float bh2 = __shfl_down_sync(0xFFFFFFFFu, t.bhi, off, kOwnerBlocks);
+    float bl2 = __shfl_down_sync(0xFFFFFFFFu, t.blo, off, kOwnerBlocks);
+    if (part < off) t.merge(h2, l2, bh2, bl2);
+  }
+  if (part == 0 && o < rank_hi) sh_owner[o] = make_float4(t.hi, t.lo, t.bhi, t.blo);
+  __syncthreads();
+  if (export_mode) {
+    for (int k = tid; k < ZERO_MAX_RANKS; k += kFinalThreads) {
+      const float4 q = (k >= rank_lo && k < rank_hi) ? sh_owner[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ex->owner[k].hi = q.x;
+      ex->owner[k].lo = q.y;
+      ex->owner[k].big_hi = q.z;
+      ex->owner[k].big_lo = q.w;
+    }
+    if (tid == 0) {
+      ex->overflow = sc->pending ? 1u : 0u;
+      ex->reserved[0] = ex->reserved[1] = ex->reserved[2] = 0u;
+    }
+    return;
+  }
+  if (tid == 0) {
+    NormAcc total;
+    for (int k = rank_lo; k < rank_hi; ++k) {
+      const float4 q = sh_owner[k];
+      total.merge(q.x, q.y, q.z, q.w);
+    }
+    finish_norm(total, max_norm, sc);
   }
 }
 
-int launch_norm_finish(const float4* records, int64_t t0, int64_t t1, float4* blocks,
-                       double max_norm, zero_scaler* sc, cudaStream_t st) {
-  if (launch_pdl(norm_blocks_kernel, dim3(kFinishBlocks), dim3(kFinishThreads), 0, st, records, t0,
-                 t1, blocks) != cudaSuccess ||
-      launch_pdl(norm_final_kernel, dim3(1), dim3(kFinishThreads), 0, st,
-                 static_cast<const float4*>(blocks), max_norm, sc) != cudaSuccess)
+// Import of an exchange: the step's overflow word, and with clipping the
+// norm fields from the records of all n_ranks owners in ascending order.
+__global__ void norm_import_kernel(const zero_exchange* ex, int32_t n_ranks, int32_t clip,
+                                   double max_norm, zero_scaler* sc) {
+  pdl_begin();
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  if (ex->overflow) sc->pending |= 1u;
+  if (!clip) return;
+  NormAcc total;
+  for (int k = 0; k < n_ranks; ++k) {
+    const zero_norm_record q = ex->owner[k];
+    total.merge(q.hi, q.lo, q.big_hi, q.big_lo);
+  }
+  finish_norm(total, max_norm, sc);
+}
+
+// First tile (plan numbering) of owner o; the plan's tile count for o = N.
+int64_t owner_tile0(const zero_plan* p, int32_t o) {
+  const int32_t s = p->rank_seg0[o];
+  return s < p->info.n_segments ? p->seg_tile0[s] : p->info.n_tiles;
+}
+
+// The owner records of [rank_lo, rank_hi) from the tile records, into
+// blocks (kOwnerBlocks share records per owner, indexed by absolute owner);
+// then the final kernel in apply or export mode. Tile t's record is
+// records[t - rec_base], n_records of them.
+int launch_norm_finish(const zero_plan* p, int32_t rank_lo, int32_t rank_hi,
+                       const float4* records, int64_t rec_base, int64_t n_records, float4* blocks,
+                       int export_mode, double max_norm, zero_scaler* sc, zero_exchange* ex,
+                       cudaStream_t st) {
+  if (rank_hi > rank_lo) {
+    OwnerTiles ot{};
+    for (int32_t o = rank_lo; o <= rank_hi; ++o) ot.t[o - rank_lo] = owner_tile0(p, o);
+    if (launch_pdl(norm_owner_kernel, dim3(kOwnerBlocks, rank_hi - rank_lo),
+                   dim3(kFinishThreads), 0, st, records, rec_base, n_records, ot, rank_lo,
+                   blocks) != cudaSuccess)
+      return ZERO_ECUDA;
+  }
+  if (launch_pdl(norm_final_kernel, dim3(1), dim3(kFinalThreads), 0, st,
+                 static_cast<const float4*>(blocks), rank_lo, rank_hi, export_mode, max_norm,
+                 sc, ex) != cudaSuccess)
     return ZERO_ECUDA;
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  return ZERO_OK;
 }
 
 // Bookkeeping alone (two-pass path, and plans without elements).
@@ -2033,6 +2074,28 @@ ZERO_API int zero_reduce_scatter_accum(const zero_plan* plan, int32_t bucket, in
   return rc;
 }
 
+namespace {
+
+// Tile records of the owners [rank_lo, rank_hi) recomputed from the reduced
+// gradients (kNorm pass), into the workspace's tile records.
+int recompute_records(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                      const float* const* grad_shards, zero_scaler* d_scaler, void* d_workspace,
+                      cudaStream_t st) {
+  int rc = check_ptr_array(reinterpret_cast<const void* const*>(grad_shards), rank_lo, rank_hi,
+                           0, 1);
+  if (rc) return rc;
+  Args* a = new_args(plan);
+  if (!a) return ZERO_ENOMEM;
+  for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = const_cast<float*>(grad_shards[i]);
+  a->scaler = d_scaler;
+  a->partials = static_cast<float4*>(d_workspace);
+  rc = launch<kNorm>(plan, *a, plan->rank_seg0[rank_lo], plan->rank_seg0[rank_hi], st);
+  delete a;
+  return rc;
+}
+
+}  // namespace
+
 ZERO_API int zero_grad_norm(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
                             const float* const* grad_shards, const zero_hparams* hp,
                             zero_scaler* d_scaler, void* d_workspace, void* stream) {
@@ -2041,25 +2104,51 @@ ZERO_API int zero_grad_norm(const zero_plan* plan, int32_t rank_lo, int32_t rank
   if (!zero_detail::aligned16(d_scaler) || !zero_detail::aligned16(d_workspace))
     return ZERO_EALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
   if (grad_shards) {
-    int rc = check_ptr_array(reinterpret_cast<const void* const*>(grad_shards), rank_lo, rank_hi,
-                             0, 1);
-    if (rc) return rc;
-    Args* a = new_args(plan);
-    if (!a) return ZERO_ENOMEM;
-    for (int32_t i = rank_lo; i < rank_hi; ++i) a->ghat[i] = const_cast<float*>(grad_shards[i]);
-    a->scaler = d_scaler;
-    a->partials = static_cast<float4*>(d_workspace);
-    rc = launch<kNorm>(plan, *a, s0, s1, st);
-    delete a;
+    const int rc = recompute_records(plan, rank_lo, rank_hi, grad_shards, d_scaler, d_workspace,
+                                     st);
     if (rc) return rc;
   }
-  const int64_t t0 = s0 < s1 ? plan->seg_tile0[s0] : 0;
-  const int64_t t1 = s0 < s1 ? plan->seg_tile0[s1 - 1] + plan->seg_tiles[s1 - 1] : 0;
   float4* records = static_cast<float4*>(d_workspace);
-  return launch_norm_finish(records, t0, t1, records + plan->info.n_tiles, hp->max_grad_norm,
-                            d_scaler, st);
+  return launch_norm_finish(plan, rank_lo, rank_hi, records, 0, plan->info.n_tiles,
+                            records + plan->info.n_tiles, 0, hp->max_grad_norm, d_scaler,
+                            nullptr, st);
+}
+
+ZERO_API int zero_grad_norm_local(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                                  const float* const* grad_shards, const zero_hparams* hp,
+                                  zero_scaler* d_scaler, void* d_workspace,
+                                  zero_exchange* d_exchange, void* stream) {
+  if (!ranks_ok(plan, rank_lo, rank_hi) || !hp || !d_scaler || !d_exchange) return ZERO_EINVAL;
+  const bool clip = hp->max_grad_norm > 0.0;
+  if (clip && !d_workspace) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler) || !zero_detail::aligned16(d_workspace) ||
+      !zero_detail::aligned16(d_exchange))
+    return ZERO_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (clip && grad_shards) {
+    const int rc = recompute_records(plan, rank_lo, rank_hi, grad_shards, d_scaler, d_workspace,
+                                     st);
+    if (rc) return rc;
+  }
+  float4* records = static_cast<float4*>(d_workspace);
+  // without clipping only the overflow word is exported (no owners)
+  return launch_norm_finish(plan, clip ? rank_lo : 0, clip ? rank_hi : 0, records, 0,
+                            plan->info.n_tiles, clip ? records + plan->info.n_tiles : nullptr, 1,
+                            hp->max_grad_norm, d_scaler, d_exchange, st);
+}
+
+ZERO_API int zero_grad_norm_apply(const zero_plan* plan, const zero_exchange* d_exchange,
+                                  const zero_hparams* hp, zero_scaler* d_scaler, void* stream) {
+  if (!plan || !hp || !d_scaler || !d_exchange) return ZERO_EINVAL;
+  if (!zero_detail::aligned16(d_scaler) || !zero_detail::aligned16(d_exchange))
+    return ZERO_EALIGN;
+  const int clip = hp->max_grad_norm > 0.0 ? 1 : 0;
+  return launch_pdl(norm_import_kernel, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream),
+                    d_exchange, plan->info.n_ranks, clip, hp->max_grad_norm, d_scaler) ==
+                 cudaSuccess
+             ? ZERO_OK
+             : ZERO_ECUDA;
 }
 
 namespace {
@@ -2197,9 +2286,11 @@ ZERO_API int zero_step_finish(const zero_plan* plan, int32_t rank_lo, int32_t ra
 ZERO_API int zero_selftest_wait_timeout(zero_scaler* d_scaler, int64_t limit_ns, void* stream) {
   if (!d_scaler || limit_ns < 1000 || limit_ns > 10000000000ll) return ZERO_EINVAL;
   if (!zero_detail::aligned16(d_scaler)) return ZERO_EALIGN;
-  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-      d_scaler, static_cast<uint64_t>(limit_ns));
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  return launch_plain(wait_timeout_probe_kernel, dim3(1), dim3(32), 0,
+                      static_cast<cudaStream_t>(stream), d_scaler,
+                      static_cast<uint64_t>(limit_ns)) == cudaSuccess
+             ? ZERO_OK
+             : ZERO_ECUDA;
 }
 
 #ifdef ZERO_CHECKED
@@ -2226,8 +2317,10 @@ ZERO_API int zero_checked_status(int64_t* violations, int64_t* first, void* stre
 
 ZERO_API int zero_selftest_check(void* stream) {
 #ifdef ZERO_CHECKED
-  zk::check_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>();
-  return cudaGetLastError() == cudaSuccess ? ZERO_OK : ZERO_ECUDA;
+  return launch_plain(zk::check_selftest_kernel, dim3(1), dim3(1), 0,
+                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ZERO_OK
+             : ZERO_ECUDA;
 #else
   (void)stream;
   return ZERO_ESTATE;
@@ -2414,7 +2507,6 @@ extern "C" ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, 
                    cudaSuccess
                ? ZERO_OK
                : ZERO_ECUDA;
-    if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
   }
   delete a;
   return rc;
@@ -2429,18 +2521,22 @@ extern "C" ZERO_API int zero_accumulate(const zero_plan* plan, int32_t rank_lo, 
 namespace zk {
 
 constexpr int64_t kNoallocTiles = ZERO_NOALLOC_MAX_TILES;
+constexpr int64_t kNoallocBlocks = static_cast<int64_t>(ZERO_MAX_RANKS) * kOwnerBlocks;
 
-// One 16-byte norm record per tile plus the finish kernels' per-block
-// records, 8 MiB + 4 KiB. Every GPU that loads this library holds this array
-// until the process exits. All calls share it, and each call overwrites the
-// records of exactly the tiles and blocks it later reads, so nothing has to
-// be cleared between calls. Calls that overlap on the GPU (different streams,
-// or different host threads without ordering) race on it.
-static __device__ __align__(256) float4 g_noalloc_partials[kNoallocTiles + kFinishBlocks];
+// One 16-byte norm record per tile, then the finish kernels' share records
+// (kOwnerBlocks per owner), 8 MiB + 16 KiB. Every GPU that loads this
+// library holds this array until the process exits. All calls share it, and
+// each call overwrites the records of exactly the tiles and shares it later
+// reads, so nothing has to be cleared between calls. Calls that overlap on
+// the GPU (different streams, or different host threads without ordering)
+// race on it.
+static __device__ __align__(256) float4 g_noalloc_partials[kNoallocTiles + kNoallocBlocks];
 
 // Device address of g_noalloc_partials per device ordinal, resolved once per
 // device with that device current. In host code the array's name only stands
-// for the symbol; it is never a device address.
+// for the symbol; it is never a device address. The address belongs to the
+// device's context at the time of the first call: a process that destroys
+// that context (cudaDeviceReset) must not call the entry point afterwards.
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 float4* g_noalloc_ptr[kNoallocMaxDevices] = {};
@@ -2472,8 +2568,8 @@ extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t ra
                            0, 1);
   if (rc) return rc;
   const int32_t s0 = plan->rank_seg0[rank_lo], s1 = plan->rank_seg0[rank_hi];
-  const int64_t t0 = s0 < s1 ? plan->seg_tile0[s0] : 0;
-  const int64_t t1 = s0 < s1 ? plan->seg_tile0[s1 - 1] + plan->seg_tiles[s1 - 1] : 0;
+  const int64_t t0 = owner_tile0(plan, rank_lo);
+  const int64_t t1 = owner_tile0(plan, rank_hi);
   if (t1 - t0 > kNoallocTiles) return ZERO_ERANGE;
   float4* scratch = nullptr;
   if ((rc = noalloc_scratch(&scratch))) return rc;
@@ -2484,9 +2580,10 @@ extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t ra
   a->scaler = d_scaler;
   a->partials = scratch;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int grid_cap = grid_size<kNorm, true>();
+  const int grid_cap = grid_size<kNorm, true>();
   if (grid_cap <= 0) rc = ZERO_ECUDA;
-  // tiles are numbered from t0 so that the partials start at the array's base
+  // tiles are numbered from t0 so that the records start at the array's
+  // base; segments go kMaxSegs to a launch
   for (int32_t b0 = s0; !rc && b0 < s1; b0 += kMaxSegs) {
     const int32_t b1 = std::min(s1, b0 + kMaxSegs);
     int64_t tiles = 0;
@@ -2502,16 +2599,21 @@ extern "C" ZERO_API int zero_grad_norm_noalloc(const zero_plan* plan, int32_t ra
     }
     a->n_segs = b1 - b0;
     a->n_tiles = tiles;
+    // extents for the checked build: window indices of this launch (the
+    // window is the whole flat buffer) and the records the array holds
+    a->wend = plan->segs[b1 - 1].hi;
+    a->n_records = kNoallocTiles;
+    if (tiles == 0) continue;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, grid_cap));
     // the kNorm body only reads fp32 gradients, so one instantiation serves
     // both 16-bit formats
     if (launch_pdl(step_kernel<kNorm, true>, dim3(grid), dim3(kThreads), 0, st, *a) !=
         cudaSuccess)
       rc = ZERO_ECUDA;
-    if (cudaGetLastError() != cudaSuccess) rc = ZERO_ECUDA;
   }
   delete a;
   if (rc) return rc;
-  return launch_norm_finish(scratch, 0, t1 - t0, scratch + kNoallocTiles, hp->max_grad_norm,
-                            d_scaler, st);
+  return launch_norm_finish(plan, rank_lo, rank_hi, scratch, t0, kNoallocTiles,
+                            scratch + kNoallocTiles, 0, hp->max_grad_norm, d_scaler, nullptr,
+                            st);
 }

@@ -13,17 +13,20 @@ Layout in HBM for a workload with N ranks processing owners [lo, hi):
   ghat       fp32 [n_own, srow]   reduced gradients (two-pass path only)
   scaler     80 bytes             zero_scaler
   flags      uint32 [n_buckets]   per-bucket non-finite flags
-  workspace  zero_workspace_bytes (norm tile partials, clip path only)
+  workspace  zero_workspace_bytes (norm tile records, clip path only)
+  exchange   1040 bytes           zero_exchange (owners split over processes)
 """
 import ctypes as C
 
 import torch
 
-from . import (ZERO_BF16, ZERO_FP16, ZeroHParams, ZeroScaler, zero_accumulate, zero_cast_params,
-               zero_gather_units, zero_grad_norm, zero_plan_create, zero_plan_destroy,
-               zero_plan_get_info, zero_reduce_scatter_accum, zero_scaler_init, zero_shard_units,
-               zero_step, zero_step_accum, zero_unit_plan_create, zero_unit_plan_destroy,
-               zero_unit_plan_get_info, zero_unit_plan_units, zero_workspace_bytes)
+from . import (ZERO_BF16, ZERO_FP16, ZeroExchange, ZeroHParams, ZeroScaler, zero_accumulate,
+               zero_cast_params, zero_gather_units, zero_grad_norm, zero_grad_norm_apply,
+               zero_grad_norm_local, zero_plan_create, zero_plan_destroy, zero_plan_get_info,
+               zero_reduce_scatter_accum, zero_scaler_init, zero_shard_units, zero_step,
+               zero_step_accum, zero_step_finish, zero_step_update_accum, zero_unit_plan_create,
+               zero_unit_plan_destroy, zero_unit_plan_get_info, zero_unit_plan_units,
+               zero_workspace_bytes)
 from . import synth
 
 
@@ -72,8 +75,9 @@ class Group:
                       if wl.n_micro > 1 else None)
         self.scaler = torch.zeros(C.sizeof(ZeroScaler), dtype=torch.uint8, device=dev)
         self.flags = torch.zeros(max(self.info.n_buckets, 1), dtype=torch.int32, device=dev)
-        ws = zero_workspace_bytes(self.plan)
+        ws = zero_workspace_bytes(self.plan, 1)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.exchange = torch.zeros(C.sizeof(ZeroExchange), dtype=torch.uint8, device=dev)
 
     def close(self):
         if self.plan:
@@ -178,9 +182,13 @@ class Group:
         self.gen_grads(step, micro=self.n_micro)
         self.step(per_bucket=per_bucket)
 
-    def step(self, per_bucket=False, replicas=None, clear_flags=True):
+    def step(self, per_bucket=False, replicas=None, clear_flags=True, exchange=None):
         """One optimizer step through the C ABI (fused or two-pass), with the
-        accumulators of the earlier micro-batches when n_micro > 1."""
+        accumulators of the earlier micro-batches when n_micro > 1.
+        exchange: None for a group that holds all its owners' decisions, or a
+        callable that sums this process's zero_exchange blob (a uint8 device
+        tensor) with the other processes' (see dist.sum_exchange), for owners
+        split over processes."""
         st = self.sptr
         if clear_flags:
             with torch.cuda.stream(self.stream):
@@ -191,9 +199,19 @@ class Group:
         m, v, w = self._state_ptrs(0), self._state_ptrs(1), self._state_ptrs(2)
         sc = self.scaler.data_ptr()
         fl = self.flags.data_ptr()
+        ex = self.exchange.data_ptr()
         if not self.two_pass:
-            zero_step_accum(self.plan, self.lo, self.hi, m, v, w, self.n_sets, None, reps, acc, k,
-                            self.wbase, self.flat.data_ptr(), self.hp, sc, fl, st)
+            if exchange is None:
+                zero_step_accum(self.plan, self.lo, self.hi, m, v, w, self.n_sets, None, reps,
+                                acc, k, self.wbase, self.flat.data_ptr(), self.hp, sc, fl, st)
+                return
+            zero_step_update_accum(self.plan, self.lo, self.hi, m, v, w, self.n_sets, None, reps,
+                                   acc, k, self.wbase, self.flat.data_ptr(), self.hp, sc, fl, st)
+            zero_grad_norm_local(self.plan, self.lo, self.hi, None, self.hp, sc, 0, ex, st)
+            exchange(self.exchange)
+            zero_grad_norm_apply(self.plan, ex, self.hp, sc, st)
+            zero_step_finish(self.plan, self.lo, self.hi, m, self.n_sets, None, self.wbase,
+                             self.flat.data_ptr(), self.hp, sc, st)
             return
         clip = self.hp.max_grad_norm > 0
         ws = self.workspace.data_ptr() if clip else 0
@@ -202,7 +220,11 @@ class Group:
         for b in buckets:
             zero_reduce_scatter_accum(self.plan, b, self.lo, self.hi, reps, acc, k, self.wbase,
                                       gp, sc, fl, ws, st)
-        if clip:
+        if exchange is not None:
+            zero_grad_norm_local(self.plan, self.lo, self.hi, None, self.hp, sc, ws, ex, st)
+            exchange(self.exchange)
+            zero_grad_norm_apply(self.plan, ex, self.hp, sc, st)
+        elif clip:
             zero_grad_norm(self.plan, self.lo, self.hi, None, self.hp, sc, ws, st)
         zero_step(self.plan, self.lo, self.hi, m, v, w, self.n_sets, gp, None, self.wbase,
                   self.flat.data_ptr(), self.hp, sc, fl, st)

@@ -111,6 +111,13 @@ typedef struct zero_segment {
   int32_t bucket;
 } zero_segment;
 
+/* Bucket k: flat range [lo, hi) and its segments
+ * [seg_first, seg_first + seg_count) of the plan's segment list. */
+typedef struct zero_bucket {
+  int64_t lo, hi;
+  int32_t seg_first, seg_count;
+} zero_bucket;
+
 typedef struct zero_plan_info {
   int64_t psi;            /* parameters: sum of the tensor sizes */
   int64_t pad;            /* zeros appended: (N - psi mod N) mod N */
@@ -155,7 +162,10 @@ typedef struct zero_plan_info {
 ZERO_API int zero_plan_create(const int64_t* numels, int32_t n_tensors, int32_t n_ranks,
                               int64_t bucket_elems, zero_dtype grad_dtype, zero_plan** out);
 ZERO_API void zero_plan_destroy(zero_plan* plan);
+/* Copy the plan's sizes, bills and wire figures to *out (host memory).
+ * zero_plan_info_get is the same call under a second name. */
 ZERO_API int zero_plan_get_info(const zero_plan* plan, zero_plan_info* out);
+ZERO_API int zero_plan_info_get(const zero_plan* plan, zero_plan_info* out);
 /* out[k] = flat offset of tensor k (n_tensors entries). */
 ZERO_API int zero_plan_tensor_offsets(const zero_plan* plan, int64_t* out);
 /* Copies min(cap, n_segments) segments; ZERO_ERANGE if cap < n_segments. */
@@ -163,9 +173,17 @@ ZERO_API int zero_plan_segments(const zero_plan* plan, zero_segment* out, int32_
 /* [lo, hi) of bucket k. */
 ZERO_API int zero_plan_bucket_range(const zero_plan* plan, int32_t bucket, int64_t* lo,
                                     int64_t* hi);
-/* Device workspace bytes zero_reduce_scatter / zero_grad_norm need for the
- * norm partial sums: one 16-byte record per tile plus 256 records. */
-ZERO_API size_t zero_workspace_bytes(const zero_plan* plan);
+/* All buckets and segments at once ("How far does splitting the batch get
+ * you?", "How does the collective hide behind the backward pass?": the
+ * gradients are reduced bucket by bucket). out: n_buckets entries, segs:
+ * n_segments entries (host memory); either may be NULL. */
+ZERO_API int zero_plan_buckets(const zero_plan* plan, zero_bucket* out, zero_segment* segs);
+/* Device workspace bytes of a step. two_pass != 0 (a clipped step): the norm
+ * records zero_reduce_scatter, zero_grad_norm and zero_grad_norm_local use,
+ * one 16-byte record per tile plus ZERO_NORM_OWNER_BLOCKS per rank.
+ * two_pass == 0: 0, the fused step uses no workspace. 0 for a NULL plan. */
+#define ZERO_NORM_OWNER_BLOCKS 16
+ZERO_API size_t zero_workspace_bytes(const zero_plan* plan, int32_t two_pass);
 
 /* ---------------------------------------------------- hyperparameters -- */
 
@@ -237,7 +255,13 @@ ZERO_API int zero_scaler_init(const zero_hparams* hp, zero_scaler* out);
  *                 a non-finite reduced gradient. The caller clears them.
  */
 
-/* Reduce-scatter (two-pass path, step 1): for the owners [rank_lo, rank_hi)
+/* Reduce-scatter (two-pass path, step 1) ("How far does splitting the batch
+ * get you?", "Why does the all-reduce not get more expensive with more
+ * ranks?": chunk i is summed hop by hop around the ring and is complete at
+ * rank i; "What does gradient accumulation actually buy?": the reduction is
+ * fp32; "Training models too big for one GPU: ZeRO & FSDP", "Mixed-precision
+ * training": divide by the loss scale, skip the step on overflow, and "Data
+ * parallelism and the all-reduce": average over the replicas): for the owners [rank_lo, rank_hi)
  * and bucket `bucket` (-1 = all buckets), write the unscaled, unclipped
  * reduced gradient to grad_shards, OR non-finite flags into d_bucket_flags
  * and d_scaler->pending, and, when d_workspace is not NULL, store the
@@ -250,13 +274,16 @@ ZERO_API int zero_reduce_scatter(const zero_plan* plan, int32_t bucket, int32_t 
                                  void* d_workspace, void* stream);
 
 /* Global gradient norm and clip coefficient (two-pass path, step 2).
- * Convention (the pages give none): L2 norm of the unscaled, averaged
- * gradient over the processed owners' elements; squares accumulated in fp32
- * float-float pairs (exact products, two-sum additions; relative error well
- * below 2^-30) in a fixed order (per tile, then a fixed partition of the
- * tiles), so the result is deterministic and independent of the grid;
+ * The pages give no clipping rule; the convention is the common one: L2 norm
+ * of the unscaled, averaged gradient over the processed owners' elements;
  * c = max_norm / (norm + 1e-6) in fp64, applied (rounded to fp32) by the next
- * zero_step only if c < 1.
+ * zero_step only if c < 1. Squares are accumulated in fp32 float-float pairs
+ * (exact products, two-sum additions) in a fixed order that depends only on
+ * the plan: per tile; per owner over a fixed partition of its tiles; the
+ * owners' records in ascending owner order; fp64 for the final value. So the
+ * result does not depend on the grid, and a window of owners gives the same
+ * owner records as any other call that covers those owners (see
+ * zero_grad_norm_local).
  * grad_shards == NULL: use the partials zero_reduce_scatter left in
  * d_workspace (it must have covered all segments of [rank_lo, rank_hi) in
  * this step). Otherwise recompute the partials from grad_shards (4 bytes
@@ -266,8 +293,72 @@ ZERO_API int zero_grad_norm(const zero_plan* plan, int32_t rank_lo, int32_t rank
                             const float* const* grad_shards, const zero_hparams* hp,
                             zero_scaler* d_scaler, void* d_workspace, void* stream);
 
+/* ------------------------------------------- scalars across processes --
+ * "Training models too big for one GPU: ZeRO & FSDP", "ZeRO stages 1, 2 and
+ * 3": each rank updates only its own slice, so when the owners are split
+ * over processes (each holding the N replicas of its owners' slices) only
+ * the step's global scalars have to cross: whether any owner saw a
+ * non-finite gradient (the step is skipped everywhere), and, when clipping,
+ * the sum of squares behind the global norm.
+ *
+ * Protocol, per step, for processes whose windows [rank_lo, rank_hi)
+ * partition [0, N):
+ *   two-pass: zero_reduce_scatter -> zero_grad_norm_local -> sum the
+ *     zero_exchange blobs of all processes -> zero_grad_norm_apply ->
+ *     zero_step (instead of zero_grad_norm);
+ *   fused: zero_step_update -> zero_grad_norm_local -> sum ->
+ *     zero_grad_norm_apply -> zero_step_finish.
+ * "Sum" is an element-wise integer sum of the blobs viewed as 260 int32
+ * words (any all-reduce with SUM over int32, e.g. NCCL or gloo): each owner
+ * record is non-zero in exactly one process, so the sum reproduces it
+ * bit for bit, and the overflow words add up to the number of windows that
+ * saw one. Every process then holds the same norm, clip coefficient and skip
+ * decision as one process running zero_grad_norm over all N owners, bit for
+ * bit. The per-bucket flags stay per process (OR them if needed). */
+
+/* One owner's squared-norm record: hi + lo is the float-float sum of the
+ * squares of its reduced gradients with |g| < 2^56; 2^192 (big_hi + big_lo)
+ * is the sum of the rest (non-finite if a g was). */
+typedef struct zero_norm_record {
+  float hi, lo, big_hi, big_lo;
+} zero_norm_record;
+
+/* The scalars one process contributes to a step (1040 bytes, device memory,
+ * 16-byte aligned). */
+typedef struct zero_exchange {
+  uint32_t overflow;        /* 1 if this window's step saw a non-finite value */
+  uint32_t reserved[3];     /* 0 */
+  zero_norm_record owner[ZERO_MAX_RANKS];  /* owners of the window; zeros elsewhere */
+} zero_exchange;
+
+/* Export: write *d_exchange from this process's window: overflow =
+ * (d_scaler->pending != 0) after this step's reduce (two-pass) or update
+ * (fused) pass; with clipping (hp->max_grad_norm > 0) the owner records of
+ * [rank_lo, rank_hi), from the records zero_reduce_scatter left in
+ * d_workspace (grad_shards NULL) or recomputed from grad_shards; zeros for
+ * every other owner. Without clipping d_workspace and grad_shards are not
+ * used (may be NULL). Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+ZERO_API int zero_grad_norm_local(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
+                                  const float* const* grad_shards, const zero_hparams* hp,
+                                  zero_scaler* d_scaler, void* d_workspace,
+                                  zero_exchange* d_exchange, void* stream);
+
+/* Import the summed exchange: a non-zero overflow word sets the step's
+ * overflow (d_scaler->pending); with clipping, the norm fields of d_scaler
+ * (norm_sq, norm, clip_coef, clip_apply, norm_step) from the records of all
+ * N owners merged in ascending owner order, as zero_grad_norm computes them.
+ * Errors: ZERO_EINVAL, ZERO_EALIGN, ZERO_ECUDA. */
+ZERO_API int zero_grad_norm_apply(const zero_plan* plan, const zero_exchange* d_exchange,
+                                  const zero_hparams* hp, zero_scaler* d_scaler, void* stream);
+
 /* One optimizer step for the owners [rank_lo, rank_hi); call it once per
  * step: it ends by updating the loss scale, t and the skip bookkeeping.
+ * Sources: "Training models too big for one GPU: ZeRO & FSDP", "ZeRO stages
+ * 1, 2 and 3" (rank i updates its own slice of the optimizer state, then the
+ * new weights are gathered), "Adam, and why it's expensive" (the update,
+ * with eps outside the square root of the bias-corrected second moment;
+ * AdamW's decoupled weight decay), "Mixed-precision training" (fp32 master
+ * rounded to the 16-bit working copy; skip on overflow; dynamic loss scale).
  *
  * Fused path (grad_shards == NULL, needs n_sets == 2, no clip): one pass
  * reads the N replicas and the current state set (d_scaler->state_index),
@@ -397,11 +488,12 @@ ZERO_API int zero_selftest_check(void* stream);
  * 128), empty launches skipped): fused zero_step L + L (update; overflow
  * re-cast check merged with the bookkeeping in the last), two-pass zero_step
  * L + 1, zero_reduce_scatter L, zero_grad_norm 2 (+ L when it recomputes the
- * partials), zero_cast_params L. */
+ * records), zero_grad_norm_local 2 with clipping (+ L when it recomputes),
+ * 1 without, zero_grad_norm_apply 1, zero_cast_params L. */
 
 /* Maximum number of norm tiles (ZERO_TILE_ELEMS elements each, counted per
  * segment) that one zero_grad_norm_noalloc call may cover: 2^19 tiles, about
- * 2.1e9 elements, 8 MiB of device memory. */
+ * 2.1e9 elements; the array is 8 MiB + 16 KiB of device memory. */
 #define ZERO_NOALLOC_MAX_TILES (1 << 19)
 
 /* zero_grad_norm_noalloc -- the global norm and clip coefficient of
@@ -411,16 +503,19 @@ ZERO_API int zero_selftest_check(void* stream);
  * allocator owns all of the GPU's memory, plugins and embedded runtimes that
  * are not allowed to call cudaMalloc themselves, and callers with a fixed
  * memory budget that cannot grow by a workspace sized from the model.
- * It allocates nothing: the per-tile partials live in one fixed device
- * array of ZERO_NOALLOC_MAX_TILES 16-byte records (8 MiB) inside the library,
- * which every GPU that loads the library holds until the process exits.
+ * It allocates nothing: the per-tile records live in one fixed device
+ * array of ZERO_NOALLOC_MAX_TILES + 64 * ZERO_NORM_OWNER_BLOCKS 16-byte
+ * records inside the library, which every GPU that loads the library holds
+ * until the process exits.
  *   grad_shards: as for zero_grad_norm, required (not NULL).
  *   Result: norm_sq, norm, clip_coef, clip_apply and norm_step in d_scaler,
  *   equal to what zero_grad_norm computes from the same gradients.
  * The first call on each device resolves the array's device address with
- * that device current; make that first call before any stream capture.
+ * that device current; make that first call before any stream capture. The
+ * address is kept for the life of the process: after cudaDeviceReset (or any
+ * other destruction of the device's context) do not call it again.
  * All calls share the array and it keeps the last call's contents (each call
- * rewrites every partial it reads). Calls that overlap on the GPU race on
+ * rewrites every record it reads). Calls that overlap on the GPU race on
  * it: order them on one stream.
  * Errors: ZERO_EINVAL (NULL arguments, bad ranks, max_grad_norm <= 0),
  * ZERO_EALIGN, ZERO_ERANGE (the owners' slices need more than

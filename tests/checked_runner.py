@@ -72,6 +72,32 @@ def gather_case():
     g.close()
 
 
+def norm_entries_case():
+    """The norm entry points on many segments: the workspace form, the
+    no-allocation form (records in the library's fixed array, numbered from
+    the call's first tile, several launches) over all owners and then over a
+    window, and the export / import pair; the forms must agree bit for bit."""
+    import torch
+    from fsdp_sharded_mixed_shard_gb300 import harness
+    numels = [97 + (k * 37) % 500 for k in range(400)]
+    wl = W.Workload("noalloc_chk", numels, 8, 101, True, 33, 1e-2, max_grad_norm=0.1, steps=1)
+    g = harness.Group(wl)
+    g.init_state()
+    g.gen_grads(1)
+    sc, ws, st = g.scaler.data_ptr(), g.workspace.data_ptr(), g.sptr
+    Z.zero_reduce_scatter(g.plan, -1, 0, 8, g.rep_ptrs(), 0, g.ghat_ptrs(), sc, 0, ws, st)
+    ex = g.exchange.data_ptr()
+    Z.zero_grad_norm_local(g.plan, 0, 8, None, g.hp, sc, ws, ex, st)
+    Z.zero_grad_norm_apply(g.plan, ex, g.hp, sc, st)
+    for lo, hi in ((0, 8), (3, 8)):
+        Z.zero_grad_norm(g.plan, lo, hi, g.ghat_ptrs(), g.hp, sc, ws, st)
+        want = g.read_scaler().norm_sq
+        Z.zero_grad_norm_noalloc(g.plan, lo, hi, g.ghat_ptrs(), g.hp, sc, st)
+        assert g.read_scaler().norm_sq == want, (lo, hi)
+    torch.cuda.synchronize()
+    g.close()
+
+
 def main():
     Z.zero_selftest_check()
     n, first = Z.zero_checked_status()
@@ -89,6 +115,9 @@ def main():
     gather_case()
     n, first = Z.zero_checked_status()
     print(json.dumps({"case": "unit_gather", "violations": n, "first": first}), flush=True)
+    norm_entries_case()
+    n, first = Z.zero_checked_status()
+    print(json.dumps({"case": "norm_entries", "violations": n, "first": first}), flush=True)
     print(json.dumps({"case": "library", "path": Z._build.ZERO_CHECKED_LIB,
                       "loaded": Z.lib()._name}), flush=True)
 

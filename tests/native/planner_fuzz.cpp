@@ -60,7 +60,25 @@ static int flat_case() {
   int64_t lo = 0, hi = 0;
   CHECK(zero_plan_bucket_range(p, info.n_buckets, &lo, &hi) != ZERO_OK);
   if (info.n_segments > 0) CHECK(zero_plan_segments(p, segs.data(), info.n_segments - 1) != ZERO_OK);
-  CHECK(zero_workspace_bytes(p) >= static_cast<size_t>(info.n_tiles) * 16);
+  CHECK(zero_workspace_bytes(p, 1) >=
+        static_cast<size_t>(info.n_tiles + static_cast<int64_t>(n) * ZERO_NORM_OWNER_BLOCKS) * 16);
+  CHECK(zero_workspace_bytes(p, 0) == 0);
+  // all buckets and segments at once: each bucket's segments are one run
+  // that tiles its range
+  std::vector<zero_bucket> bk(info.n_buckets > 0 ? info.n_buckets : 1);
+  std::vector<zero_segment> segs2(info.n_segments > 0 ? info.n_segments : 1);
+  CHECK(zero_plan_buckets(p, bk.data(), segs2.data()) == ZERO_OK);
+  CHECK(zero_plan_buckets(p, nullptr, nullptr) == ZERO_OK);
+  for (int32_t k = 0; k < info.n_buckets; ++k) {
+    int64_t covered = 0;
+    for (int32_t s = bk[k].seg_first; s < bk[k].seg_first + bk[k].seg_count; ++s) {
+      CHECK(s >= 0 && s < info.n_segments && segs2[s].bucket == k);
+      covered += segs2[s].hi - segs2[s].lo;
+    }
+    CHECK(covered == bk[k].hi - bk[k].lo);
+  }
+  zero_plan_info alias;
+  CHECK(zero_plan_info_get(p, &alias) == ZERO_OK && alias.psi == info.psi);
   zero_plan_destroy(p);
   return 0;
 }

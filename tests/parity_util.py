@@ -59,23 +59,34 @@ def assert_state(got, want, what):
     assert e <= MASTER_REL, "%s max rel err %.3g" % (what, e)
 
 
-def norm_tol(n_elems):
-    # relative tolerance on norm^2: the checker's fp64 sum is within
-    # (n-1) * 2^-53 of the exact sum; the device accumulates exact fp32
-    # products in float-float pairs along summation paths of a few thousand
-    # additions (within 2^-30 of the exact sum, worst case); plus the fp32
-    # subnormal floor handled by the caller's absolute term
-    return 2.0 * n_elems * 2.0 ** -53 + 2.0 ** -30
+def norm_tol(n_elems, n_tiles, n_ranks):
+    """Relative tolerance on norm^2 between the device and the checker, the
+    sum of two bounds (every square is exact on both sides, all terms are
+    non-negative, so every partial sum is at most the total):
+      checker: fp64 recursive sums, in chunks of 2^20 elements, chunk sums
+        added in order: at most (min(n, 2^20) + ceil(n / 2^20)) * 2^-53;
+      device: fp32 float-float (hi, lo) additions and merges, the total kept
+        as hi + lo in fp64; along a chain of k of them lo holds at most
+        k * 2^-23 of the partial sum and each rounding of lo errs by 2^-24 of
+        that, so a chain of at most L additions errs by at most L^2 * 2^-47.
+        L = 16 (a thread's elements of one tile) + 21 (the tile record: 16
+        per lane, 5 shuffle levels) + ceil(T / 4096) (a finish thread's
+        share of one owner's at most T tiles) + 8 (the CTA tree) + 4 (the 16
+        shares of an owner) + N (owner records merged in order).
+    """
+    oracle = (min(n_elems, 1 << 20) + -(-n_elems // (1 << 20))) * 2.0 ** -53
+    chain = 16 + 21 + -(-n_tiles // 4096) + 8 + 4 + n_ranks
+    return oracle + chain * chain * 2.0 ** -47
 
 
-def compare_scaler(dev, orc, n_elems, clip):
+def compare_scaler(dev, orc, n_elems, clip, n_tiles, n_ranks):
     assert dev.t == orc.t, (dev.t, orc.t)
     assert dev.scale == orc.scale, (dev.scale, orc.scale)
     assert dev.overflow == orc.overflow
     assert dev.good_steps == orc.good_steps
     assert dev.error == 0
     if clip and not orc.overflow:
-        assert abs(dev.norm_sq - orc.norm_sq) <= norm_tol(n_elems) * orc.norm_sq
+        assert abs(dev.norm_sq - orc.norm_sq) <= norm_tol(n_elems, n_tiles, n_ranks) * orc.norm_sq
         if dev.clip_coef != orc.clip_coef:
             # only a norm at an fp32 rounding boundary may move c by one ulp
             assert abs(float(dev.clip_coef) - float(orc.clip_coef)) <= \
@@ -162,7 +173,7 @@ def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True):
             gm, gmm, gv = (t.numpy() for t in g.current_state())
             report(wl, step, "full", wlen, dev, sc, (gm, gmm, gv, g.params_u16()),
                    (master, m, v, params), np.array_equal(g.flags_u32(), flags[:p.n_buckets]))
-            compare_scaler(dev, sc, wlen, wl.max_grad_norm > 0)
+            compare_scaler(dev, sc, wlen, wl.max_grad_norm > 0, g.info.n_tiles, wl.n_ranks)
             assert np.array_equal(g.flags_u32(), flags[:p.n_buckets])
             assert_state(gm, master, "master")
             assert_state(gmm, m, "exp_avg")
@@ -249,7 +260,8 @@ def run_sampled(wl, steps=None, n_random=2048, n_threads=None):
             gm, gmm, gv, gp = gather_state(g, elems)
             report(wl, step, "sampled", len(elems), dev, sc, (gm, gmm, gv, gp),
                    (master, m, v, params), np.array_equal(g.flags_u32(), flags[:p.n_buckets]))
-            compare_scaler(dev, sc, (hi - lo) * p.shard, wl.max_grad_norm > 0)
+            compare_scaler(dev, sc, (hi - lo) * p.shard, wl.max_grad_norm > 0, g.info.n_tiles,
+                           wl.n_ranks)
             assert np.array_equal(g.flags_u32(), flags[:p.n_buckets])
             assert_state(gm, master, "master")
             assert_state(gmm, m, "exp_avg")

@@ -58,6 +58,9 @@ def test_struct_sizes():
     assert C.sizeof(Z.ZeroPlanInfo) == 168
     assert C.sizeof(Z.ZeroHParams) == 64
     assert C.sizeof(Z.ZeroSegment) == 24
+    assert C.sizeof(Z.ZeroBucket) == 24
+    assert C.sizeof(Z.ZeroNormRecord) == 16
+    assert C.sizeof(Z.ZeroExchange) == 16 + 16 * Z.ZERO_MAX_RANKS
 
 
 def _compare(numels, n, bsz, dtype=Z.ZERO_BF16):
@@ -81,7 +84,25 @@ def _compare(numels, n, bsz, dtype=Z.ZERO_BF16):
             assert a == pytest.approx(b, rel=1e-15, abs=0)
         assert info.step_bytes_fused == 2 * n + 26
         assert info.n_tiles == sum(-(-(hi - lo) // Z.ZERO_TILE_ELEMS) for lo, hi, _, _ in osegs)
-        assert Z.zero_workspace_bytes(p) >= info.n_tiles * 8
+        ws = Z.zero_workspace_bytes(p, 1)
+        assert ws >= 16 * (info.n_tiles + n * Z.ZERO_NORM_OWNER_BLOCKS) and ws % 256 == 0
+        assert Z.zero_workspace_bytes(p, 0) == 0
+        # the names the boundary lists: zero_plan_info_get, zero_plan_buckets
+        alias = Z.zero_plan_info_get(p)
+        assert bytes(alias) == bytes(info)
+        buckets, segs = Z.zero_plan_buckets(p)
+        assert segs == [tuple(s) for s in osegs]
+        assert len(buckets) == op.n_buckets
+        of_bucket = {}
+        for i, sg in enumerate(osegs):
+            of_bucket.setdefault(sg[3], []).append(i)
+        for k, (lo, hi, first, count) in enumerate(buckets):
+            assert (lo, hi) == Z.zero_plan_bucket_range(p, k)
+            mine = of_bucket.get(k, [])
+            assert count == len(mine) and (not mine or first == mine[0])
+            assert mine == list(range(first, first + count))
+            # the bucket's segments tile [lo, hi) (a bucket past psi_pad is empty)
+            assert sum(osegs[i][1] - osegs[i][0] for i in mine) == hi - lo
     finally:
         Z.zero_plan_destroy(p)
 
@@ -135,6 +156,27 @@ def test_host_validation_without_gpu():
     with pytest.raises(Z.ZeroError) as e:
         Z.zero_grad_norm(p, 0, 4, None, hp, 16, 16)
     assert e.value.status == -1
+    clip = Z.ZeroHParams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0, 0, 2000, 1.0)
+    # exchange export: no exchange buffer; a clipped export without a
+    # workspace; a misaligned exchange buffer
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm_local(p, 0, 2, None, hp, 16, 0, 0)
+    assert e.value.status == -1
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm_local(p, 0, 2, None, clip, 16, 0, 16)
+    assert e.value.status == -1
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm_local(p, 2, 1, None, hp, 16, 0, 16)
+    assert e.value.status == -1
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm_local(p, 0, 2, None, hp, 16, 0, 24)
+    assert e.value.status == -2
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm_apply(p, 0, clip, 16)
+    assert e.value.status == -1
+    with pytest.raises(Z.ZeroError) as e:
+        Z.zero_grad_norm_apply(p, 24, clip, 16)
+    assert e.value.status == -2
     for bad_limit in (0, 999, 10**11):
         with pytest.raises(Z.ZeroError) as e:
             Z.zero_selftest_wait_timeout(16, bad_limit)

@@ -267,11 +267,71 @@ def test_norm_chunked_sum_within_fp64_bound():
     assert abs(sc.norm_sq - exact) <= psi * 2.0 ** -53 * exact
 
 
-def test_clip_coef_rule():
-    apply, c, nrm = oracle.clip_coef(4.0, 1.0)
-    assert apply and nrm == 2.0 and c == F32(1.0 / (2.0 + 1e-6))
-    apply, c, _ = oracle.clip_coef(0.25, 1.0)
-    assert not apply and c == 1.0
+def _torch_clip(grads, max_norm):
+    """torch.nn.utils.clip_grad_norm_ on fp64 CPU tensors: an outside
+    implementation of the same convention (total L2 norm over all tensors,
+    coefficient max_norm / (norm + 1e-6), clamped at 1). Returns (norm, the
+    multiplier it applied, the clipped gradients)."""
+    import torch
+    ps = []
+    for g in grads:
+        t = torch.zeros(len(g), dtype=torch.float64, requires_grad=True)
+        t.grad = torch.tensor(g, dtype=torch.float64)
+        ps.append(t)
+    before = [p.grad.clone() for p in ps]
+    total = float(torch.nn.utils.clip_grad_norm_(ps, max_norm, norm_type=2.0))
+    after = [p.grad.numpy().copy() for p in ps]
+    k = int(np.argmax(np.abs(before[0].numpy())))
+    mult = float(after[0][k] / before[0][k].item())
+    return total, mult, after
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_clip_coef_matches_torch_clip_grad_norm(case):
+    """orc_clip_coef against torch's clip_grad_norm_ on fp64 gradients,
+    norms on both sides of max_norm: the same apply decision, the same
+    norm (to fp64 rounding) and, when it clips, the same coefficient after
+    rounding to fp32 (one ulp when torch's norm and the checker's sit on
+    either side of an fp32 rounding boundary). A misplaced eps
+    (max/norm + eps) moves c by ~eps/c, i.e. many fp32 ulps at these norms."""
+    rng = np.random.default_rng(1000 + case)
+    sizes = [int(x) for x in rng.integers(1, 5000, size=int(rng.integers(1, 5)))]
+    scale = float(10.0 ** rng.uniform(-4, 2))
+    grads = [rng.standard_normal(n) * scale for n in sizes]
+    max_norm = float(rng.choice([0.05, 0.5, 1.0, 3.0, 1e3]))
+    nsq = math.fsum(float(x) * float(x) for g in grads for x in g)
+    apply, c, nrm = oracle.clip_coef(nsq, max_norm)
+    total, mult, after = _torch_clip(grads, max_norm)
+    assert nrm == pytest.approx(total, rel=4e-16)
+    assert apply == (mult < 1.0)
+    if apply:
+        assert abs(float(c) - float(F32(mult))) <= 2.0 ** -23 * float(c)
+        for g, a in zip(grads, after):
+            want = np.asarray(g) * float(c)
+            assert np.allclose(a, want, rtol=2.0 ** -22, atol=0.0)
+    else:
+        assert c == 1.0 and mult == 1.0
+        for g, a in zip(grads, after):
+            assert np.array_equal(a, np.asarray(g))
+
+
+def test_clip_coef_at_and_near_the_limit():
+    """Norms just below, at and above the point where c reaches 1, against
+    torch. Within an ulp of that point the fp64 test c < 1 follows the norm's
+    last bit (torch's norm and sqrt of the checker's sum may differ there),
+    but the fp32 multiplier that reaches the gradient is 1.0 on both sides;
+    further out the decisions agree."""
+    for max_norm in (1.0, 0.25, 7.0):
+        x = max_norm - 1e-6
+        for nrm in (np.nextafter(x, 0.0), x, np.nextafter(x, 2 * x), 0.5 * max_norm,
+                    2 * max_norm):
+            g = [[float(nrm)]]
+            apply, c, got = oracle.clip_coef(float(nrm) * float(nrm), max_norm)
+            total, mult, _ = _torch_clip(g, max_norm)
+            effective = float(c) if apply else 1.0
+            assert effective == float(F32(mult)), (max_norm, nrm, c, mult)
+            if nrm in (0.5 * max_norm, 2 * max_norm):
+                assert apply == (mult < 1.0)
 
 
 # ------------------------------------------------------- skip and scaler ----

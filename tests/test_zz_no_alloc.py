@@ -1,17 +1,19 @@
 """zero_grad_norm_noalloc: the global-norm call for callers that cannot
 allocate device memory (a host framework's allocator owns the GPU's memory,
 or a fixed budget leaves no room for a model-sized workspace). It keeps its
-tile partials in a fixed array inside the library instead of a caller
+tile records in a fixed array inside the library instead of a caller
 workspace; these tests check, through the C ABI, that it gives what the
-workspace form gives, on two calls in a row, and that it refuses sizes
-beyond its array. Collected last on purpose (file name), so a run that stops
-at the first failure has run every other test before it."""
+workspace form (zero_grad_norm recomputing from the same gradients) gives,
+bit for bit, on calls in a row, and that it refuses sizes beyond its array.
+Before every call the scaler's norm fields are overwritten with values no
+norm call produces, so a call that launched or wrote nothing fails.
+Collected last on purpose (file name), so a run that stops at the first
+failure has run every other test before it."""
 import pytest
 import torch
 
 import fsdp_sharded_mixed_shard_gb300 as Z
 from fsdp_sharded_mixed_shard_gb300 import harness, workloads as W
-from parity_util import norm_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -22,25 +24,47 @@ def _need_gpu():
         pytest.skip("needs a CUDA GPU")
 
 
+def _poison(g):
+    s = g.read_scaler()
+    s.norm_sq, s.norm, s.clip_coef, s.clip_apply, s.norm_step = -1.0, -1.0, -1.0, -7, -7
+    g.scaler.copy_(torch.frombuffer(bytearray(bytes(s)), dtype=torch.uint8).to(g.device))
+    torch.cuda.synchronize()
+
+
+def _both(g, lo, hi):
+    """(workspace form, no-allocation form) of the norm of the owners
+    [lo, hi) from the reduced gradients in g.ghat."""
+    sc, ws, st = g.scaler.data_ptr(), g.workspace.data_ptr(), g.sptr
+    _poison(g)
+    Z.zero_grad_norm(g.plan, lo, hi, g.ghat_ptrs(), g.hp, sc, ws, st)
+    want = g.read_scaler()
+    _poison(g)
+    Z.zero_grad_norm_noalloc(g.plan, lo, hi, g.ghat_ptrs(), g.hp, sc, st)
+    got = g.read_scaler()
+    return want, got
+
+
+def _assert_same(want, got):
+    assert want.norm_step > 0 and want.norm_sq > 0
+    assert (got.norm_sq, got.norm, got.clip_coef, got.clip_apply, got.norm_step) == \
+        (want.norm_sq, want.norm, want.clip_coef, want.clip_apply, want.norm_step)
+    assert got.error == 0
+
+
 def test_noalloc_norm_matches_workspace_norm_two_calls():
     wl = W.Workload("noalloc", [300_007, 4096, 13], 4, 50_000, True, 31, 1e-2,
                     max_grad_norm=0.5, steps=2)
     g = harness.Group(wl)
     try:
         g.init_state()
-        sc, ws, st = g.scaler.data_ptr(), g.workspace.data_ptr(), g.sptr
-        n_elems = g.info.psi_pad
+        sc, st = g.scaler.data_ptr(), g.sptr
         for step in (1, 2):   # two calls in a row, on different gradients
             g.gen_grads(step)
             Z.zero_reduce_scatter(g.plan, -1, 0, 4, g.rep_ptrs(), 0, g.ghat_ptrs(), sc, 0, 0, st)
-            Z.zero_grad_norm(g.plan, 0, 4, g.ghat_ptrs(), g.hp, sc, ws, st)
-            want = g.read_scaler()
-            Z.zero_grad_norm_noalloc(g.plan, 0, 4, g.ghat_ptrs(), g.hp, sc, st)
-            got = g.read_scaler()
-            assert abs(got.norm_sq - want.norm_sq) <= norm_tol(n_elems) * want.norm_sq
-            assert got.clip_coef == want.clip_coef and got.clip_apply == want.clip_apply
-            assert got.norm_step == want.norm_step and got.error == 0
-            # the clipped update that follows works from either result
+            want, got = _both(g, 0, 4)
+            _assert_same(want, got)
+            assert got.clip_apply == 1
+            # the clipped update that follows works from the no-allocation result
             Z.zero_step(g.plan, 0, 4, g._state_ptrs(0), g._state_ptrs(1), g._state_ptrs(2), 1,
                         g.ghat_ptrs(), None, 0, g.flat.data_ptr(), g.hp, sc, 0, st)
             assert g.read_scaler().t == step
@@ -55,15 +79,33 @@ def test_noalloc_rank_subset():
     try:
         g.init_state()
         g.gen_grads(1)
-        sc, ws, st = g.scaler.data_ptr(), g.workspace.data_ptr(), g.sptr
+        sc, st = g.scaler.data_ptr(), g.sptr
         Z.zero_reduce_scatter(g.plan, -1, 5, 7, g.rep_ptrs(), g.wbase, g.ghat_ptrs(), sc, 0, 0,
                               st)
-        Z.zero_grad_norm(g.plan, 5, 7, g.ghat_ptrs(), g.hp, sc, ws, st)
-        want = g.read_scaler()
-        Z.zero_grad_norm_noalloc(g.plan, 5, 7, g.ghat_ptrs(), g.hp, sc, st)
-        got = g.read_scaler()
-        assert abs(got.norm_sq - want.norm_sq) <= norm_tol(g.wlen) * want.norm_sq
-        assert got.clip_coef == want.clip_coef
+        want, got = _both(g, 5, 7)
+        _assert_same(want, got)
+    finally:
+        g.close()
+
+
+def test_noalloc_many_segments_then_a_smaller_call():
+    """More segments than one launch takes (several launches, each numbering
+    its records from the call's first tile), then a smaller call over fewer
+    owners: the second call reads only records it rewrote."""
+    numels = [97 + (k * 37) % 500 for k in range(400)]
+    wl = W.Workload("noalloc_segs", numels, 8, 101, True, 33, 1e-2, max_grad_norm=0.1, steps=1)
+    g = harness.Group(wl)
+    try:
+        assert g.info.n_segments > 3 * 128
+        g.init_state()
+        g.gen_grads(1)
+        sc, st = g.scaler.data_ptr(), g.sptr
+        Z.zero_reduce_scatter(g.plan, -1, 0, 8, g.rep_ptrs(), 0, g.ghat_ptrs(), sc, 0, 0, st)
+        big_want, big_got = _both(g, 0, 8)
+        _assert_same(big_want, big_got)
+        small_want, small_got = _both(g, 6, 8)
+        _assert_same(small_want, small_got)
+        assert small_got.norm_sq < big_got.norm_sq
     finally:
         g.close()
 
