@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--impl", default="libzero", choices=["libzero", "reference"])
     ap.add_argument("--workload", default="flat_1p5b",
                     choices=["tiny_flat", "gpt2_small", "flat_1p5b", "stage3_slice", "llama_2b"])
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="steps of the end-to-end leg (0: leave it out, e.g. for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--micro", type=int, default=1,
@@ -267,6 +268,7 @@ def job_throughput(psi_per_rank_step, steps, world, total_ms):
 # ------------------------------------------------------------ libzero arm ----
 
 def run_libzero(args, rank, world, dist):
+    import numpy as np
     import torch
     import fsdp_sharded_mixed_shard_gb300 as Z
     from fsdp_sharded_mixed_shard_gb300 import harness
@@ -288,19 +290,23 @@ def run_libzero(args, rank, world, dist):
     st = g.sptr
     N = wl.n_ranks
     lo, hi = wl.ranks
-    reps = g.rep_ptrs()
-    m, v, w = g._state_ptrs(0), g._state_ptrs(1), g._state_ptrs(2)
+    # per-rank pointer tables built once as uint64 arrays, which the binding
+    # passes through unchanged (lists are marshalled on every call)
+    table = lambda ptrs: None if ptrs is None else np.array(  # noqa: E731
+        [0 if q is None else q for q in ptrs], dtype=np.uint64)
+    reps = table(g.rep_ptrs())
+    m, v, w = table(g._state_ptrs(0)), table(g._state_ptrs(1)), table(g._state_ptrs(2))
     sc, fl, flat = g.scaler.data_ptr(), g.flags.data_ptr(), g.flat.data_ptr()
     ws = g.workspace.data_ptr()
     clip = wl.max_grad_norm > 0
-    gp = g.ghat_ptrs() if g.two_pass else None
+    gp = table(g.ghat_ptrs()) if g.two_pass else None
 
     # phases of one step (each a C-ABI call on stream st); for the fused path
     # the update is one kernel launch per 128 segments. With k micro-batches
     # the first k - 1 are accumulated in fp32 and the last is added inside
     # the reduce (the same replica buffer stands for every micro-batch).
     k_micro = wl.n_micro
-    acc = g.accum_ptrs() if k_micro > 1 else None
+    acc = table(g.accum_ptrs()) if k_micro > 1 else None
 
     def phases():
         pre = []
@@ -321,9 +327,10 @@ def run_libzero(args, rank, world, dist):
             out.append(("grad_norm", lambda: Z.zero_grad_norm(g.plan, lo, hi, None, g.hp, sc, ws,
                                                               st)))
         out += [("update", lambda: Z.zero_step_update(
-                    g.plan, lo, hi, m, v, w, 1, gp, None, g.wbase, flat, g.hp, sc, fl, st)),
+                    g.plan, lo, hi, m, v, w, g.n_sets, gp, None, g.wbase, flat, g.hp, sc, fl,
+                    st)),
                 ("finish", lambda: Z.zero_step_finish(
-                    g.plan, lo, hi, m, 1, gp, g.wbase, flat, g.hp, sc, st))]
+                    g.plan, lo, hi, m, g.n_sets, gp, g.wbase, flat, g.hp, sc, st))]
         return out
 
     ph = phases()
@@ -461,11 +468,42 @@ def run_libzero(args, rank, world, dist):
                                               / peak, 4),
                 "kernel_gbs": kernel_gbs}
 
-    # end to end through the C ABI: every step copies that step's replicas from
-    # pinned host memory and reads the updated parameters and the scaler back.
-    # Steps are pipelined over two replica buffers and two parameter buffers:
-    # the host->device copy of step k+1 (split over two copy streams) runs
-    # while step k computes, and step k's read-back runs on a third stream.
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, g, wl, K, world, dist, k_micro, acc, m, v, w, sc, fl, ws, clip, gp,
+                      lo, hi, N, dev, pstep)
+    sk = g.read_scaler()
+    g.close()
+
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic: seeded counter-based generator (SplitMix64 + Irwin-Hall normal), "
+                    "same replicas every timed step",
+            "config": dict(config_of(wl, path), parallelism="%d simulated ranks per GPU x %d GPUs"
+                           % (N, world)),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * K,
+            "clocks": clk, "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
+            "phase_events": "per-kernel CUDA events on %d of %d timed steps (%s)"
+                            % (len(sampled), K, "every step" if every == 1 else
+                               "steps %d, %d, ... of the timed loop" % (sampled[0], sampled[0] + every)),
+            "launch": "CUDA graph replay of one captured step (eager on event steps)"
+                      if graph is not None else "eager C-ABI calls",
+            "wall_s_timed": round(wall, 3), "scaler_t": sk.t, "device_error": sk.error}
+    return line
+
+
+def run_e2e(args, g, wl, K, world, dist, k_micro, acc, m, v, w, sc, fl, ws, clip, gp, lo, hi,
+            N, dev, pstep):
+    """End to end through the C ABI: every step copies that step's replicas
+    from pinned host memory and reads the updated parameters and the scaler
+    back. Steps are pipelined over two replica buffers and two parameter
+    buffers: the host->device copy of step k+1 (split over two copy streams)
+    runs while step k computes, and step k's read-back runs on a third
+    stream."""
+    import torch
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    st = g.sptr
     E = max(1, min(args.e2e_steps, K))
     host_reps = torch.empty(g.replicas.shape, dtype=torch.int16, pin_memory=True)
     host_reps.copy_(g.replicas)
@@ -505,7 +543,8 @@ def run_libzero(args, rank, world, dist):
                                         ws if clip else 0, st)
             if clip:
                 Z.zero_grad_norm(g.plan, lo, hi, None, g.hp, sc, ws, st)
-            Z.zero_step(g.plan, lo, hi, m, v, w, 1, gp, None, g.wbase, fp, g.hp, sc, fl, st)
+            Z.zero_step(g.plan, lo, hi, m, v, w, g.n_sets, gp, None, g.wbase, fp, g.hp, sc, fl,
+                        st)
 
     for e in computed + read_back:
         e.record(g.stream)
@@ -550,25 +589,7 @@ def run_libzero(args, rank, world, dist):
            "d2h_bytes_per_step": int(g.flat.numel() * 2 + g.scaler.numel()),
            "pipelined": "two replica and parameter buffers; H2D of step k+1 overlaps step k"}
     del dev_reps, host_reps
-    sk = g.read_scaler()
-    g.close()
-
-    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic: seeded counter-based generator (SplitMix64 + Irwin-Hall normal), "
-                    "same replicas every timed step",
-            "config": dict(config_of(wl, path), parallelism="%d simulated ranks per GPU x %d GPUs"
-                           % (N, world)),
-            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * K,
-            "clocks": clk, "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
-            "phase_events": "per-kernel CUDA events on %d of %d timed steps (%s)"
-                            % (len(sampled), K, "every step" if every == 1 else
-                               "steps %d, %d, ... of the timed loop" % (sampled[0], sampled[0] + every)),
-            "launch": "CUDA graph replay of one captured step (eager on event steps)"
-                      if graph is not None else "eager C-ABI calls",
-            "wall_s_timed": round(wall, 3), "scaler_t": sk.t, "device_error": sk.error}
-    return line
+    return e2e
 
 
 # ------------------------------------------------ stage-3 unit all-gather ----

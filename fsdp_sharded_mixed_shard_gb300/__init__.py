@@ -22,6 +22,7 @@ __all__ = [
     "zero_plan_tensor_offsets", "zero_plan_segments", "zero_plan_buckets",
     "zero_plan_bucket_range", "zero_workspace_bytes", "zero_scaler_init",
     "zero_reduce_scatter", "zero_grad_norm", "zero_grad_norm_local", "zero_grad_norm_apply",
+    "zero_ring_hop",
     "zero_step", "zero_step_update", "zero_step_finish",
     "zero_cast_params", "zero_accumulate", "zero_reduce_scatter_accum", "zero_step_accum",
     "zero_step_update_accum", "zero_grad_norm_noalloc", "zero_selftest_wait_timeout", "zero_strerror",
@@ -169,6 +170,7 @@ def lib():
         L.zero_grad_norm_local.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP),
                                            _P(ZeroHParams), _VP, _VP, _VP, _VP]
         L.zero_grad_norm_apply.argtypes = [_VP, _VP, _P(ZeroHParams), _VP, _VP]
+        L.zero_ring_hop.argtypes = [_VP, C.c_int32, C.c_int32, _VP, _VP, _VP, _VP, _VP, _VP]
         L.zero_step.argtypes = [_VP, C.c_int32, C.c_int32, _P(_VP), _P(_VP), _P(_VP), C.c_int32,
                                 _P(_VP), _P(_VP), C.c_int64, _VP, _P(ZeroHParams), _VP, _VP, _VP]
         L.zero_step_update.argtypes = L.zero_step.argtypes
@@ -352,6 +354,12 @@ def zero_grad_norm_local(plan, rank_lo, rank_hi, grad_shards, hp, d_scaler, d_wo
 def zero_grad_norm_apply(plan, d_exchange, hp, d_scaler, stream=0):
     _check("zero_grad_norm_apply", lib().zero_grad_norm_apply(
         plan, _vp(d_exchange), C.byref(hp), _vp(d_scaler), _vp(stream)))
+
+
+def zero_ring_hop(plan, rank, hop, grad, recv, out, d_scaler, d_bucket_flags=0, stream=0):
+    _check("zero_ring_hop", lib().zero_ring_hop(
+        plan, rank, hop, _vp(grad), _vp(recv), _vp(out), _vp(d_scaler), _vp(d_bucket_flags),
+        _vp(stream)))
 
 
 def zero_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, grad_shards,

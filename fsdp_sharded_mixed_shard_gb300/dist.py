@@ -63,3 +63,82 @@ def sum_exchange(blob, stream=None, group=None):
         words.copy_(host)
         return
     dist.all_reduce(words, op=dist.ReduceOp.SUM, group=group)
+
+
+# ------------------------------------------------- ring reduce-scatter ----
+#
+# "How far does splitting the batch get you?", "Why does the all-reduce not
+# get more expensive with more ranks?": with one gradient replica per
+# process, chunk i (owner i's slice) starts at rank i+1, collects every
+# rank's values hop by hop and ends, complete, at rank i after N - 1 hops.
+# libzero's zero_ring_hop does each rank's arithmetic; this driver moves the
+# fp32 partials between neighbours.
+
+def ring_schedule(rank, world):
+    """[(hop, chunk)] of one rank: at hop h (1 .. world) it works on chunk
+    (rank - h) mod world; after hops 1 .. world-1 it sends that partial to
+    rank + 1 and receives the next chunk's from rank - 1; hop `world` is its
+    own chunk."""
+    return [(h, (rank - h) % world) for h in range(1, world + 1)]
+
+
+def ring_pass(send, recv, rank, world, stream=None, group=None):
+    """Send `send` to rank + 1 and receive `recv` from rank - 1 (device or
+    host tensors of the same size). With NCCL the pair runs on `stream`;
+    otherwise (gloo) the device buffers go through host memory after
+    `stream` is synchronized."""
+    nxt, prv = (rank + 1) % world, (rank - 1) % world
+    if send.is_cuda and dist.get_backend(group) == "nccl":
+        s = stream if stream is not None else torch.cuda.current_stream(send.device)
+        with torch.cuda.stream(s):
+            reqs = dist.batch_isend_irecv([dist.P2POp(dist.isend, send, nxt, group),
+                                           dist.P2POp(dist.irecv, recv, prv, group)])
+            for r in reqs:
+                r.wait()
+        return
+    if send.is_cuda:
+        (stream or torch.cuda.current_stream(send.device)).synchronize()
+        hs, hr = send.cpu(), torch.empty(recv.shape, dtype=recv.dtype)
+    else:
+        hs, hr = send, recv
+    reqs = [dist.isend(hs, nxt, group=group), dist.irecv(hr, prv, group=group)]
+    for r in reqs:
+        r.wait()
+    if send.is_cuda:
+        recv.copy_(hr)
+
+
+def ring_reduce_scatter(plan, rank, world, grad, shard, bufs, d_scaler, d_flags=0, stream=None,
+                        group=None):
+    """The reduce-scatter of one step over `world` processes (world == the
+    plan's N): grad is this rank's 16-bit gradient (device address of flat
+    element 0), shard receives this rank's reduced gradient (a float32 device
+    tensor of S elements), bufs two float32 device tensors of S elements."""
+    from . import zero_ring_hop
+    send, recv = bufs
+    sptr = 0 if stream is None else stream.cuda_stream
+    for hop, _ in ring_schedule(rank, world)[:-1]:
+        zero_ring_hop(plan, rank, hop, grad, recv.data_ptr() if hop > 1 else 0,
+                      send.data_ptr(), d_scaler, d_flags, sptr)
+        ring_pass(send, recv, rank, world, stream, group)
+    zero_ring_hop(plan, rank, world, grad, recv.data_ptr() if world > 1 else 0,
+                  shard.data_ptr(), d_scaler, d_flags, sptr)
+
+
+def all_gather_params(flat, rank, world, shard_elems, stream=None, group=None):
+    """Every rank's slot [r*S, (r+1)*S) of the 16-bit parameter buffer `flat`
+    (a device int16 tensor of at least world*S elements) from its owner: the
+    all-gather of the updated weights ("Training models too big for one GPU:
+    ZeRO & FSDP", "ZeRO stages 1, 2 and 3")."""
+    n = world * shard_elems
+    mine = flat[rank * shard_elems:(rank + 1) * shard_elems]
+    if flat.is_cuda and dist.get_backend(group) == "nccl":
+        s = stream if stream is not None else torch.cuda.current_stream(flat.device)
+        with torch.cuda.stream(s):
+            dist.all_gather_into_tensor(flat[:n], mine.clone(), group=group)
+        return
+    if flat.is_cuda:
+        (stream or torch.cuda.current_stream(flat.device)).synchronize()
+    parts = [torch.empty(shard_elems, dtype=flat.dtype) for _ in range(world)]
+    dist.all_gather(parts, mine.cpu(), group=group)
+    flat[:n].copy_(torch.cat(parts))

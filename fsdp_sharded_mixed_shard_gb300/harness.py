@@ -9,7 +9,9 @@ Layout in HBM for a workload with N ranks processing owners [lo, hi):
                                   [lo*S, hi*S), rows padded to 16 bytes
   flat       int16 [row]          16-bit working parameters (same window)
   state      fp32 [n_sets, 3, n_own, srow]  master / exp_avg / exp_avg_sq
-                                  shard of each owned rank, rows padded to 16 B
+                                  shard of each owned rank, rows padded to 16 B;
+                                  n_sets = 2 (ping-pong) unless the two-pass
+                                  path is asked for one set
   ghat       fp32 [n_own, srow]   reduced gradients (two-pass path only)
   scaler     80 bytes             zero_scaler
   flags      uint32 [n_buckets]   per-bucket non-finite flags
@@ -42,12 +44,16 @@ def hparams_of(wl):
 class Group:
     """All device state of one simulated data-parallel group on one GPU."""
 
-    def __init__(self, wl, device="cuda", two_pass=None, stream=None, alloc_replicas=True):
+    def __init__(self, wl, device="cuda", two_pass=None, stream=None, alloc_replicas=True,
+                 n_sets=None):
         self.wl = wl
         self.device = torch.device(device)
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.two_pass = (wl.max_grad_norm > 0) if two_pass is None else two_pass
-        self.n_sets = 1 if self.two_pass else 2
+        # optimizer state sets: two by default (ping-pong: each step reads
+        # one set and writes the other); the two-pass path also takes one
+        # (updated in place, 12 bytes per element less memory)
+        self.n_sets = 2 if n_sets is None else n_sets
         self.is_bf16 = wl.is_bf16
         self.plan = zero_plan_create(wl.numels, wl.n_ranks, wl.bucket_elems,
                                      ZERO_BF16 if wl.is_bf16 else ZERO_FP16)
@@ -331,3 +337,126 @@ class UnitGroup:
         """Write buffer slots slot0, ... back into the units' slices."""
         ptrs = [self.buffer_ptr(slot0 + i) for i in range(unit_hi - unit_lo)]
         zero_shard_units(self.plan, unit_lo, unit_hi, ptrs, self.shard_ptrs(), self.sptr)
+
+
+class RingRank:
+    """Device state of one rank of a group whose N ranks are N processes
+    (one gradient replica each; "How far does splitting the batch get you?",
+    "Why does the all-reduce not get more expensive with more ranks?"):
+
+      grad     int16 [row]            this rank's 16-bit gradient, all psi_pad
+                                      elements (row rounded up to 8)
+      flat     int16 [row]            16-bit working parameters, all slots
+                                      (own slot written by the step, the
+                                      others by the all-gather)
+      state    fp32 [n_sets, 3, srow] master / exp_avg / exp_avg_sq of this
+                                      rank's slice
+      shard    fp32 [srow]            this rank's reduced gradient
+      bufs     fp32 [2, srow]         partials sent to and received from the
+                                      neighbours
+    plus the scaler, bucket flags, norm workspace and exchange blob.
+    """
+
+    def __init__(self, wl, rank, device="cuda", stream=None, n_sets=2):
+        self.wl = wl
+        self.rank = rank
+        self.device = torch.device(device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.plan = zero_plan_create(wl.numels, wl.n_ranks, wl.bucket_elems,
+                                     ZERO_BF16 if wl.is_bf16 else ZERO_FP16)
+        self.info = zero_plan_get_info(self.plan)
+        self.N, self.S = wl.n_ranks, self.info.shard_elems
+        self.n_sets = n_sets
+        self.hp = hparams_of(wl)
+        self.row = _round_up(max(self.info.psi_pad, 1), 8)
+        self.srow = _round_up(max(self.S, 1), 4)
+        dev = self.device
+        self.grad = torch.zeros(self.row, dtype=torch.int16, device=dev)
+        self.flat = torch.zeros(self.row, dtype=torch.int16, device=dev)
+        self.state = torch.zeros((n_sets, 3, self.srow), dtype=torch.float32, device=dev)
+        self.shard = torch.zeros(self.srow, dtype=torch.float32, device=dev)
+        self.bufs = torch.zeros((2, self.srow), dtype=torch.float32, device=dev)
+        self.scaler = torch.zeros(C.sizeof(ZeroScaler), dtype=torch.uint8, device=dev)
+        self.flags = torch.zeros(max(self.info.n_buckets, 1), dtype=torch.int32, device=dev)
+        ws = zero_workspace_bytes(self.plan, 1)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.exchange = torch.zeros(C.sizeof(ZeroExchange), dtype=torch.uint8, device=dev)
+
+    def close(self):
+        if self.plan:
+            zero_plan_destroy(self.plan)
+            self.plan = None
+
+    @property
+    def sptr(self):
+        return self.stream.cuda_stream
+
+    def _per_rank(self, ptr):
+        out = [None] * self.N
+        out[self.rank] = ptr
+        return out
+
+    def _state_ptrs(self, which):
+        out = [None] * (self.n_sets * self.N)
+        for s in range(self.n_sets):
+            out[s * self.N + self.rank] = self.state[s, which].data_ptr()
+        return out
+
+    def init_state(self):
+        """Master slice from the seeded generator, m = v = 0, the own slot of
+        the parameters cast from it, the others all-gathered by the caller."""
+        wl, r, S = self.wl, self.rank, self.S
+        with torch.cuda.stream(self.stream):
+            self.state.zero_()
+            synth.gpu_fill_master(self.state[0, 0].data_ptr(), S, r * S, wl.seed, wl.psi,
+                                  self.sptr)
+            zero_cast_params(self.plan, r, r + 1, self._per_rank(self.state[0, 0].data_ptr()),
+                             self.flat.data_ptr(), 0, self.sptr)
+            self.scaler.copy_(torch.frombuffer(bytearray(bytes(zero_scaler_init(self.hp))),
+                                               dtype=torch.uint8))
+
+    def read_scaler(self):
+        self.stream.synchronize()
+        return ZeroScaler.from_buffer_copy(bytes(self.scaler.cpu().numpy().tobytes()))
+
+    def gen_grads(self, step, scale=None):
+        """This rank's replica of step `step` (replica index = rank), with the
+        workload's injection when it lands in this replica."""
+        if scale is None:
+            scale = self.read_scaler().scale
+        wl = self.wl
+        spec = synth.grad_spec(seed=wl.seed, sigma=wl.sigma, bias_sigma=wl.bias_sigma,
+                               loss_scale=scale, outliers=wl.outliers, psi=wl.psi)
+        synth.gpu_fill_grad(self.grad.data_ptr(), self.info.psi_pad, 0, spec,
+                            wl.gen_step(step, wl.n_micro), self.rank, wl.is_bf16, self.sptr)
+        inj = wl.inject
+        if inj is not None and inj[0] == step and inj[1] == self.rank:
+            with torch.cuda.stream(self.stream):
+                self.grad[inj[2]] = inj[3] - 65536 if inj[3] >= 32768 else inj[3]
+
+    def step(self, group=None):
+        """One optimizer step: ring reduce-scatter, the global scalars across
+        the processes, the update of this rank's slice, the all-gather."""
+        from . import dist as zdist
+        st, r = self.sptr, self.rank
+        with torch.cuda.stream(self.stream):
+            self.flags.zero_()
+        sc, fl = self.scaler.data_ptr(), self.flags.data_ptr()
+        zdist.ring_reduce_scatter(self.plan, r, self.N, self.grad.data_ptr(), self.shard,
+                                  (self.bufs[0], self.bufs[1]), sc, fl, self.stream, group)
+        gp = self._per_rank(self.shard.data_ptr())
+        ex = self.exchange.data_ptr()
+        clip = self.hp.max_grad_norm > 0
+        zero_grad_norm_local(self.plan, r, r + 1, gp if clip else None, self.hp, sc,
+                             self.workspace.data_ptr(), ex, st)
+        zdist.sum_exchange(self.exchange, self.stream, group)
+        zero_grad_norm_apply(self.plan, ex, self.hp, sc, st)
+        zero_step(self.plan, r, r + 1, self._state_ptrs(0), self._state_ptrs(1),
+                  self._state_ptrs(2), self.n_sets, gp, None, 0, self.flat.data_ptr(), self.hp,
+                  sc, fl, st)
+        zdist.all_gather_params(self.flat, r, self.N, self.S, self.stream, group)
+
+    def current_state(self):
+        idx = self.read_scaler().state_index if self.n_sets == 2 else 0
+        st = self.state[idx, :, :self.S].cpu()
+        return st[0], st[1], st[2]

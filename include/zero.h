@@ -369,9 +369,12 @@ ZERO_API int zero_grad_norm_apply(const zero_plan* plan, const zero_exchange* d_
  *
  * Two-pass path (grad_shards != NULL, after zero_reduce_scatter and, when
  * hp->max_grad_norm > 0, zero_grad_norm): if the step's overflow word is set
- * nothing is written; otherwise the current state set is updated in place
- * from the reduced gradients (times the clip coefficient when it applies)
- * and the parameters are written (30 bytes per element). n_sets is 1 or 2.
+ * nothing is written; otherwise AdamW runs on the reduced gradients (times
+ * the clip coefficient when it applies) and the parameters are written
+ * (30 bytes per element). n_sets == 2: the current set is read and the
+ * other one written, and the finish makes it current (measured about 4 %
+ * faster on GB300 than updating in place); n_sets == 1: the one set is
+ * updated in place (12 bytes per element less memory).
  *
  * Errors: ZERO_EINVAL (bad ranges or NULL pointers, fused with clip or with
  * n_sets != 2), ZERO_EALIGN, ZERO_ECUDA. */
@@ -451,6 +454,42 @@ ZERO_API int zero_step_update_accum(const zero_plan* plan, int32_t rank_lo, int3
                                     int64_t window_base, void* flat_params,
                                     const zero_hparams* hp, zero_scaler* d_scaler,
                                     uint32_t* d_bucket_flags, void* stream);
+
+/* -------------------------------------- ring reduce-scatter across processes --
+ * "How far does splitting the batch get you?", "Why does the all-reduce not
+ * get more expensive with more ranks?": when the N ranks are N processes,
+ * each with its own 16-bit gradient (the whole padded flat vector), the
+ * reduce-scatter is a ring. Chunk i is owner i's slice [i*S, (i+1)*S): rank
+ * i+1 starts it with its own values, each rank on the way adds its own, and
+ * after N - 1 hops rank i adds its own last, so the sum is taken in the ring
+ * order i+1, ..., N-1, 0, ..., i of zero_reduce_scatter, bit for bit. The
+ * partial sums stay fp32 on the wire ("What does gradient accumulation
+ * actually buy?": an fp32 reduce-scatter), 4 bytes per element per hop.
+ *
+ * zero_ring_hop: this rank's part of hop `hop` (1 .. N) of one step, for
+ * chunk c = (rank - hop) mod N:
+ *   hop 1:        out[k] = widen(grad[c*S + k]); recv must be NULL;
+ *   1 < hop < N:  out[k] = recv[k] + widen(grad[c*S + k]) (fp32, one rounding);
+ *   hop N:        c = rank; out[k] = (recv[k] + widen(grad[c*S + k])) *
+ *                 fp32(1/(S_l*N)), S_l = d_scaler->scale: the unscaled
+ *                 reduced gradient of this rank's slice (grad_shards[rank] of
+ *                 zero_grad_norm_local / zero_step); a non-finite value ORs 1
+ *                 into its bucket's flag and d_scaler->pending.
+ *   (N = 1: hop 1 is the last hop, recv NULL.)
+ * After hops 1 .. N-1 the caller sends `out` to rank (rank + 1) mod N and
+ * receives the next hop's `recv` from rank (rank - 1) mod N (for example with
+ * torch.distributed send/recv; NCCL keeps it on the stream).
+ *   grad: device pointer at flat element 0 of this rank's gradient (psi_pad
+ *         elements, padding zeros); recv, out: S floats each (device).
+ * Reads 2 (+4 when recv) and writes 4 bytes per element. The rest of the
+ * step runs as on one process with the window [rank, rank + 1):
+ * zero_grad_norm_local / zero_grad_norm_apply across processes, then
+ * zero_step; the new parameters are all-gathered by the caller.
+ * Errors: ZERO_EINVAL (bad rank or hop, recv given on hop 1 or missing
+ * after it, NULL pointers), ZERO_EALIGN, ZERO_ECUDA. */
+ZERO_API int zero_ring_hop(const zero_plan* plan, int32_t rank, int32_t hop, const void* grad,
+                           const float* recv, float* out, zero_scaler* d_scaler,
+                           uint32_t* d_bucket_flags, void* stream);
 
 /* Write the 16-bit working copy of the owners' slices from one fp32 master
  * set (round to nearest even): master[i] is rank i's shard (N entries).

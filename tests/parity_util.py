@@ -118,10 +118,10 @@ def report(wl, step, mode, n_compared, dev, orc, got, want, flags_equal):
         f.write(json.dumps(rec) + "\n")
 
 
-def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True):
+def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True, n_sets=None):
     """Full element-wise comparison over every step of `wl`. Returns the
     per-step max relative errors for reporting."""
-    g = harness.Group(wl, two_pass=two_pass)
+    g = harness.Group(wl, two_pass=two_pass, n_sets=n_sets)
     try:
         g.init_state()
         p, _, _ = oracle.make_plan(wl.numels, wl.n_ranks, wl.bucket_elems)
@@ -229,12 +229,12 @@ def gather_state(g, elems):
     return out[0], out[1], out[2], params
 
 
-def run_sampled(wl, steps=None, n_random=2048, n_threads=None):
+def run_sampled(wl, steps=None, n_random=2048, n_threads=None, n_sets=None):
     """Full-size run on the device; the checker regenerates every input on
     the host, computes the global quantities (flags, overflow, norm) over all
     elements and the updates of the sampled elements."""
     steps = wl.steps if steps is None else steps
-    g = harness.Group(wl)
+    g = harness.Group(wl, n_sets=n_sets)
     try:
         g.init_state()
         p, _, _ = oracle.make_plan(wl.numels, wl.n_ranks, wl.bucket_elems)

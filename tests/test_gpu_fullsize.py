@@ -49,8 +49,8 @@ def test_indices_beyond_2p31_fused():
 def test_indices_beyond_2p31_two_pass_clip():
     """One rank whose shard alone holds 2^31 + 12,345 elements, fp16 with a
     dynamic scale and an active clip: the two-pass path, norm records and
-    the update address past 2^31 within a shard."""
+    the update (in place, one state set) address past 2^31 within a shard."""
     wl = W.Workload("int64_clip", [2 ** 31 + 12_345], 1, 0, False, 42, 1e-4, init_scale=4096.0,
                     dynamic_scale=True, max_grad_norm=1.0, steps=2)
-    dev, orc = run_sampled(wl)
+    dev, orc = run_sampled(wl, n_sets=1)
     assert dev.t == 2 and dev.clip_apply == 1

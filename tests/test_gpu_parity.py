@@ -51,6 +51,18 @@ def test_flat_fp16_dynamic_clip_inject():
     assert dev.t == 4 and dev.scale == 32768.0 and dev.n_skipped == 1
 
 
+@pytest.mark.parametrize("per_bucket", [False, True])
+def test_two_pass_in_place_one_set(per_bucket):
+    """The two-pass path with one optimizer state set, updated in place (the
+    harness default is two sets, read one and write the other): clip, a
+    dynamic fp16 scale and a skipped step, whole buckets or bucket by bucket."""
+    psi = 600_011
+    wl = W.FLAT_1P5B.scaled(numels=[psi], bucket_elems=100_000 if per_bucket else 0,
+                            inject=(2, 3, psi // 2, W.FP16_POS_INF), steps=4)
+    stats, dev, orc = run_small(wl, per_bucket=per_bucket, n_sets=1)
+    assert dev.t == 3 and dev.n_skipped == 1 and dev.state_index == 0
+
+
 def test_flat_fp16_inject_fused_skip_recast():
     """Same injection on the fused path: the speculative pass writes the other
     state set and the parameters; the skip re-casts them from the kept set."""
