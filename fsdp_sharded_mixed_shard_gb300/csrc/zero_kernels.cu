@@ -78,7 +78,7 @@ constexpr int kFlagClip = 1;        // kUpdate: apply the clip coefficient from 
 constexpr int kFlagIfPending = 2;   // kCast: only when the overflow word is set
 constexpr int kFlagUseScalerSet = 4;// kCast: master set = scaler->state_index
 constexpr int kFlagPartials = 8;    // kReduce: write norm partials
-constexpr int kFlagFinish = 16;     // kCast: also do the step's bookkeeping (once, last CTA)
+constexpr int kFlagFinish = 16;     // kCast, kFused: also do the step's bookkeeping (once, last CTA)
 
 struct Seg {
   int64_t lo, hi;          // flat element range
@@ -1163,6 +1163,42 @@ __device__ __forceinline__ TileGeom tile_geom(const Args& a, int64_t g, bool off
   return t;
 }
 
+// The step's finish folded into a single-launch fused pass (kFlagFinish):
+// run by the 512 consumer threads after their last tile. Every CTA counts
+// itself done (after its stores, made visible); the last one to finish does
+// the bookkeeping. When the step overflowed it first re-casts the whole
+// launch's parameters from the kept state set, alone: slow (one SM), but an
+// overflow is rare and the host folds only windows of at most
+// kFoldMaxElems elements. No CTA waits for another.
+template <bool kBf16>
+__device__ void fused_finish(const Args& a, const StepScalars& s) {
+  __shared__ int sh_last;
+  consumer_sync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t done = atomicAdd(&a.scaler->finish_count, 1u);
+    sh_last = done == gridDim.x - 1;
+    if (sh_last) __threadfence();
+  }
+  consumer_sync();
+  if (!sh_last) return;
+  if (*reinterpret_cast<volatile uint32_t*>(&a.scaler->pending)) {
+    NormAcc unused_acc;
+    bool unused = false;
+    for (int i = 0; i < a.n_segs; ++i) {
+      const Seg& sg = a.segs[i];
+      for (int64_t j = sg.lo + threadIdx.x; j < sg.hi; j += kConsumers)
+        do_scalar<kCast, kBf16>(a, s, j, sg.rank, 0, unused_acc, unused);
+    }
+    consumer_sync();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    step_bookkeeping(a.scaler, a.beta1, a.beta2, a.bk_dynamic, a.bk_growth, a.bk_flip);
+    a.scaler->finish_count = 0;
+  }
+}
+
 template <int MODE, bool kBf16, int EPT, bool kAcc, bool kOff>
 __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_constant__ Args a,
                                                                int n_slots,
@@ -1200,7 +1236,20 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
   }
   __syncthreads();
   const StepScalars s = sh_s;
-  if (s.skip) return;
+  if (s.skip) {
+    // a folded finish still runs once (the state index was invalid: the
+    // error is recorded, the bookkeeping follows as it would in the finish)
+    if constexpr (MODE == kFused) {
+      if ((a.mode_flags & kFlagFinish) && threadIdx.x == 0) {
+        const uint32_t done = atomicAdd(&a.scaler->finish_count, 1u);
+        if (done == gridDim.x - 1) {
+          step_bookkeeping(a.scaler, a.beta1, a.beta2, a.bk_dynamic, a.bk_growth, a.bk_flip);
+          a.scaler->finish_count = 0;
+        }
+      }
+    }
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.n_ranks;
   const int n_plan = a.plan.n;
@@ -1530,6 +1579,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
         }
       }
     }
+  }
+  if constexpr (MODE == kFused) {
+    if (a.mode_flags & kFlagFinish) fused_finish<kBf16>(a, s);
   }
 }
 
@@ -2068,6 +2120,19 @@ int seg_range(const zero_plan* p, int32_t bucket, int32_t rank_lo, int32_t rank_
   return ZERO_OK;
 }
 
+// A fused step folds its finish into the pass (one launch, the last CTA does
+// the bookkeeping) when the pass is one launch over at most kFoldMaxElems
+// elements: short steps then pay one launch instead of two, and the rare
+// overflow's re-cast by one CTA stays under about 25 MB of traffic.
+constexpr int64_t kFoldMaxElems = int64_t(1) << 22;
+
+bool fold_finish(const zero_plan* p, int32_t rank_lo, int32_t rank_hi) {
+  const int32_t s0 = p->rank_seg0[rank_lo], s1 = p->rank_seg0[rank_hi];
+  if (s1 <= s0 || s1 - s0 > kMaxSegs) return false;
+  const int64_t elems = static_cast<int64_t>(rank_hi - rank_lo) * p->info.shard_elems;
+  return elems > 0 && elems <= kFoldMaxElems;
+}
+
 }  // namespace zk
 
 using namespace zk;
@@ -2393,6 +2458,26 @@ ZERO_API int zero_step_accum(const zero_plan* plan, int32_t rank_lo, int32_t ran
                              const float* const* accum, int32_t n_micro, int64_t window_base,
                              void* flat_params, const zero_hparams* hp, zero_scaler* d_scaler,
                              uint32_t* d_bucket_flags, void* stream) {
+  if (grad_shards == nullptr && ranks_ok(plan, rank_lo, rank_hi) &&
+      fold_finish(plan, rank_lo, rank_hi)) {
+    Args* a = nullptr;
+    int rc = prepare_step(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets, nullptr,
+                          replicas, window_base, flat_params, hp, d_scaler, d_bucket_flags, true,
+                          true, &a);
+    if (rc) return rc;
+    if ((rc = set_accumulators(*a, plan, accum, n_micro))) {
+      delete a;
+      return rc;
+    }
+    a->mode_flags |= kFlagFinish;
+    a->bk_dynamic = hp->dynamic_scale;
+    a->bk_growth = hp->growth_interval;
+    a->bk_flip = 1;
+    rc = launch<kFused>(plan, *a, plan->rank_seg0[rank_lo], plan->rank_seg0[rank_hi],
+                        static_cast<cudaStream_t>(stream));
+    delete a;
+    return rc;
+  }
   int rc = zero_step_update_accum(plan, rank_lo, rank_hi, master, exp_avg, exp_avg_sq, n_sets,
                                   grad_shards, replicas, accum, n_micro, window_base,
                                   flat_params, hp, d_scaler, d_bucket_flags, stream);

@@ -139,6 +139,8 @@ def all_gather_params(flat, rank, world, shard_elems, stream=None, group=None):
         return
     if flat.is_cuda:
         (stream or torch.cuda.current_stream(flat.device)).synchronize()
-    parts = [torch.empty(shard_elems, dtype=flat.dtype) for _ in range(world)]
-    dist.all_gather(parts, mine.cpu(), group=group)
-    flat[:n].copy_(torch.cat(parts))
+    # as bytes: gloo's all-gather takes no 16-bit integer tensors
+    nbytes = shard_elems * flat.element_size()
+    parts = [torch.empty(nbytes, dtype=torch.uint8) for _ in range(world)]
+    dist.all_gather(parts, mine.cpu().contiguous().view(torch.uint8), group=group)
+    flat[:n].copy_(torch.cat(parts).view(flat.dtype))

@@ -386,9 +386,12 @@ ZERO_API int zero_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
                        uint32_t* d_bucket_flags, void* stream);
 
 /* zero_step in two calls, for callers that want to place their own work (or
- * timing events) between the update and the bookkeeping. zero_step(...) is
- * exactly zero_step_update(...) followed by zero_step_finish(...) with the
- * same arguments.
+ * timing events) between the update and the bookkeeping. zero_step(...)
+ * gives exactly the results of zero_step_update(...) followed by
+ * zero_step_finish(...) with the same arguments. (A fused zero_step whose
+ * pass is one launch over at most 2^22 elements folds the finish into the
+ * pass: the last CTA to finish does the bookkeeping and, if the step
+ * overflowed, re-casts the parameters; one launch instead of two.)
  * zero_step_update launches the update kernel of the chosen path (fused or
  * two-pass) and nothing else. zero_step_finish re-casts the parameters from
  * the kept master set if the fused step overflowed, then updates the loss
@@ -525,7 +528,8 @@ ZERO_API int zero_selftest_check(void* stream);
 
 /* Kernels launched per call, for accounting (L = ceil(segments processed /
  * 128), empty launches skipped): fused zero_step L + L (update; overflow
- * re-cast check merged with the bookkeeping in the last), two-pass zero_step
+ * re-cast check merged with the bookkeeping in the last), or 1 when it folds
+ * the finish into the pass (L == 1, at most 2^22 elements), two-pass zero_step
  * L + 1, zero_reduce_scatter L, zero_grad_norm 2 (+ L when it recomputes the
  * records), zero_grad_norm_local 2 with clipping (+ L when it recomputes),
  * 1 without, zero_grad_norm_apply 1, zero_cast_params L. */

@@ -73,6 +73,49 @@ def test_flat_fp16_inject_fused_skip_recast():
     assert dev.t == 2 and dev.scale == 32768.0
 
 
+@pytest.mark.parametrize("n_micro", [1, 2])
+def test_folded_finish_equals_two_launches(n_micro):
+    """zero_step on a small fused step is one launch (the last CTA does the
+    bookkeeping, and on an overflow re-casts the parameters alone);
+    zero_step_update + zero_step_finish is two. Same state, parameters and
+    scaler after every step, bit for bit, through a skipped step."""
+    import fsdp_sharded_mixed_shard_gb300 as Z
+    psi = 4 * 50_001 - 1
+    wl = W.Workload("fold", [psi], 4, 0, False, 24, 1e-4, init_scale=4096.0,
+                    dynamic_scale=True, steps=4, n_micro=n_micro,
+                    inject=(2, 1, psi // 2, W.FP16_POS_INF))
+    a, b = harness.Group(wl), harness.Group(wl)
+    try:
+        for g in (a, b):
+            g.init_state()
+        for step in range(1, wl.steps + 1):
+            for g in (a, b):
+                for mb in range(1, n_micro):
+                    g.gen_grads(step, micro=mb)
+                    g.accumulate(first=(mb == 1))
+                g.gen_grads(step)
+            a.step()   # zero_step_accum: folded
+            m, v, w = b._state_ptrs(0), b._state_ptrs(1), b._state_ptrs(2)
+            acc = b.accum_ptrs() if n_micro > 1 else None
+            b.flags.zero_()
+            Z.zero_step_update_accum(b.plan, 0, 4, m, v, w, 2, None, b.rep_ptrs(), acc, n_micro,
+                                     0, b.flat.data_ptr(), b.hp, b.scaler.data_ptr(),
+                                     b.flags.data_ptr(), b.sptr)
+            Z.zero_step_finish(b.plan, 0, 4, m, 2, None, 0, b.flat.data_ptr(), b.hp,
+                               b.scaler.data_ptr(), b.sptr)
+            torch.cuda.synchronize()
+            assert bytes(a.scaler.cpu().numpy()) == bytes(b.scaler.cpu().numpy()), step
+            assert torch.equal(a.flat, b.flat), step
+            sa, sb = a.current_state(), b.current_state()
+            for x, y in zip(sa, sb):
+                assert torch.equal(x.view(torch.int32), y.view(torch.int32)), step
+        s = a.read_scaler()
+        assert s.t == 3 and s.n_skipped == 1 and s.finish_count == 0
+    finally:
+        a.close()
+        b.close()
+
+
 @pytest.mark.parametrize("rank", [0, 5])
 def test_stage3_slice_small(rank):
     S = 20011  # odd: rank 5's window starts off the 16-byte grid

@@ -106,3 +106,38 @@ def test_ring_schedule_covers_every_chunk_once():
             assert sorted(chunks) == list(range(world))
             for r in range(world):
                 assert zdist.ring_schedule((r + 1) % world, world)[h][1] == chunks[r]
+
+
+def _gather_worker(rank, world, port, S, q):
+    sys.path.insert(0, ROOT)
+    from fsdp_sharded_mixed_shard_gb300 import dist as zdist
+    dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank,
+                            world_size=world)
+    flat = torch.full((world * S + 5,), -1, dtype=torch.int16)
+    flat[rank * S:(rank + 1) * S] = torch.arange(S, dtype=torch.int16) * 7 + rank * 1000 - 30000
+    zdist.all_gather_params(flat, rank, world, S)
+    q.put((rank, flat.numpy().copy()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,S", [(2, 5), (3, 1001), (4, 1)])
+def test_all_gather_params_fills_every_slot(world, S):
+    """The parameter all-gather on CPU ranks: every rank ends with every
+    rank's 16-bit slot, and nothing past world * S is touched."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_worker, args=(r, world, port, S, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    want = np.concatenate([np.arange(S, dtype=np.int16) * 7 + r * 1000 - 30000
+                           for r in range(world)]).astype(np.int16)
+    for r in range(world):
+        assert np.array_equal(got[r][:world * S], want)
+        assert (got[r][world * S:] == -1).all()
