@@ -398,8 +398,12 @@ def run_libzero(args, rank, world, dist):
     else:
         every, first_sampled = PHASE_SAMPLE, min(PHASE_SAMPLE - 1, K - 1)
     sampled = [k for k in range(K) if k % every == first_sampled % every and k >= first_sampled]
+    # cold steps: one event pair per step; with a single phase it is the
+    # phase's own pair (an event pair costs the GPU a few microseconds, which
+    # two nested pairs would count twice)
+    nested = flush_buf is not None and len(ph) > 1
     step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(K if flush_buf is not None else 0)]
+                for _ in range(K if nested else 0)]
     evs = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(len(sampled) * max(1, k_micro))] for name, _ in ph}
     ev_i = {name: 0 for name, _ in ph}
@@ -408,13 +412,19 @@ def run_libzero(args, rank, world, dist):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    if flush_buf is not None and hasattr(torch.cuda, "_sleep"):
+        # cold steps are short: a GPU-side pause before the loop lets the host
+        # enqueue ahead of the GPU, so no event pair waits for the host
+        with torch.cuda.stream(g.stream):
+            torch.cuda._sleep(int(2e7))
     wall0 = time.time()
     t0.record(g.stream)
     for k in range(K):
         if flush_buf is not None:
             with torch.cuda.stream(g.stream):
                 flush_buf.fill_(k)
-            step_evs[k][0].record(g.stream)
+            if nested:
+                step_evs[k][0].record(g.stream)
         if k not in sampled_set:
             if graph is not None:
                 with torch.cuda.stream(g.stream):  # replay() launches on the current stream
@@ -429,7 +439,7 @@ def run_libzero(args, rank, world, dist):
             a.record(g.stream)
             f()
             b.record(g.stream)
-        if flush_buf is not None:
+        if nested:
             step_evs[k][1].record(g.stream)
     t1.record(g.stream)
     torch.cuda.synchronize()
@@ -438,8 +448,10 @@ def run_libzero(args, rank, world, dist):
     if dist:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    if flush_buf is not None:
+    if nested:
         total_ms = sum(a.elapsed_time(b) for a, b in step_evs)
+    elif flush_buf is not None:
+        total_ms = sum(a.elapsed_time(b) for a, b in evs[ph[0][0]][:ev_i[ph[0][0]]])
     phase_ms = {name: statistics.mean(a.elapsed_time(b) for a, b in evs[name][:ev_i[name]])
                 for name, _ in ph}
 
