@@ -66,6 +66,8 @@ def parse_args():
                          "every unit) on the 8.81B-parameter layout at 64 ranks instead")
     ap.add_argument("--units-align", type=int, default=1,
                     help="unit padding grain in elements for --gather (1: multiple of N)")
+    ap.add_argument("--units-per-call", type=int, default=1,
+                    help="--gather: units gathered per call (a prefetch window), 1 or more")
     ap.add_argument("--numel-cap", type=int, default=0,
                     help="run the workload's first N flat parameters only (small profiling case)")
     ap.add_argument("--flat", type=int, default=0,
@@ -641,19 +643,28 @@ def run_gather(args, rank, world, dist):
             k += 1
         uw = W.UnitWorkload(uw.name + "_first%d" % k, uw.numels[:k], list(range(k)), k,
                             uw.n_ranks, uw.align_elems, uw.seed)
-    g = harness.UnitGroup(uw, device=dev, window=2)
+    W_ = max(1, args.units_per_call)
+    # two sets of W unit buffers: consecutive calls alternate between them
+    g = harness.UnitGroup(uw, device=dev, window=2 * W_)
     g.fill_shards()
     U = uw.n_units
-    order = list(range(U)) + list(reversed(range(U)))
-    calls = [(u, i % 2) for i, u in enumerate(order)]
+    # forward: windows of W units in order; backward: the same windows in reverse
+    fwd = [(u, min(u + W_, U)) for u in range(0, U, W_)]
+    calls = [(lo_u, hi_u, (i % 2) * W_) for i, (lo_u, hi_u) in
+             enumerate(fwd + list(reversed(fwd)))]
     gathered = 2 * g.info.psi_pad
     for _ in range(args.warmup):
-        for u, slot in calls:
-            g.gather(u, u + 1, slot)
+        for lo_u, hi_u, slot in calls:
+            g.gather(lo_u, hi_u, slot)
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in calls] for _ in range(K)]
+    # per-call events on one timed step in PHASE_SAMPLE (never the first; the
+    # last step when there are fewer): an event between two launches stops
+    # the next one from starting early, so the other steps run back to back
+    first = min(PHASE_SAMPLE - 1, K - 1)
+    sampled = [k for k in range(first, K, PHASE_SAMPLE)]
+    evs = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in calls] for k in sampled}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(device_uuid(dev))
     if dist:
@@ -663,9 +674,13 @@ def run_gather(args, rank, world, dist):
     time.sleep(0.3)
     t0.record(g.stream)
     for k in range(K):
-        for (u, slot), (a, b) in zip(calls, evs[k]):
+        if k not in evs:
+            for lo_u, hi_u, slot in calls:
+                g.gather(lo_u, hi_u, slot)
+            continue
+        for (lo_u, hi_u, slot), (a, b) in zip(calls, evs[k]):
             a.record(g.stream)
-            g.gather(u, u + 1, slot)
+            g.gather(lo_u, hi_u, slot)
             b.record(g.stream)
     t1.record(g.stream)
     torch.cuda.synchronize()
@@ -674,15 +689,20 @@ def run_gather(args, rank, world, dist):
         dist.barrier()
     total_ms = max_over_ranks(dist, t0.elapsed_time(t1))
     ms_per_step = total_ms / K
-    # per-unit launch durations of the block units (the root unit differs in size)
-    block = [i for i, (u, _) in enumerate(calls) if g.units[u].psi_pad == g.info.max_unit_psi_pad]
-    blk_ms = statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(K)
-                             for i in block)
+    # call durations of the calls made of block units only (the root unit
+    # differs in size), per gathered block unit
+    blk = g.info.max_unit_psi_pad
+    block = [i for i, (lo_u, hi_u, _) in enumerate(calls)
+             if all(g.units[u].psi_pad == blk for u in range(lo_u, hi_u))]
+    per_unit = [evs[k][i][0].elapsed_time(evs[k][i][1]) / (calls[i][1] - calls[i][0])
+                for k in sampled for i in block]
+    blk_ms = statistics.mean(per_unit)
     peak, peak_kind = peaks()
-    unit_bytes = 4 * g.info.max_unit_psi_pad
+    unit_bytes = 4 * blk
     achieved = unit_bytes / (blk_ms / 1e3) / 1e9
-    # one launch per call (64 slices, at most 256 per launch) for a non-empty unit
-    launches = sum(1 for u, _ in calls if g.units[u].shard_elems)
+    # one launch per 256 slices of non-empty units in a call (N slices per unit)
+    launches = sum(-(-sum(g.N for u in range(lo_u, hi_u) if g.units[u].shard_elems) // 256)
+                   for lo_u, hi_u, _ in calls)
     traffic = profiled_traffic("copy_kernel", uw.name, "gather.cu")
     # per-rank accounting of the layout under each sharding strategy (host)
     import fsdp_sharded_mixed_shard_gb300 as Z
@@ -703,7 +723,7 @@ def run_gather(args, rank, world, dist):
             "config": {"workload": uw.name, "n_units": U, "n_ranks": 64,
                        "align_elems": uw.align_elems, "psi": g.info.psi,
                        "psi_pad": g.info.psi_pad, "block_unit_elems": g.info.max_unit_psi_pad,
-                       "gathers_per_step": len(calls),
+                       "gathers_per_step": len(calls), "units_per_call": W_,
                        "l2": "inputs larger than L2 (%.1f GB of shards)" % (2 * g.info.psi_pad / 1e9)},
             "roofline": {"bound": "hbm", "kernel": "copy_kernel", "achieved": round(achieved, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -713,6 +733,7 @@ def run_gather(args, rank, world, dist):
                          "step_achieved_gbs": round(4 * gathered / (ms_per_step / 1e3) / 1e9, 1),
                          "step_frac": round(4 * gathered / (ms_per_step / 1e3) / 1e9 / peak, 4)},
             "accounting_per_rank": accounting,
+            "phase_events": "per-call CUDA events on %d of %d timed steps" % (len(sampled), K),
             "e2e": None, "gpu_launches": launches * K, "clocks": clk}
     g.close()
     return line
