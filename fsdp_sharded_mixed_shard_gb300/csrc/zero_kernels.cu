@@ -1183,12 +1183,28 @@ __device__ void fused_finish(const Args& a, const StepScalars& s) {
   consumer_sync();
   if (!sh_last) return;
   if (*reinterpret_cast<volatile uint32_t*>(&a.scaler->pending)) {
+    // the re-cast of every tile of the launch, as step_kernel<kCast> does it:
+    // 16-byte vectors where the owner sits on the grid, single elements at
+    // the edges
     NormAcc unused_acc;
     bool unused = false;
-    for (int i = 0; i < a.n_segs; ++i) {
-      const Seg& sg = a.segs[i];
-      for (int64_t j = sg.lo + threadIdx.x; j < sg.hi; j += kConsumers)
-        do_scalar<kCast, kBf16>(a, s, j, sg.rank, 0, unused_acc, unused);
+    for (int64_t g = 0; g < a.n_tiles; ++g) {
+      const Seg& sg = a.segs[find_seg(a, g)];
+      const int64_t lo = sg.lo + (g - sg.tile_local0) * kTile;
+      const int64_t hi = min(lo + kTile, sg.hi);
+      const int64_t rank0 = static_cast<int64_t>(sg.rank) * a.shard;
+      int64_t va = hi, vb = hi;
+      if (((rank0 - a.wbase) & 3) == 0) {
+        va = min(lo + ((a.wbase - lo) & 7), hi);
+        vb = va + ((hi - va) & ~static_cast<int64_t>(7));
+      }
+      const int nvec = static_cast<int>((vb - va) >> 3);
+      for (int q = threadIdx.x; q < nvec; q += kConsumers)
+        do_vector<kCast, kBf16>(a, s, va + static_cast<int64_t>(q) * kVec, sg.rank, unused_acc);
+      const int nhead = static_cast<int>(va - lo), ntail = static_cast<int>(hi - vb);
+      for (int q = threadIdx.x; q < nhead + ntail; q += kConsumers)
+        do_scalar<kCast, kBf16>(a, s, q < nhead ? lo + q : vb + (q - nhead), sg.rank, 0,
+                                unused_acc, unused);
     }
     consumer_sync();
   }
