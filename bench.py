@@ -110,6 +110,7 @@ def psi_step(wl):
 
 L2_BYTES = 129e6   # GB300 L2
 FOLD_MAX_ELEMS = 1 << 22  # zero_step: largest single-launch fused window that folds its finish
+SHORT_MAX_ELEMS = 1 << 20  # zero_step: largest fused window (N <= 4, one micro-batch) taken by the short-step kernel
 FLUSH_BYTES = 256 << 20
 
 
@@ -476,8 +477,12 @@ def run_libzero(args, rank, world, dist):
                    "reduce_scatter": "bulk_kernel<kReduce>",
                    "update": "bulk_kernel<kUpdate>", "accumulate": "accumulate_kernel:add",
                    "accumulate_first": "accumulate_kernel:first"}[dom]
+    if (dom == "fused_step" and L == 1 and (hi - lo) * g.S <= SHORT_MAX_ELEMS and N <= 4
+            and k_micro == 1):
+        kernel_name = "short_fused_kernel"
     if k_micro > 1 and dom in ("fused_update", "fused_step", "reduce_scatter"):
-        kernel_name = kernel_name[:-1] + ",acc>"
+        kernel_name = (kernel_name[:-1] + ",acc>" if kernel_name.endswith(">")
+                       else kernel_name + "<acc>")
     kernel_gbs = {n: round(bytes_per_param[n] * pstep / (phase_ms[n] / 1e3) / 1e9, 1)
                   for n, _ in ph if bytes_per_param[n] > 0}
     traffic = profiled_traffic(kernel_name, wl.name)

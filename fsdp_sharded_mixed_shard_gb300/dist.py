@@ -132,14 +132,15 @@ def all_gather_params(flat, rank, world, shard_elems, stream=None, group=None):
     ZeRO & FSDP", "ZeRO stages 1, 2 and 3")."""
     n = world * shard_elems
     mine = flat[rank * shard_elems:(rank + 1) * shard_elems]
+    # the slots travel as bytes: neither NCCL nor gloo gathers int16 tensors
     if flat.is_cuda and dist.get_backend(group) == "nccl":
         s = stream if stream is not None else torch.cuda.current_stream(flat.device)
         with torch.cuda.stream(s):
-            dist.all_gather_into_tensor(flat[:n], mine.clone(), group=group)
+            dist.all_gather_into_tensor(flat[:n].view(torch.uint8),
+                                        mine.clone().view(torch.uint8), group=group)
         return
     if flat.is_cuda:
         (stream or torch.cuda.current_stream(flat.device)).synchronize()
-    # as bytes: gloo's all-gather takes no 16-bit integer tensors
     nbytes = shard_elems * flat.element_size()
     parts = [torch.empty(nbytes, dtype=torch.uint8) for _ in range(world)]
     dist.all_gather(parts, mine.cpu().contiguous().view(torch.uint8), group=group)

@@ -478,3 +478,26 @@ def test_out_of_phase_windows_and_buckets(rank_lo, rank_hi, bucket, per_bucket, 
         p, _, _ = oracle.make_plan(wl.numels, 8, bucket)
         assert p.shard % 2 == 1
         run_small(wl, per_bucket=per_bucket and clip > 0, two_pass=clip > 0)
+
+
+@pytest.mark.parametrize("n,psi,bf16,scale,dynamic,lo,hi,bucket,inject", [
+    (4, 4 * 30_001 - 1, False, 1024.0, False, 0, 4, 0, None),   # S odd: every 16-bit phase
+    (4, 4 * 30_001 - 1, False, 1000.0, False, 0, 4, 0, None),   # S_l not a power of two
+    (3, 3 * 30_002, True, 1.0, False, 0, 3, 0, None),           # S_l N = 3
+    (2, 2 * 30_003, True, 2.0 ** -20, False, 0, 2, 7, None),    # small S_l, odd buckets
+    (4, 4 * 30_001 - 1, True, 1.0, False, 1, 3, 0, None),       # a window of two owners
+    (1, 1_000_000, True, 1.0, False, 0, 1, 0, None),
+    (4, 4 * 30_002, False, 3000.0, True, 0, 4, 0, (2, 2, 70_001, 0x7C00)),  # overflow, re-cast
+])
+def test_short_steps(n, psi, bf16, scale, dynamic, lo, hi, bucket, inject):
+    """Fused steps over at most 2^20 elements at N <= 4 without micro-batch
+    accumulators run the short-step kernel (one wave of small CTAs, each CTA
+    inside one owner's slice). Every shard phase against the 16-byte grid,
+    loss scales whose product with N is and is not a power of two (two ways
+    of forming 1 / (S_l N)), rank windows and an overflowed step, against the
+    checker element by element."""
+    wl = W.Workload("short", [psi], n, bucket, bf16, 71, 1e-3, init_scale=scale,
+                    dynamic_scale=dynamic, steps=3, rank_lo=lo, rank_hi=hi, inject=inject)
+    stats, dev, orc = run_small(wl, two_pass=False)
+    if inject is not None:
+        assert dev.n_skipped == 1 and dev.scale == 1500.0

@@ -142,3 +142,49 @@ def test_split_windows_equal_one_process(name):
     _compare(whole, parts, S)
     if wl.inject is not None:
         assert whole["scaler"][3] == 1  # one step skipped everywhere
+
+
+def _nccl_child(port, q):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as tdist
+    from fsdp_sharded_mixed_shard_gb300 import dist as zdist
+    try:
+        torch.cuda.set_device(0)
+        tdist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0,
+                                 world_size=1, timeout=datetime.timedelta(seconds=120))
+        wl = CASES["clip_fp16_inject_other_window"][0]
+        stream = torch.cuda.current_stream()
+        snap = _run_window(wl, wl.steps, lambda blob: zdist.sum_exchange(blob, stream))
+        # the parameter all-gather's NCCL branch, one rank: the buffer is unchanged
+        flat = torch.arange(64, dtype=torch.int16, device="cuda")
+        before = flat.clone()
+        zdist.all_gather_params(flat, 0, 1, 64, stream)
+        torch.cuda.synchronize()
+        q.put(("ok", snap, bool(torch.equal(flat, before))))
+        tdist.destroy_process_group()
+    except BaseException as e:
+        q.put(("error: %r" % (e,), None, None))
+        raise
+
+
+def test_exchange_over_nccl_single_rank():
+    """The exchange's NCCL branch (an all-reduce on the stream) and the
+    parameter all-gather's (all_gather_into_tensor) with a one-rank NCCL
+    group: the step equals the one-process step without an exchange, bit
+    for bit. One rank waits on nobody; more ranks need more GPUs."""
+    wl = CASES["clip_fp16_inject_other_window"][0]
+    whole = _run_window(wl, wl.steps)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_nccl_child, args=(_free_port(), q))
+    p.start()
+    try:
+        status, snap, gathered = q.get(timeout=600)
+    finally:
+        p.join(timeout=120)
+        if p.is_alive():
+            p.terminate()
+    assert status == "ok", status
+    assert p.exitcode == 0
+    _compare(whole, [snap], (wl.psi + (-wl.psi) % wl.n_ranks) // wl.n_ranks)
+    assert gathered
