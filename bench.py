@@ -110,7 +110,8 @@ def psi_step(wl):
 
 L2_BYTES = 129e6   # GB300 L2
 FOLD_MAX_ELEMS = 1 << 22  # zero_step: largest single-launch fused window that folds its finish
-SHORT_MAX_ELEMS = 1 << 20  # zero_step: largest fused window (N <= 4, one micro-batch) taken by the short-step kernel
+SHORT_MAX_ELEMS = 1 << 20  # zero_step: largest fused window (N <= 16, one micro-batch) taken by the short-step kernel
+SHORT_MAX_RANKS = 16
 FLUSH_BYTES = 256 << 20
 
 
@@ -477,8 +478,8 @@ def run_libzero(args, rank, world, dist):
                    "reduce_scatter": "bulk_kernel<kReduce>",
                    "update": "bulk_kernel<kUpdate>", "accumulate": "accumulate_kernel:add",
                    "accumulate_first": "accumulate_kernel:first"}[dom]
-    if (dom == "fused_step" and L == 1 and (hi - lo) * g.S <= SHORT_MAX_ELEMS and N <= 4
-            and k_micro == 1):
+    if (dom == "fused_step" and L == 1 and (hi - lo) * g.S <= SHORT_MAX_ELEMS
+            and N <= SHORT_MAX_RANKS and k_micro == 1):
         kernel_name = "short_fused_kernel"
     if k_micro > 1 and dom in ("fused_update", "fused_step", "reduce_scatter"):
         kernel_name = (kernel_name[:-1] + ",acc>" if kernel_name.endswith(">")

@@ -58,6 +58,7 @@
 #include <vector>
 
 #include "checked.cuh"
+#include "f64emu.h"
 #include "pdl.cuh"
 #include "zero_internal.h"
 
@@ -416,29 +417,94 @@ __device__ __forceinline__ int find_seg(const Args& a, int64_t g) {
 // Loss scale, skip and step-count bookkeeping at the end of a step
 // ("Training models too big for one GPU: ZeRO & FSDP", "Mixed-precision
 // training": pick the scale dynamically and skip a step on overflow).
-__device__ void step_bookkeeping(zero_scaler* sc, double beta1, double beta2, int dynamic,
-                                 int growth_interval, int flip_sets) {
-  const uint32_t ov = sc->pending;
+// RN(x * y) in fp64, in integer arithmetic where f64emu covers it (the
+// narrow fp64 pipe otherwise): the same bits either way.
+__device__ __forceinline__ double dmul_exact(double x, double y) {
+  uint64_t r;
+  if (f64emu::mul(static_cast<uint64_t>(__double_as_longlong(x)),
+                  static_cast<uint64_t>(__double_as_longlong(y)), &r))
+    return __longlong_as_double(static_cast<long long>(r));
+  return __dmul_rn(x, y);
+}
+
+// Adam's bias correction of step t + 1 from the stored power pw = beta^t:
+// p = RN(pw beta) (the next stored power) and bc = RN32(RN(1 - p)).
+__device__ __forceinline__ void bias_correction(double pw, double beta, double* p, float* bc) {
+  const double q = dmul_exact(pw, beta);
+  uint64_t d;
+  uint32_t f;
+  if (f64emu::one_minus(static_cast<uint64_t>(__double_as_longlong(q)), &d) &&
+      f64emu::to_f32(d, &f)) {
+    *bc = __uint_as_float(f);
+  } else {
+    *bc = __double2float_rn(__dsub_rn(1.0, q));
+  }
+  *p = q;
+}
+
+// fp32(1 / (S_l N k)) with the product and quotient in fp64. When S_l is a
+// power of two and so is N k, the quotient is a power of two, exact in fp64
+// and in fp32, formed from the exponents alone.
+__device__ __forceinline__ float inverse_scale(float sl, int32_t n_ranks, int32_t n_micro) {
+  const uint32_t sb = __float_as_uint(sl);
+  const uint64_t nk = static_cast<uint64_t>(n_ranks) * static_cast<uint64_t>(n_micro);
+  const int es = static_cast<int>((sb >> 23) & 0xFFu);
+  if ((sb & 0x807FFFFFu) == 0 && es != 0 && es != 255 && nk != 0 && (nk & (nk - 1)) == 0) {
+    const int e = es - 127 + (63 - __clzll(static_cast<long long>(nk)));
+    if (e >= -126 && e <= 126) return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  }
+  const double denom = __dmul_rn(__dmul_rn(static_cast<double>(sl), static_cast<double>(n_ranks)),
+                                 static_cast<double>(n_micro));
+  return __double2float_rn(__ddiv_rn(1.0, denom));
+}
+
+// The scaler fields the bookkeeping reads, taken before it writes any.
+struct ScalerSnap {
+  double p1, p2;  // beta1_pow * beta1, beta2_pow * beta2: the powers after a good step
+  float scale;
+  int32_t good_steps, t, n_skipped, state_index;
+  uint32_t pending;
+};
+
+// The bookkeeping's stores, from a snapshot and the step's overflow vote.
+__device__ __forceinline__ void bookkeeping_store(zero_scaler* sc, const ScalerSnap& q, bool ov,
+                                                  int dynamic, int growth_interval,
+                                                  int flip_sets) {
   sc->pending = 0;
   sc->overflow = ov ? 1u : 0u;
   if (ov) {
     if (dynamic) {
-      const float half = __fmul_rn(sc->scale, 0.5f);
+      const float half = __fmul_rn(q.scale, 0.5f);
       sc->scale = half < 1.0f ? 1.0f : half;
     }
     sc->good_steps = 0;
-    sc->n_skipped += 1;
+    sc->n_skipped = q.n_skipped + 1;
     return;
   }
-  sc->t += 1;
-  sc->beta1_pow = __dmul_rn(sc->beta1_pow, beta1);
-  sc->beta2_pow = __dmul_rn(sc->beta2_pow, beta2);
-  sc->good_steps += 1;
-  if (dynamic && sc->good_steps >= growth_interval) {
-    sc->scale = __fmul_rn(sc->scale, 2.0f);
-    sc->good_steps = 0;
+  sc->t = q.t + 1;
+  sc->beta1_pow = q.p1;
+  sc->beta2_pow = q.p2;
+  int good = q.good_steps + 1;
+  if (dynamic && good >= growth_interval) {
+    sc->scale = __fmul_rn(q.scale, 2.0f);
+    good = 0;
   }
-  if (flip_sets) sc->state_index ^= 1;
+  sc->good_steps = good;
+  if (flip_sets) sc->state_index = q.state_index ^ 1;
+}
+
+__device__ void step_bookkeeping(zero_scaler* sc, double beta1, double beta2, int dynamic,
+                                 int growth_interval, int flip_sets) {
+  ScalerSnap q;
+  q.pending = sc->pending;
+  q.scale = sc->scale;
+  q.good_steps = sc->good_steps;
+  q.t = sc->t;
+  q.n_skipped = sc->n_skipped;
+  q.state_index = sc->state_index;
+  q.p1 = dmul_exact(sc->beta1_pow, beta1);
+  q.p2 = dmul_exact(sc->beta2_pow, beta2);
+  bookkeeping_store(sc, q, q.pending != 0, dynamic, growth_interval, flip_sets);
 }
 
 // -------------------------------------------------------------- prologue --
@@ -455,16 +521,14 @@ __device__ void compute_step_scalars(const Args& a, StepScalars* out) {
   s.dst = 0;
   if (MODE == kFused || MODE == kReduce) {
     // average over the N ranks and the k micro-batches of each, after the loss scale
-    const double denom = __dmul_rn(
-        __dmul_rn(static_cast<double>(sc->scale), static_cast<double>(a.n_ranks)),
-        static_cast<double>(a.n_micro));
-    s.inv = __double2float_rn(__ddiv_rn(1.0, denom));
+    s.inv = inverse_scale(sc->scale, a.n_ranks, a.n_micro);
   }
   if (MODE == kFused || MODE == kUpdate) {
-    const double p1 = __dmul_rn(sc->beta1_pow, a.beta1);
-    const double p2 = __dmul_rn(sc->beta2_pow, a.beta2);
-    s.bc1 = __double2float_rn(__dsub_rn(1.0, p1));
-    s.bc2 = __double2float_rn(__dsub_rn(1.0, p2));
+    double p1, p2;  // the next powers: only the bookkeeping stores them
+    bias_correction(sc->beta1_pow, a.beta1, &p1, &s.bc1);
+    bias_correction(sc->beta2_pow, a.beta2, &p2, &s.bc2);
+    (void)p1;
+    (void)p2;
     const int idx = sc->state_index;
     if (idx < 0 || idx >= a.n_sets || (MODE == kFused && a.n_sets != 2)) {
       set_error(sc, ZERO_DEVERR_STATE_INDEX);
@@ -1617,40 +1681,34 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 // are the same bits. The last CTA to finish does the step's bookkeeping,
 // after re-casting the parameters from the kept state set when the step
 // overflowed. No CTA waits for another.
-constexpr int kShortThreads = 128;
+constexpr int kShortThreads = 256;  // 8 CTAs per SM; half the CTAs of 128 count in the tail
 constexpr int kShortChunk = 4;  // replicas whose loads are in flight together
+constexpr uint32_t kShortVoteUnit = 1u << 16;  // finish_count: CTAs below, votes above
 
 // The fused pass's step scalars, computed by four threads of different warps
-// at once (the fp64 operations are few but slow on this part, and every
-// warp of the CTA waits for the last of them). Same values as
-// compute_step_scalars<kFused>. When S_l * N * micro-batches is a power of
-// two (a power-of-two loss scale), 1 / (S_l N k) is that power's inverse,
-// exact in fp64 and in fp32, and is formed from the exponents alone.
-__device__ __forceinline__ void short_step_scalars(const Args& a, StepScalars* sh) {
+// at once (every warp of the CTA waits for the last of them), plus the
+// scaler fields the bookkeeping needs. Same values as
+// compute_step_scalars<kFused>.
+__device__ __forceinline__ void short_step_scalars(const Args& a, StepScalars* sh,
+                                                   ScalerSnap* snap) {
   zero_scaler* sc = a.scaler;
   const int t = threadIdx.x;
   if (t == 0) {
     const float sl = sc->scale;
-    const uint32_t sb = __float_as_uint(sl);
-    const uint64_t nk = static_cast<uint64_t>(a.n_ranks) * static_cast<uint64_t>(a.n_micro);
-    const int es = static_cast<int>((sb >> 23) & 0xFFu);
-    const int e = es - 127 + (63 - __clzll(static_cast<long long>(nk)));
-    if ((sb & 0x807FFFFFu) == 0 && es != 0 && es != 255 && nk != 0 && (nk & (nk - 1)) == 0 &&
-        e >= -126 && e <= 126) {
-      sh->inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    } else {
-      const double denom = __dmul_rn(
-          __dmul_rn(static_cast<double>(sl), static_cast<double>(a.n_ranks)),
-          static_cast<double>(a.n_micro));
-      sh->inv = __double2float_rn(__ddiv_rn(1.0, denom));
-    }
+    sh->inv = inverse_scale(sl, a.n_ranks, a.n_micro);
     sh->clip = 1.0f;
+    snap->scale = sl;
   } else if (t == 32) {
-    sh->bc1 = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc->beta1_pow, a.beta1)));
+    bias_correction(sc->beta1_pow, a.beta1, &snap->p1, &sh->bc1);
   } else if (t == 64) {
-    sh->bc2 = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc->beta2_pow, a.beta2)));
+    bias_correction(sc->beta2_pow, a.beta2, &snap->p2, &sh->bc2);
   } else if (t == 96) {
+    snap->pending = sc->pending;
+    snap->good_steps = sc->good_steps;
+    snap->t = sc->t;
+    snap->n_skipped = sc->n_skipped;
     const int idx = sc->state_index;
+    snap->state_index = idx;
     int skip = 0;
     if (idx < 0 || idx >= a.n_sets || a.n_sets != 2) {
       set_error(sc, ZERO_DEVERR_STATE_INDEX);
@@ -1682,13 +1740,14 @@ __device__ __forceinline__ void ld4_h(const unsigned short* p, int64_t w, int sh
 }
 
 template <bool kBf16>
-__global__ void __launch_bounds__(kShortThreads, 16) short_fused_kernel(
+__global__ void __launch_bounds__(kShortThreads, 2048 / kShortThreads) short_fused_kernel(
     const __grid_constant__ Args a, int32_t own_lo, uint32_t ctas_per_owner,
     uint32_t quads_per_owner) {
   __shared__ StepScalars sh_s;
+  __shared__ ScalerSnap sh_snap;
   __shared__ int sh_last;
   pdl_begin();
-  short_step_scalars(a, &sh_s);
+  short_step_scalars(a, &sh_s, &sh_snap);
   // the CTA's owner (uniform); 32-bit quad indices: the host takes this
   // kernel for at most kShortMaxElems elements
   const uint32_t o = blockIdx.x / ctas_per_owner;
@@ -1758,8 +1817,8 @@ __global__ void __launch_bounds__(kShortThreads, 16) short_fused_kernel(
   }
   __syncthreads();
   const StepScalars s = sh_s;
+  bool raised = false;
   if (!s.skip && n > 0) {
-    bool raised = false;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (e < n) {
@@ -1793,17 +1852,29 @@ __global__ void __launch_bounds__(kShortThreads, 16) short_fused_kernel(
       }
     }
   }
-  // the step's bookkeeping, once, by the last CTA to finish
-  __syncthreads();
+  // The step's bookkeeping, once, by the last CTA to finish. The CTA count
+  // and the number of CTAs that saw a non-finite gradient share one word
+  // (low and high 16 bits; at most 2^18 / kShortThreads + 4 CTAs), so the
+  // last CTA learns the step's vote from its own atomic: together with the
+  // pending word read at the start (a vote of an earlier launch) it is the
+  // pending word at the end. The scaler's other fields were read at the
+  // start too (nothing else writes them during the step), so the
+  // bookkeeping is stores only. The fence before the count orders this
+  // CTA's parameter stores before an overflowed step's re-cast.
+  const int cta_raised = __syncthreads_or(raised ? 1 : 0);
   if (threadIdx.x == 0) {
     __threadfence();
-    const uint32_t done = atomicAdd(&a.scaler->finish_count, 1u);
-    sh_last = done == gridDim.x - 1;
-    if (sh_last) __threadfence();
+    const uint32_t old =
+        atomicAdd(&a.scaler->finish_count, cta_raised ? kShortVoteUnit + 1u : 1u);
+    const bool last = (old & (kShortVoteUnit - 1u)) == gridDim.x - 1;
+    const bool ov = (old >> 16) != 0 || cta_raised || sh_snap.pending != 0;
+    sh_last = last ? (ov ? 2 : 1) : 0;
   }
   __syncthreads();
   if (!sh_last) return;
-  if (!s.skip && *reinterpret_cast<volatile uint32_t*>(&a.scaler->pending)) {
+  const bool ov = sh_last == 2;
+  if (!s.skip && ov) {
+    __threadfence();  // the other CTAs' parameter stores come before the re-cast's
     // re-cast every owner's parameters from the kept set, four quads in
     // flight per thread
     const uint32_t qpo = quads_per_owner;
@@ -1847,8 +1918,7 @@ __global__ void __launch_bounds__(kShortThreads, 16) short_fused_kernel(
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    __threadfence();
-    step_bookkeeping(a.scaler, a.beta1, a.beta2, a.bk_dynamic, a.bk_growth, a.bk_flip);
+    bookkeeping_store(a.scaler, sh_snap, ov, a.bk_dynamic, a.bk_growth, a.bk_flip);
     a.scaler->finish_count = 0;
   }
 }
@@ -2395,13 +2465,15 @@ int seg_range(const zero_plan* p, int32_t bucket, int32_t rank_lo, int32_t rank_
 constexpr int64_t kFoldMaxElems = int64_t(1) << 22;
 
 // Fused steps over at most kShortMaxElems elements of at most kShortMaxRanks
-// replicas, without micro-batch accumulators, run short_fused_kernel (small
-// CTAs, 16 per SM) instead of the pipelined pass. Measured on GB300, cold,
-// CUDA events: 1M parameters at N = 4 18.4 against 20.5 us, 100k at N = 4
-// 14.3 against 14.5 us; at N = 8 (500k), N = 64 (1M) and with accumulators
-// the pipelined pass was as fast or faster, so they keep it.
+// replicas, without micro-batch accumulators, run short_fused_kernel (one
+// wave of 256-thread CTAs) instead of the pipelined pass. Measured on GB300,
+// cold, CUDA events, short kernel against pipelined pass: 1M parameters at
+// N = 4 16.4 against 20.9 us, N = 8 18.5 against 20.9, N = 16 22.7 against
+// 24.7; the pipelined pass was faster at N = 64 (48 against 55 us for 1M)
+// and from 2M elements on (2M at N = 8 a tie, 4M at N = 4 37 against 40),
+// and with accumulators, so those keep it.
 constexpr int64_t kShortMaxElems = int64_t(1) << 20;
-constexpr int32_t kShortMaxRanks = 4;
+constexpr int32_t kShortMaxRanks = 16;
 
 int launch_short(const zero_plan* p, Args& a, int32_t rank_lo, int32_t rank_hi,
                  cudaStream_t st) {
@@ -2411,6 +2483,7 @@ int launch_short(const zero_plan* p, Args& a, int32_t rank_lo, int32_t rank_hi,
   a.wend = static_cast<int64_t>(rank_hi) * S - a.wbase;
   a.bucket_elems = p->info.bucket_elems;
   const dim3 grid(cpo * static_cast<uint32_t>(rank_hi - rank_lo));
+  if (grid.x >= kShortVoteUnit) return ZERO_ERANGE;  // the CTA count shares a word with the vote
   const cudaError_t e =
       p->info.grad_dtype == ZERO_BF16
           ? launch_pdl(short_fused_kernel<true>, grid, dim3(kShortThreads), 0, st, a, rank_lo,

@@ -392,7 +392,7 @@ ZERO_API int zero_step(const zero_plan* plan, int32_t rank_lo, int32_t rank_hi,
  * pass is one launch over at most 2^22 elements folds the finish into the
  * pass: the last CTA to finish does the bookkeeping and, if the step
  * overflowed, re-casts the parameters; one launch instead of two. At most
- * 2^20 elements with N <= 4 and one micro-batch it runs a kernel without the
+ * 2^20 elements with N <= 16 and one micro-batch it runs a kernel without the
  * copy pipeline, measured faster there.)
  * zero_step_update launches the update kernel of the chosen path (fused or
  * two-pass) and nothing else. zero_step_finish re-casts the parameters from

@@ -118,9 +118,22 @@ def report(wl, step, mode, n_compared, dev, orc, got, want, flags_equal):
         f.write(json.dumps(rec) + "\n")
 
 
-def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True, n_sets=None):
-    """Full element-wise comparison over every step of `wl`. Returns the
-    per-step max relative errors for reporting."""
+def set_step_count(g, t0):
+    """Put the group's scaler at step t0, as t0 good steps would leave it:
+    the beta powers formed by t0 successive fp64 products."""
+    dev = g.read_scaler()
+    p1 = p2 = 1.0
+    for _ in range(t0):
+        p1 *= g.wl.beta1
+        p2 *= g.wl.beta2
+    dev.t, dev.beta1_pow, dev.beta2_pow = t0, p1, p2
+    g.scaler.copy_(torch.frombuffer(bytearray(bytes(dev)), dtype=torch.uint8))
+    return p1, p2
+
+
+def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True, n_sets=None, t0=0):
+    """Full element-wise comparison over every step of `wl` (from step t0 + 1
+    when t0 > 0). Returns the per-step max relative errors for reporting."""
     g = harness.Group(wl, two_pass=two_pass, n_sets=n_sets)
     try:
         g.init_state()
@@ -131,6 +144,9 @@ def run_small(wl, per_bucket=False, two_pass=None, check_replicas=True, n_sets=N
         bf = wl.is_bf16
         hp = oracle_hp(wl)
         sc = oracle.scaler(wl.init_scale)
+        if t0:
+            set_step_count(g, t0)
+            sc.t = t0
         master = synth.master_f32(wlen, wbase, wl.seed, wl.psi)
         m = np.zeros(wlen, F32)
         v = np.zeros(wlen, F32)

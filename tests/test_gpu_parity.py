@@ -488,9 +488,13 @@ def test_out_of_phase_windows_and_buckets(rank_lo, rank_hi, bucket, per_bucket, 
     (4, 4 * 30_001 - 1, True, 1.0, False, 1, 3, 0, None),       # a window of two owners
     (1, 1_000_000, True, 1.0, False, 0, 1, 0, None),
     (4, 4 * 30_002, False, 3000.0, True, 0, 4, 0, (2, 2, 70_001, 0x7C00)),  # overflow, re-cast
+    (8, 8 * 30_001 - 3, True, 1.0, False, 0, 8, 0, None),
+    (16, 16 * 20_001 - 5, False, 1024.0, False, 0, 16, 30_001, None),
+    (16, 16 * 20_003, True, 1.0, False, 3, 11, 0, None),          # owners 3..10 of 16
+    (12, 12 * 20_002, False, 1000.0, True, 0, 12, 0, (3, 11, 12 * 20_002 - 1, 0xFC00)),
 ])
 def test_short_steps(n, psi, bf16, scale, dynamic, lo, hi, bucket, inject):
-    """Fused steps over at most 2^20 elements at N <= 4 without micro-batch
+    """Fused steps over at most 2^20 elements at N <= 16 without micro-batch
     accumulators run the short-step kernel (one wave of small CTAs, each CTA
     inside one owner's slice). Every shard phase against the 16-byte grid,
     loss scales whose product with N is and is not a power of two (two ways
@@ -500,4 +504,26 @@ def test_short_steps(n, psi, bf16, scale, dynamic, lo, hi, bucket, inject):
                     dynamic_scale=dynamic, steps=3, rank_lo=lo, rank_hi=hi, inject=inject)
     stats, dev, orc = run_small(wl, two_pass=False)
     if inject is not None:
-        assert dev.n_skipped == 1 and dev.scale == 1500.0
+        assert dev.n_skipped == 1 and dev.scale == scale / 2
+
+
+@pytest.mark.parametrize("t0", [1000, 6800, 100_000, 720_000, 2_000_000])
+@pytest.mark.parametrize("n,two_pass", [(4, False), (8, False), (4, True)])
+def test_bias_corrections_late_in_training(t0, n, two_pass):
+    """Steps t0 + 1 and t0 + 2, with the scaler's beta powers as t0 good
+    steps leave them: the bias corrections come from the integer form of
+    the fp64 product and difference while the powers are normal, from the
+    fp64 pipe once beta1^t (t0 >= 6800) or beta2^t (t0 >= 720,000) has
+    become subnormal or zero. Short-step kernel (N = 4, fused), pipelined
+    fused pass (N = 8) and update pass (two-pass), against the checker
+    element by element; the stored powers continue the fp64 product chain
+    bit for bit."""
+    wl = W.Workload("late", [70_001], n, 0, True, 81, 1e-3, steps=2,
+                    max_grad_norm=0.5 if two_pass else 0.0)
+    stats, dev, orc = run_small(wl, two_pass=two_pass, t0=t0)
+    p1 = p2 = 1.0
+    for _ in range(t0 + 2):
+        p1 *= wl.beta1
+        p2 *= wl.beta2
+    assert dev.t == t0 + 2
+    assert dev.beta1_pow == p1 and dev.beta2_pow == p2
