@@ -1681,7 +1681,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) bulk_kernel(const __grid_cons
 // are the same bits. The last CTA to finish does the step's bookkeeping,
 // after re-casting the parameters from the kept state set when the step
 // overflowed. No CTA waits for another.
-constexpr int kShortThreads = 256;  // 8 CTAs per SM: half as many counting at the end as with 128
+// 256 threads, 8 CTAs per SM: half as many CTAs count at the end as with 128 (at least 128:
+// threads 0, 32, 64 and 96 form the step scalars)
+constexpr int kShortThreads = 256;
 constexpr int kShortChunk = 4;  // replicas whose loads are in flight together
 constexpr uint32_t kShortVoteUnit = 1u << 16;  // finish_count: CTAs below, votes above
 
