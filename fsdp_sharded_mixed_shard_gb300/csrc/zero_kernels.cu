@@ -28,6 +28,12 @@
  *                             a cross-process exchange, and their import).
  *   scaler_finish_kernel      loss-scale / skip / step-count bookkeeping (one
  *                             thread).
+ *   short_fused_kernel        a whole fused step of at most 2^20 elements at
+ *                             N <= 16: one wave of 256-thread CTAs without
+ *                             the copy pipeline, each thread four elements,
+ *                             the bookkeeping in the last CTA.
+ *   ring_hop_kernel           one rank's part of one hop of the reduce-scatter
+ *                             when the ranks are separate processes.
  *
  * Work decomposition: the owned elements are cut into segments (one bucket of
  * one rank) and each segment into tiles of ZERO_TILE_ELEMS elements. A
@@ -162,16 +168,6 @@ __device__ __forceinline__ float widen(uint32_t h16) {
 }
 
 template <bool kBf16>
-__device__ __forceinline__ void widen8(const uint4& w, float (&x)[8]) {
-  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x[2 * k] = widen<kBf16>(u[k] & 0xFFFFu);
-    x[2 * k + 1] = widen<kBf16>(u[k] >> 16);
-  }
-}
-
-template <bool kBf16>
 __device__ __forceinline__ uint16_t narrow(float x) {
   if constexpr (kBf16) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -199,11 +195,6 @@ __device__ __forceinline__ void load8f(const float* p, float (&x)[8]) {
   float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
   x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
-__device__ __forceinline__ void store8f(float* p, const float (&x)[8]) {
-  __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
-  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(x[4], x[5], x[6], x[7]));
 }
 
 // One AdamW update ("Training models too big for one GPU: ZeRO & FSDP",
