@@ -44,6 +44,9 @@ def cases():
                                                          13, 1e-3, steps=2, n_micro=3))
     yield "shard_4_mod_8_fused_n64", dict(wl=W.Workload("s4", [64 * 3_004], 64, 0, True, 11,
                                                         1e-3, steps=2))
+    yield "short_step_overflow_recast_n12", dict(wl=W.Workload(
+        "sov", [12 * 20_002], 12, 0, False, 17, 1e-3, init_scale=1000.0, dynamic_scale=True,
+        steps=3, inject=(2, 11, 12 * 20_002 - 1, 0xFC00)))
 
 
 def gather_case():

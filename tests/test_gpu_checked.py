@@ -1,7 +1,8 @@
 """The checked build (libzero_checked.so: every kernel tests the memory ranges
 it touches) on parity cases that cover fused and two-pass paths, both
 formats, 8 to 64 ranks, a rank subset with its own window, micro-batches,
-the scalar head/tail paths, the unit all-gather / shard at every 16-byte
+the scalar head/tail paths, the short-step kernel with an overflowed step's
+re-cast, the unit all-gather / shard at every 16-byte
 phase and the norm entry points (workspace, no-allocation, export / import):
 results still match the checker and no kernel records a violation;
 the planted self-test violation is reported."""
@@ -33,8 +34,9 @@ def test_checked_build_records_no_violation():
     assert got["selftest"]["first"] == (1 << 48) | 42
     assert got["library"]["loaded"].endswith("libzero_checked.so")
     cases = [x for x in lines if x["case"] not in ("selftest", "library")]
-    assert len(cases) == 13
+    assert len(cases) == 14
     assert {"odd_shard_two_pass_n8", "shard_4_mod_8_fused_n64", "odd_shard_micro_fused_n8",
-            "random_shapes_24", "norm_entries"} <= {x["case"] for x in cases}
+            "random_shapes_24", "norm_entries", "short_step_overflow_recast_n12"} <= \
+        {x["case"] for x in cases}
     for x in cases:
         assert x["violations"] == 0, x

@@ -527,3 +527,32 @@ def test_bias_corrections_late_in_training(t0, n, two_pass):
         p2 *= wl.beta2
     assert dev.t == t0 + 2
     assert dev.beta1_pow == p1 and dev.beta2_pow == p2
+
+
+@pytest.mark.parametrize("n,psi,two_pass", [(4, 90_001, False), (64, 64 * 3_001, False),
+                                            (8, 120_007, True)])
+def test_state_index_outside_the_sets_is_a_device_error(n, psi, two_pass):
+    """A scaler whose state index names no state set (a caller's corrupted or
+    hand-written scaler): the step sets ZERO_DEVERR_STATE_INDEX in the
+    scaler's error word and writes neither state set nor the parameters.
+    Short-step kernel (N = 4), pipelined fused pass (N = 64) and the
+    two-pass update (N = 8, clip)."""
+    wl = W.Workload("badidx", [psi], n, 0, True, 91, 1e-3, steps=1,
+                    max_grad_norm=0.5 if two_pass else 0.0)
+    g = harness.Group(wl)
+    try:
+        g.init_state()
+        g.gen_grads(1)
+        sc = g.read_scaler()
+        sc.state_index = 5
+        g.scaler.copy_(torch.frombuffer(bytearray(bytes(sc)), dtype=torch.uint8))
+        torch.cuda.synchronize()
+        state0, flat0 = g.state.clone(), g.flat.clone()
+        g.step()
+        torch.cuda.synchronize()
+        dev = g.read_scaler()
+        assert dev.error == 1  # ZERO_DEVERR_STATE_INDEX
+        assert torch.equal(g.state.view(torch.int32), state0.view(torch.int32))
+        assert torch.equal(g.flat, flat0)
+    finally:
+        g.close()
