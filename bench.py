@@ -125,6 +125,13 @@ def needs_flush(wl, path):
     return step_bytes(wl, path) < 2 * L2_BYTES
 
 
+def run_config(wl, path, world):
+    """The line's `config`: the workload and how its ranks are placed (the
+    same for both arms)."""
+    return dict(config_of(wl, path), parallelism="%d simulated ranks per GPU x %d GPUs"
+                % (wl.n_ranks, world))
+
+
 def config_of(wl, path):
     psip = wl.psi + (-wl.psi) % wl.n_ranks
     lo, hi = wl.ranks
@@ -513,8 +520,7 @@ def run_libzero(args, rank, world, dist):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic: seeded counter-based generator (SplitMix64 + Irwin-Hall normal), "
                     "same replicas every timed step",
-            "config": dict(config_of(wl, path), parallelism="%d simulated ranks per GPU x %d GPUs"
-                           % (N, world)),
+            "config": run_config(wl, path, world),
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * K,
             "clocks": clk, "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
             "phase_events": "per-kernel CUDA events on %d of %d timed steps (%s)"
@@ -869,7 +875,8 @@ def run_reference(args):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic: seeded counter-based generator", "config": config_of(wl, path),
+            "data": "synthetic: seeded counter-based generator",
+            "config": run_config(wl, path, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,

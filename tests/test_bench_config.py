@@ -42,3 +42,14 @@ def test_traffic_figures_survive_comment_edits_only():
     c = "int f(int x) {\n  return x + 2;\n}\n"
     assert bench.code_sha(a) == bench.code_sha(b)
     assert bench.code_sha(a) != bench.code_sha(c)
+
+
+def test_both_arms_report_the_same_config():
+    """The libzero arm and the reference (checker) arm build their `config`
+    through one function, so the driver can match the two lines."""
+    import inspect
+    cfg = bench.run_config(W.FLAT_1P5B, "two_pass", 1)
+    assert cfg == dict(bench.config_of(W.FLAT_1P5B, "two_pass"),
+                       parallelism="8 simulated ranks per GPU x 1 GPUs")
+    assert "run_config(" in inspect.getsource(bench.run_reference)
+    assert "run_config(" in inspect.getsource(bench.run_libzero)
