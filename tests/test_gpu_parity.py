@@ -556,3 +556,22 @@ def test_state_index_outside_the_sets_is_a_device_error(n, psi, two_pass):
         assert torch.equal(g.flat, flat0)
     finally:
         g.close()
+
+
+@pytest.mark.parametrize("beta1,beta2", [(0.95, 0.98), (0.5, 0.75), (0.8, 0.9999)])
+@pytest.mark.parametrize("t0", [0, 37, 5000])
+@pytest.mark.parametrize("n,two_pass", [(4, False), (8, True)])
+def test_bias_corrections_other_betas(beta1, beta2, t0, n, two_pass):
+    """Betas other than the workloads' 0.9 / 0.999, from several step counts:
+    the bias corrections' integer form on the device (and its fp64 fallback
+    once a power is subnormal: 0.5^5000) against the checker's fp64 products,
+    element by element, and the stored powers against the fp64 chain."""
+    wl = W.Workload("betas", [50_003], n, 0, False, 93, 1e-3, init_scale=256.0, steps=2,
+                    beta1=beta1, beta2=beta2, max_grad_norm=0.5 if two_pass else 0.0)
+    stats, dev, orc = run_small(wl, two_pass=two_pass, t0=t0)
+    p1 = p2 = 1.0
+    for _ in range(t0 + 2):
+        p1 *= beta1
+        p2 *= beta2
+    assert dev.t == t0 + 2
+    assert dev.beta1_pow == p1 and dev.beta2_pow == p2
