@@ -73,15 +73,17 @@ def test_flat_fp16_inject_fused_skip_recast():
     assert dev.t == 2 and dev.scale == 32768.0
 
 
-@pytest.mark.parametrize("n_micro", [1, 2])
-def test_folded_finish_equals_two_launches(n_micro):
-    """zero_step on a small fused step is one launch (the last CTA does the
-    bookkeeping, and on an overflow re-casts the parameters alone);
-    zero_step_update + zero_step_finish is two. Same state, parameters and
-    scaler after every step, bit for bit, through a skipped step."""
+@pytest.mark.parametrize("n,n_micro", [(4, 1), (4, 2), (16, 1)])
+def test_folded_finish_equals_two_launches(n, n_micro):
+    """zero_step on a small fused step is one launch (the short-step kernel
+    without micro-batches, the pipelined pass with them; the last CTA does
+    the bookkeeping, and on an overflow re-casts the parameters alone);
+    zero_step_update + zero_step_finish is two launches of the pipelined
+    pass and the finish. Same state, parameters and scaler after every step,
+    bit for bit, through a skipped step."""
     import fsdp_sharded_mixed_shard_gb300 as Z
-    psi = 4 * 50_001 - 1
-    wl = W.Workload("fold", [psi], 4, 0, False, 24, 1e-4, init_scale=4096.0,
+    psi = n * 50_001 - 1
+    wl = W.Workload("fold", [psi], n, 0, False, 24, 1e-4, init_scale=4096.0,
                     dynamic_scale=True, steps=4, n_micro=n_micro,
                     inject=(2, 1, psi // 2, W.FP16_POS_INF))
     a, b = harness.Group(wl), harness.Group(wl)
@@ -98,10 +100,10 @@ def test_folded_finish_equals_two_launches(n_micro):
             m, v, w = b._state_ptrs(0), b._state_ptrs(1), b._state_ptrs(2)
             acc = b.accum_ptrs() if n_micro > 1 else None
             b.flags.zero_()
-            Z.zero_step_update_accum(b.plan, 0, 4, m, v, w, 2, None, b.rep_ptrs(), acc, n_micro,
+            Z.zero_step_update_accum(b.plan, 0, n, m, v, w, 2, None, b.rep_ptrs(), acc, n_micro,
                                      0, b.flat.data_ptr(), b.hp, b.scaler.data_ptr(),
                                      b.flags.data_ptr(), b.sptr)
-            Z.zero_step_finish(b.plan, 0, 4, m, 2, None, 0, b.flat.data_ptr(), b.hp,
+            Z.zero_step_finish(b.plan, 0, n, m, 2, None, 0, b.flat.data_ptr(), b.hp,
                                b.scaler.data_ptr(), b.sptr)
             torch.cuda.synchronize()
             assert bytes(a.scaler.cpu().numpy()) == bytes(b.scaler.cpu().numpy()), step
